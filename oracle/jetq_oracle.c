@@ -1,0 +1,511 @@
+/*
+ * jetq oracle: a plain, slow, obviously-correct CPU statement of the
+ * block-scaled FP8 (E4M3) quantize-and-GEMM precision flow.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the library calls this code; only the
+ * tests, __graft_entry__.smoke() and bench.py's CPU-baseline leg load it.  It
+ * shares no code, header, table or constant with the CUDA path.
+ *
+ * Sources (web pages, cited by title and section):
+ *   [JR]  "Jet-RL: Enabling On-Policy FP8 Reinforcement Learning with Unified
+ *         Training and Rollout Precision Flow" (paper-graph-ui explainer),
+ *         section "GEMM Quantization: Granularity, Layout, and Kernel Design"
+ *         and "The Three GEMM Operations and Their Quantization Configuration".
+ *   [JR2] the papercache summary of the same paper, section 2.1 (quantizer
+ *         equation: X^ = round(X / S_X), S_X = max|X| / Delta_max,
+ *         Delta_max = 448 for E4M3), section 2.2 (the shapes of FProp, WGrad,
+ *         DGrad) and section 4.2 (1x128 activations, 128x128 weights, the
+ *         WGrad operands grouped along the token axis).
+ *   [MB]  the Miles "Blackwell-native RL recipes" post, MXFP8 section
+ *         (32 consecutive E4M3 values share one E8M0 scale, rounded up so the
+ *         block maximum is not clipped; row-wise and column-wise copies are
+ *         each quantized from full precision).
+ *
+ * Readings where the pages are silent or garbled (each is listed in the
+ * design notes):
+ *   - round() is round-to-nearest, ties to even, saturating at +-448.
+ *   - the scale is an FP32 number S = fl32(amax / 448) and the quotient is
+ *     taken in FP32, q = E4M3(fl32(x / S)): two roundings, in that order.
+ *   - an all-zero group has S = 0 and every code 0x00 (MX: scale byte 127).
+ *   - column groups never cross segment bounds; a partial group's amax
+ *     covers only its valid rows; each segment of the column copy starts at a
+ *     multiple of the group size and its padding codes are 0x00.
+ *
+ * Build: plain C99, -O2 -ffp-contract=off, no fast-math.  Arithmetic is
+ * IEEE binary32/binary64 as written; FLT_EVAL_METHOD must be 0.
+ */
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#if FLT_EVAL_METHOD != 0
+#error "the oracle needs FLT_EVAL_METHOD == 0 (float arithmetic rounded to float)"
+#endif
+
+#define E4M3_MAX 448.0
+
+/* ------------------------------------------------------------------------ */
+/* BF16 and FP32 bit views                                                  */
+/* ------------------------------------------------------------------------ */
+
+static float bf16_value(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16; /* bf16 is the top half of a binary32 */
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* ------------------------------------------------------------------------ */
+/* E4M3 ("FN" variant of the OCP 8-bit float spec cited by [JR2] 2.1):      */
+/* sign bit, 4 exponent bits with bias 7, 3 mantissa bits, no infinities,   */
+/* S.1111.111 is NaN, largest finite magnitude 1.75 * 2^8 = 448.            */
+/* ------------------------------------------------------------------------ */
+
+double jo_e4m3_decode(uint8_t code)
+{
+    int sign = code >> 7;
+    int e = (code >> 3) & 0xF;
+    int m = code & 0x7;
+    double mag;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        mag = ldexp((double)m, -9); /* subnormal: m/8 * 2^(1-7) */
+    else
+        mag = ldexp(1.0 + m / 8.0, e - 7);
+    return sign ? -mag : mag;
+}
+
+/*
+ * Nearest finite E4M3 value to v, ties to the code with an even mantissa
+ * (the last code bit), magnitudes above 448 saturated to 448, sign of zero
+ * kept.  Positive finite codes 0x00..0x7E are increasing in value, so the
+ * search is over that ordered list; the comparison is against the exact
+ * midpoint of two neighbours (a binary64 number), so no rounding enters.
+ */
+uint8_t jo_e4m3_encode(double v)
+{
+    uint8_t sign;
+    double a, mid;
+    int lo, hi;
+    if (isnan(v))
+        return 0x7F;
+    sign = signbit(v) ? 0x80 : 0x00;
+    a = fabs(v);
+    lo = 0;
+    hi = 0x7E;
+    while (lo < hi) { /* largest code c with decode(c) <= a */
+        int c = (lo + hi + 1) / 2;
+        if (jo_e4m3_decode((uint8_t)c) <= a)
+            lo = c;
+        else
+            hi = c - 1;
+    }
+    if (lo == 0x7E)
+        return (uint8_t)(sign | 0x7E); /* saturate */
+    mid = 0.5 * (jo_e4m3_decode((uint8_t)lo) + jo_e4m3_decode((uint8_t)(lo + 1)));
+    if (a < mid)
+        return (uint8_t)(sign | lo);
+    if (a > mid)
+        return (uint8_t)(sign | (lo + 1));
+    return (uint8_t)(sign | ((lo & 1) ? lo + 1 : lo)); /* tie: even mantissa */
+}
+
+/* ------------------------------------------------------------------------ */
+/* FP32-scale group quantizer, [JR2] 2.1 and [JR] "GEMM Quantization":      */
+/*   S = fl32(amax / 448),  q = E4M3(fl32(x / S)).                          */
+/* ------------------------------------------------------------------------ */
+
+static float scale_of(float amax)
+{
+    return amax / (float)E4M3_MAX; /* binary32 division, round to nearest */
+}
+
+static uint8_t quant_value(float x, float s)
+{
+    if (s == 0.0f)
+        return 0x00; /* all-zero group */
+    return jo_e4m3_encode((double)(x / s)); /* x / s rounded to binary32 */
+}
+
+/*
+ * Row-wise groups of `gs` consecutive columns ([JR] 1x128 activation
+ * quantization: one scale per token and 128-channel group).
+ *   x  : bf16 [rows x cols], row stride ldx (elements)
+ *   q  : codes [rows x cols], row stride ldq (bytes)
+ *   s  : scales [cols/gs x rows], group-major: s[g * rows + r]
+ */
+void jo_quant_rowgroups(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, int64_t gs,
+                        uint8_t *q, int64_t ldq, float *s)
+{
+    int64_t r, g, j;
+    for (r = 0; r < rows; ++r) {
+        for (g = 0; g < cols / gs; ++g) {
+            float amax = 0.0f, sc;
+            for (j = 0; j < gs; ++j) {
+                float v = fabsf(bf16_value(x[r * ldx + g * gs + j]));
+                if (v > amax)
+                    amax = v;
+            }
+            sc = scale_of(amax);
+            s[g * rows + r] = sc;
+            for (j = 0; j < gs; ++j)
+                q[r * ldq + g * gs + j] = quant_value(bf16_value(x[r * ldx + g * gs + j]), sc);
+        }
+    }
+}
+
+/* padded start of every segment in the column copy: pad[e] = sum_{j<e} ceil(n_j/gs)*gs */
+static void padded_starts(const int64_t *off, int nseg, int64_t gs, int64_t *pad)
+{
+    int e;
+    pad[0] = 0;
+    for (e = 0; e < nseg; ++e) {
+        int64_t n = off[e + 1] - off[e];
+        pad[e + 1] = pad[e] + ((n + gs - 1) / gs) * gs;
+    }
+}
+
+/* total padded length of the column copy (a multiple of gs) */
+int64_t jo_colcopy_length(const int64_t *off, int nseg, int64_t gs)
+{
+    int64_t *pad = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nseg + 1));
+    int64_t total;
+    padded_starts(off, nseg, gs, pad);
+    total = pad[nseg];
+    free(pad);
+    return total;
+}
+
+/*
+ * Column-wise groups of `gs` consecutive rows, stored transposed ([JR2] 4.2:
+ * the WGrad operands are grouped 128 along the token axis; [MB]: the
+ * column-wise copy is quantized from full precision).
+ *   x    : bf16 [rows x cols], row stride ldx
+ *   off  : segment bounds, off[0] = 0 <= ... <= off[nseg] = rows
+ *   qc   : codes [cols x ldqc]; segment e occupies columns pad[e] .. ,
+ *          padding codes inside a segment's last group are 0x00
+ *   sc   : scales [P/gs x cols], sc[(pad[e]/gs + t) * cols + c]
+ */
+void jo_quant_colgroups(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, int64_t gs,
+                        const int64_t *off, int nseg, uint8_t *qc, int64_t ldqc, float *sc)
+{
+    int64_t *pad = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nseg + 1));
+    int e;
+    (void)rows;
+    padded_starts(off, nseg, gs, pad);
+    for (e = 0; e < nseg; ++e) {
+        int64_t n_e = off[e + 1] - off[e];
+        int64_t t, c, i;
+        for (t = 0; t * gs < n_e; ++t) {
+            int64_t r0 = off[e] + t * gs;
+            int64_t valid = (n_e - t * gs < gs) ? n_e - t * gs : gs;
+            int64_t col0 = pad[e] + t * gs;
+            for (c = 0; c < cols; ++c) {
+                float amax = 0.0f, s;
+                for (i = 0; i < valid; ++i) {
+                    float v = fabsf(bf16_value(x[(r0 + i) * ldx + c]));
+                    if (v > amax)
+                        amax = v;
+                }
+                s = scale_of(amax);
+                sc[(col0 / gs) * cols + c] = s;
+                for (i = 0; i < gs; ++i)
+                    qc[c * ldqc + col0 + i] =
+                        (i < valid) ? quant_value(bf16_value(x[(r0 + i) * ldx + c]), s) : 0x00;
+            }
+        }
+    }
+    free(pad);
+}
+
+/*
+ * Square blocks of bs x bs ([JR] 128x128 per-block weight quantization,
+ * S_W(i,j) = max|W_tile(i,j)| / 448, W^ = round(W / S_W)).
+ *   w  : bf16 [rows x cols], row stride ldw
+ *   q  : codes [rows x cols] (dense), s : [rows/bs x cols/bs] row-major
+ *   qT : optional transposed codes [cols x rows], sT : [cols/bs x rows/bs]
+ *        ([JR]: for DGrad "only a transpose" of the quantized weight).
+ */
+void jo_quant_blocks(const uint16_t *w, int64_t rows, int64_t cols, int64_t ldw, int64_t bs,
+                     uint8_t *q, float *s, uint8_t *qT, float *sT)
+{
+    int64_t bi, bj, i, j;
+    for (bi = 0; bi < rows / bs; ++bi) {
+        for (bj = 0; bj < cols / bs; ++bj) {
+            float amax = 0.0f, sc;
+            for (i = 0; i < bs; ++i)
+                for (j = 0; j < bs; ++j) {
+                    float v = fabsf(bf16_value(w[(bi * bs + i) * ldw + bj * bs + j]));
+                    if (v > amax)
+                        amax = v;
+                }
+            sc = scale_of(amax);
+            s[bi * (cols / bs) + bj] = sc;
+            if (sT)
+                sT[bj * (rows / bs) + bi] = sc;
+            for (i = 0; i < bs; ++i)
+                for (j = 0; j < bs; ++j) {
+                    int64_t r = bi * bs + i, c = bj * bs + j;
+                    uint8_t code = quant_value(bf16_value(w[r * ldw + c]), sc);
+                    q[r * cols + c] = code;
+                    if (qT)
+                        qT[c * rows + r] = code;
+                }
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* MXFP8 ([MB], MXFP8 section): blocks of 32 consecutive values share one   */
+/* E8M0 scale 2^e, "rounded up" so the block maximum is not clipped:        */
+/* e is the smallest integer with amax <= 448 * 2^e, clamped to [-127,127]; */
+/* the scale byte is e + 127 and q = E4M3(x * 2^-e) (the product is exact   */
+/* in binary64, so there is exactly one rounding).  All-zero block: byte    */
+/* 127 (scale 1) and codes 0x00.                                            */
+/* ------------------------------------------------------------------------ */
+
+int jo_e8m0_exponent(float amax)
+{
+    int e;
+    double a = (double)amax;
+    if (a == 0.0)
+        return 0;
+    /* frexp: a = f * 2^k with f in [0.5, 1); start from a bound below the answer */
+    {
+        int k;
+        (void)frexp(a, &k);
+        e = k - 10; /* 448 * 2^(k-10) < 2^(k-1) <= a, so the answer is larger */
+    }
+    while (a > E4M3_MAX * ldexp(1.0, e)) /* exact comparisons in binary64 */
+        ++e;
+    if (e < -127)
+        e = -127;
+    if (e > 127)
+        e = 127;
+    return e;
+}
+
+static uint8_t mx_value(float x, int e, int zero_block)
+{
+    if (zero_block)
+        return 0x00;
+    return jo_e4m3_encode((double)x * ldexp(1.0, -e));
+}
+
+/*
+ * Row-wise MX blocks of `bs` consecutive columns.
+ *   x : bf16 [rows x cols] stride ldx ; q : [rows x cols] stride ldq
+ *   e8: logical scale bytes [rows x cols/bs] (row-major)
+ */
+void jo_quant_mx_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, int64_t bs,
+                      uint8_t *q, int64_t ldq, uint8_t *e8)
+{
+    int64_t r, g, j;
+    for (r = 0; r < rows; ++r) {
+        for (g = 0; g < cols / bs; ++g) {
+            float amax = 0.0f;
+            int e;
+            for (j = 0; j < bs; ++j) {
+                float v = fabsf(bf16_value(x[r * ldx + g * bs + j]));
+                if (v > amax)
+                    amax = v;
+            }
+            e = jo_e8m0_exponent(amax);
+            e8[r * (cols / bs) + g] = (uint8_t)(e + 127);
+            for (j = 0; j < bs; ++j)
+                q[r * ldq + g * bs + j] = mx_value(bf16_value(x[r * ldx + g * bs + j]), e, amax == 0.0f);
+        }
+    }
+}
+
+/*
+ * Column-wise MX blocks of `bs` consecutive rows inside each segment, stored
+ * transposed like jo_quant_colgroups; segments start at multiples of `seg_align`
+ * (a multiple of bs) in the column copy.
+ *   qc : [cols x ldqc] ; e8 : logical scale bytes [cols x P/bs] (row-major)
+ */
+void jo_quant_mx_cols(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, int64_t bs,
+                      int64_t seg_align, const int64_t *off, int nseg, uint8_t *qc, int64_t ldqc,
+                      uint8_t *e8)
+{
+    int64_t *pad = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nseg + 1));
+    int64_t P;
+    int e;
+    (void)rows;
+    padded_starts(off, nseg, seg_align, pad);
+    P = pad[nseg];
+    for (e = 0; e < nseg; ++e) {
+        int64_t n_e = off[e + 1] - off[e];
+        int64_t t, c, i;
+        for (t = 0; t * bs < ((n_e + seg_align - 1) / seg_align) * seg_align; ++t) {
+            int64_t r0 = off[e] + t * bs;
+            int64_t valid = n_e - t * bs;
+            int64_t col0 = pad[e] + t * bs;
+            if (valid < 0)
+                valid = 0;
+            if (valid > bs)
+                valid = bs;
+            for (c = 0; c < cols; ++c) {
+                float amax = 0.0f;
+                int ex;
+                for (i = 0; i < valid; ++i) {
+                    float v = fabsf(bf16_value(x[(r0 + i) * ldx + c]));
+                    if (v > amax)
+                        amax = v;
+                }
+                ex = jo_e8m0_exponent(amax);
+                e8[c * (P / bs) + col0 / bs] = (uint8_t)(ex + 127);
+                for (i = 0; i < bs; ++i)
+                    qc[c * ldqc + col0 + i] =
+                        (i < valid) ? mx_value(bf16_value(x[(r0 + i) * ldx + c]), ex, amax == 0.0f) : 0x00;
+            }
+        }
+    }
+    free(pad);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Dequantizers: x^ = decode(q) * S, in binary64, back to the natural       */
+/* [rows x cols] layout of the tensor the copy was made from.               */
+/* ------------------------------------------------------------------------ */
+
+void jo_dequant_rowgroups(const uint8_t *q, int64_t rows, int64_t cols, int64_t ldq, int64_t gs,
+                          const float *s, double *out)
+{
+    int64_t r, c;
+    for (r = 0; r < rows; ++r)
+        for (c = 0; c < cols; ++c)
+            out[r * cols + c] = jo_e4m3_decode(q[r * ldq + c]) * (double)s[(c / gs) * rows + r];
+}
+
+void jo_dequant_colgroups(const uint8_t *qc, int64_t ldqc, const float *sc, int64_t rows, int64_t cols,
+                          int64_t gs, const int64_t *off, int nseg, double *out)
+{
+    int64_t *pad = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nseg + 1));
+    int e;
+    (void)rows;
+    padded_starts(off, nseg, gs, pad);
+    for (e = 0; e < nseg; ++e) {
+        int64_t i, c;
+        for (i = 0; i < off[e + 1] - off[e]; ++i) {
+            int64_t col = pad[e] + i; /* position in the column copy */
+            for (c = 0; c < cols; ++c)
+                out[(off[e] + i) * cols + c] =
+                    jo_e4m3_decode(qc[c * ldqc + col]) * (double)sc[(col / gs) * cols + c];
+        }
+    }
+    free(pad);
+}
+
+void jo_dequant_blocks(const uint8_t *q, int64_t rows, int64_t cols, int64_t bs, const float *s,
+                       double *out)
+{
+    int64_t r, c;
+    for (r = 0; r < rows; ++r)
+        for (c = 0; c < cols; ++c)
+            out[r * cols + c] = jo_e4m3_decode(q[r * cols + c]) * (double)s[(r / bs) * (cols / bs) + c / bs];
+}
+
+void jo_dequant_mx_rows(const uint8_t *q, int64_t rows, int64_t cols, int64_t ldq, int64_t bs,
+                        const uint8_t *e8, double *out)
+{
+    int64_t r, c;
+    for (r = 0; r < rows; ++r)
+        for (c = 0; c < cols; ++c)
+            out[r * cols + c] =
+                jo_e4m3_decode(q[r * ldq + c]) * ldexp(1.0, (int)e8[r * (cols / bs) + c / bs] - 127);
+}
+
+void jo_dequant_mx_cols(const uint8_t *qc, int64_t ldqc, const uint8_t *e8, int64_t P, int64_t rows,
+                        int64_t cols, int64_t bs, int64_t seg_align, const int64_t *off, int nseg,
+                        double *out)
+{
+    int64_t *pad = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nseg + 1));
+    int e;
+    (void)rows;
+    padded_starts(off, nseg, seg_align, pad);
+    for (e = 0; e < nseg; ++e) {
+        int64_t i, c;
+        for (i = 0; i < off[e + 1] - off[e]; ++i) {
+            int64_t col = pad[e] + i;
+            for (c = 0; c < cols; ++c)
+                out[(off[e] + i) * cols + c] =
+                    jo_e4m3_decode(qc[c * ldqc + col]) * ldexp(1.0, (int)e8[c * (P / bs) + col / bs] - 127);
+        }
+    }
+    free(pad);
+}
+
+/* ------------------------------------------------------------------------ */
+/* The three linear-layer GEMMs of [JR2] 2.2, in binary64 on dequantized    */
+/* operands given in their natural layouts:                                 */
+/*   FProp  Y[n,d]   = sum_c X[n,c]  W[d,c]      (Y = X W^T)                */
+/*   DGrad  dX[n,c]  = sum_d dY[n,d] W[d,c]      (dX = dY W)                */
+/*   WGrad  dW[d,c]  = sum_n dY[n,d] X[n,c]      (dW = dY^T X)              */
+/* Each output also gets bound = sum |term|, the scale of its rounding      */
+/* error.  `at` lists (i, j) output coordinates (count pairs); NULL means    */
+/* every output, written row-major into y / bound.                          */
+/* ------------------------------------------------------------------------ */
+
+static void dot_terms(const double *a, int64_t sa, const double *b, int64_t sb, int64_t k, double *y,
+                      double *bound)
+{
+    double acc = 0.0, mag = 0.0;
+    int64_t i;
+    for (i = 0; i < k; ++i) {
+        double t = a[i * sa] * b[i * sb];
+        acc += t;
+        mag += fabs(t);
+    }
+    *y = acc;
+    *bound = mag;
+}
+
+void jo_fprop(const double *X, const double *W, int64_t N, int64_t D, int64_t C, const int64_t *at,
+              int64_t count, double *y, double *bound)
+{
+    int64_t i;
+    if (!at) {
+        int64_t n, d;
+        for (n = 0; n < N; ++n)
+            for (d = 0; d < D; ++d)
+                dot_terms(X + n * C, 1, W + d * C, 1, C, &y[n * D + d], &bound[n * D + d]);
+        return;
+    }
+    for (i = 0; i < count; ++i)
+        dot_terms(X + at[2 * i] * C, 1, W + at[2 * i + 1] * C, 1, C, &y[i], &bound[i]);
+}
+
+void jo_dgrad(const double *dY, const double *W, int64_t N, int64_t D, int64_t C, const int64_t *at,
+              int64_t count, double *y, double *bound)
+{
+    int64_t i;
+    if (!at) {
+        int64_t n, c;
+        for (n = 0; n < N; ++n)
+            for (c = 0; c < C; ++c)
+                dot_terms(dY + n * D, 1, W + c, C, D, &y[n * C + c], &bound[n * C + c]);
+        return;
+    }
+    for (i = 0; i < count; ++i)
+        dot_terms(dY + at[2 * i] * D, 1, W + at[2 * i + 1], C, D, &y[i], &bound[i]);
+}
+
+void jo_wgrad(const double *dY, const double *X, int64_t N, int64_t D, int64_t C, const int64_t *at,
+              int64_t count, double *y, double *bound)
+{
+    int64_t i;
+    if (!at) {
+        int64_t d, c;
+        for (d = 0; d < D; ++d)
+            for (c = 0; c < C; ++c)
+                dot_terms(dY + d, D, X + c, C, N, &y[d * C + c], &bound[d * C + c]);
+        return;
+    }
+    for (i = 0; i < count; ++i)
+        dot_terms(dY + at[2 * i], D, X + at[2 * i + 1], C, N, &y[i], &bound[i]);
+}
