@@ -1,0 +1,250 @@
+/*
+ * jetq: block-scaled FP8 (E4M3) quantize-and-GEMM for one GB300 (sm_103a).
+ *
+ * One quantizer and one set of GEMMs serve both RL rollout and RL training, so
+ * the rollout forward and the training forward see bit-identical quantized
+ * operands and return bit-identical outputs ("unified precision flow",
+ * Jet-RL, section 4.1 of the papercache summary; on-policy weight sync, SkyRL
+ * FP8 post, "On-Policy FP8 weight sync").
+ *
+ * Conventions for every entry point:
+ *  - All pointers are DEVICE pointers, allocated and owned by the caller.  The
+ *    library allocates nothing, frees nothing and keeps no pointer after the
+ *    call returns.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default
+ *    stream) and the call returns without synchronizing.
+ *  - Arguments are validated on the host before anything is launched; a
+ *    failed check returns an error code and launches nothing.  Outputs are
+ *    undefined after a JETQ_ERR_CUDA return.
+ *  - Every wait inside a kernel is bounded.  A kernel that gives up records
+ *    the fact in a device error word, which jetq_check_device_error() reads.
+ *  - Codes are E4M3 bytes (OCP "FN" variant: bias 7, no infinities, largest
+ *    finite value 448).  BF16 inputs are uint16_t bit patterns.
+ *  - Row strides (ld*) are in elements of the pointed-to type and must keep
+ *    every row 16-byte aligned; base pointers must be 16-byte aligned.
+ *  - C (channels), D (output features) are multiples of 128.  N (tokens) is
+ *    any value >= 0.
+ *
+ * Quantization readings (the pages are silent or garbled on these; the
+ * oracle uses the same ones):
+ *  - FP32-scale recipe: S = fl32(amax / 448); q = E4M3_rne_satfinite(fl32(x / S)).
+ *    An all-zero group has S = 0 and codes 0x00.
+ *  - MXFP8 recipe: e = smallest integer with amax <= 448 * 2^e, clamped to
+ *    [-127, 127]; scale byte = e + 127 (E8M0); q = E4M3_rne_satfinite(x * 2^-e).
+ *    An all-zero block has scale byte 127 and codes 0x00.
+ */
+#ifndef JETQ_H
+#define JETQ_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define JETQ_API __attribute__((visibility("default")))
+#else
+#define JETQ_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    JETQ_OK = 0,
+    JETQ_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad enum */
+    JETQ_ERR_UNSUPPORTED_SHAPE = 2, /* C or D not a multiple of 128, ld too small */
+    JETQ_ERR_MISALIGNED = 3,        /* pointer or row stride not 16-byte aligned */
+    JETQ_ERR_ARCH = 4,              /* current device is not compute capability 10.3 */
+    JETQ_ERR_CUDA = 5,              /* a CUDA runtime call or a launch failed */
+    JETQ_ERR_TIMEOUT = 6            /* a kernel gave up a bounded wait (device error word) */
+} jetq_status;
+
+typedef enum {
+    JETQ_RECIPE_BLOCK128 = 0, /* 1x128 activation groups, 128x128 weight blocks, FP32 scales */
+    JETQ_RECIPE_MXFP8 = 1     /* 1x32 blocks, E8M0 power-of-two scales rounded up */
+} jetq_recipe;
+
+typedef enum {
+    JETQ_PATH_AUTO = 0,   /* DECODE when N <= 256 tokens, else TRAIN */
+    JETQ_PATH_TRAIN = 1,  /* wide tiles for large N */
+    JETQ_PATH_DECODE = 2  /* narrow tiles that spread the weight stream over every SM */
+} jetq_path;
+
+typedef enum {
+    JETQ_OUT_F32 = 0,
+    JETQ_OUT_BF16 = 1 /* round-to-nearest-even of the FP32 result */
+} jetq_out_dtype;
+
+/* Human-readable name of a status code (static storage). */
+JETQ_API const char *jetq_status_string(jetq_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+JETQ_API int jetq_version(void);
+
+/*
+ * Synchronize `stream`, then read and clear the device error word of every
+ * kernel family.  Returns JETQ_ERR_TIMEOUT if any kernel gave up a bounded
+ * wait since the last call, JETQ_ERR_CUDA if the synchronization failed.
+ */
+JETQ_API jetq_status jetq_check_device_error(void *stream);
+
+/* ======================================================================== */
+/* Layouts                                                                  */
+/* ======================================================================== */
+/*
+ * Row-wise FP32-scale copy of an [R x K] tensor (groups of 128 along K):
+ *   codes  q[r * K + k]                        (dense, K-major)
+ *   scales s[(k / 128) * R + r]                (group-major, rows contiguous)
+ *
+ * Column-wise FP32-scale copy of an [N x C] tensor (groups of 128 along N,
+ * never crossing a segment bound), stored transposed:
+ *   codes  qc[c * ldqc + p]    p = position in the column copy
+ *   scales sc[(p / 128) * C + c]
+ * Segment e (tokens off[e] .. off[e+1]-1) starts at column-copy position
+ * pad[e] = sum_{j<e} ceil(n_j / 128) * 128, so every 128-group of positions
+ * belongs to one segment.  Positions of a segment's last, partial group past
+ * its tokens hold code 0x00.  Positions from pad[nseg] up to the capacity are
+ * not written.  Capacity: jetq_colcopy_capacity(N, nseg).
+ *
+ * 128x128 weight copy of W [D x C]:
+ *   codes  q[d * C + c],  scales s[(d / 128) * (C / 128) + c / 128]
+ *   transposed copy (for DGrad): qT[c * D + d],  sT[(c / 128) * (D / 128) + d / 128]
+ *
+ * MXFP8 scale bytes of a K-major payload with R rows and K columns (one byte
+ * per row and 32 columns) are kept in 2048-byte atoms of 128 rows x 16 scale
+ * bytes, the unit the tensor-core block-scaled MMA consumes:
+ *   KA = ceil(K / 512) atoms per 128-row band
+ *   byte(r, j) at ((r / 128) * KA + j / 16) * 2048 + (r % 128) * 16 + j % 16,  j = k / 32
+ *   size = ceil(R / 128) * KA * 2048 bytes (jetq_mx_scale_bytes)
+ * Bytes for rows >= R or j >= K / 32 inside an atom are not written.
+ */
+
+/* Capacity (positions, a multiple of 128) a column copy of N tokens in nseg segments needs. */
+JETQ_API int64_t jetq_colcopy_capacity(int64_t n, int nseg);
+
+/* Bytes of the MX scale-atom array for a K-major payload of `rows` x `k`. */
+JETQ_API int64_t jetq_mx_scale_bytes(int64_t rows, int64_t k);
+
+/* ======================================================================== */
+/* Quantizers                                                               */
+/* ======================================================================== */
+
+/*
+ * Activation / gradient quantizer, FP32-scale recipe, one pass over X.
+ * Jet-RL (paper-graph-ui explainer), "GEMM Quantization": 1x128 per-group
+ * activation scales S = max|X[n, c:c+128]| / 448; papercache summary 4.2: the
+ * backward GEMMs need 1x128 and 128x1 quantizations of the same tensor, which
+ * are fused; Miles Blackwell post, MXFP8 section: both copies are quantized
+ * from full precision.
+ *
+ *   x       BF16 [n x c], row stride ldx (elements, multiple of 8)
+ *   q_row   codes [n x c] and s_row [c/128 x n]        (nullable pair: skip)
+ *   q_col   codes [c x ldq_col] and s_col [ldq_col/128 x c] (nullable pair: skip);
+ *           ldq_col >= jetq_colcopy_capacity(n, nseg), a multiple of 128
+ *   seg_offsets  device int64 [nseg + 1], 0 = off[0] <= ... <= off[nseg] = n;
+ *           NULL means one segment [0, n) (nseg is then ignored)
+ * Row-wise groups ignore segments.  Offsets are read on the device; values
+ * outside [0, n] are clamped.  n == 0 is a no-op.
+ */
+JETQ_API jetq_status jetq_quant_act_1x128(const uint16_t *x, int64_t n, int64_t c, int64_t ldx,
+                                 uint8_t *q_row, float *s_row,
+                                 uint8_t *q_col, float *s_col, int64_t ldq_col,
+                                 const int64_t *seg_offsets, int nseg, void *stream);
+
+/*
+ * Weight quantizer, 128x128 blocks (Jet-RL explainer, "GEMM Quantization":
+ * S_W(i,j) = max|W_tile(i,j)| / 448; the DGrad operand is the same FP8
+ * weight, only transposed).  Runs after every optimizer step; its output is
+ * what training and rollout both consume.
+ *
+ *   w      BF16 [d x c], row stride ldw
+ *   q, s   codes [d x c], scales [d/128 x c/128]
+ *   qT, sT transposed codes [c x d], scales [c/128 x d/128] (nullable pair)
+ */
+JETQ_API jetq_status jetq_quant_w_128x128(const uint16_t *w, int64_t d, int64_t c, int64_t ldw,
+                                 uint8_t *q, float *s, uint8_t *qT, float *sT, void *stream);
+
+/*
+ * MXFP8 quantizer (Miles Blackwell post, MXFP8 section: 32 consecutive E4M3
+ * values share one E8M0 scale rounded up; row-wise and column-wise copies are
+ * each quantized from BF16).
+ *
+ *   x        BF16 [rows x cols], row stride ldx; cols a multiple of 128
+ *   q_row    codes [rows x cols], e8_row scale atoms for (rows, cols)   (nullable pair)
+ *   q_col    codes [cols x ldq_col], e8_col scale atoms for (cols, ldq_col) (nullable pair);
+ *            segments start on multiples of 128 exactly as in the FP32-scale
+ *            column copy; whole 32-blocks past a segment's end have scale
+ *            byte 127 and codes 0x00
+ *   seg_offsets, nseg  as for jetq_quant_act_1x128
+ */
+JETQ_API jetq_status jetq_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx,
+                            uint8_t *q_row, uint8_t *e8_row,
+                            uint8_t *q_col, uint8_t *e8_col, int64_t ldq_col,
+                            const int64_t *seg_offsets, int nseg, void *stream);
+
+/* ======================================================================== */
+/* GEMMs                                                                    */
+/* ======================================================================== */
+/*
+ * The three linear-layer GEMMs (papercache summary 2.2):
+ *   FProp  Y  = X W^T    [N x D] = [N x C] [C x D]
+ *   DGrad  dX = dY W     [N x C] = [N x D] [D x C]
+ *   WGrad  dW = dY^T X   [D x C] = [D x N] [N x C]
+ * Every operand is K-major (the contraction dimension contiguous).
+ *
+ * BLOCK128 arithmetic, identical for every path and tile shape (this is what
+ * makes rollout FProp bitwise equal to training FProp):
+ *   acc = 0;  for kb = 0, 1, ... (K-blocks of 128, ascending):
+ *       P  = sum over the block of qa * qb   (tensor core, FP32, fresh accumulator)
+ *       s  = fl32(Sa[row, kb] * Sb[col, kb])
+ *       acc = fma(P, s, acc)
+ *   out = acc (F32) or bf16_rne(acc); WGrad with accumulate: out = fl32(out_old + acc).
+ * MXFP8 arithmetic: the tensor core's block-scaled MMA over all of K into one
+ * FP32 accumulator.
+ *
+ * Output stride ld* is in output elements (a multiple of 4 for F32, 8 for BF16).
+ */
+
+/*
+ * FProp.  BLOCK128: qx = row copy of X [n x c], sx [c/128 x n]; qw [d x c],
+ * sw [d/128 x c/128].  MXFP8: qx row MX copy of X, sx its scale atoms (n, c);
+ * qw row MX copy of W [d x c], sw its scale atoms (d, c).
+ */
+JETQ_API jetq_status jetq_gemm_fprop(jetq_recipe recipe,
+                            const uint8_t *qx, const void *sx,
+                            const uint8_t *qw, const void *sw,
+                            int64_t n, int64_t d, int64_t c,
+                            void *y, jetq_out_dtype y_dtype, int64_t ldy,
+                            jetq_path path, void *stream);
+
+/*
+ * DGrad.  BLOCK128: qdy = row copy of dY [n x d], sdy [d/128 x n]; qwt = the
+ * transposed weight copy [c x d], swt [c/128 x d/128].  MXFP8: qdy row MX
+ * copy of dY (n, d); qwt = column MX copy of W ([c x d], blocks of 32 along d).
+ */
+JETQ_API jetq_status jetq_gemm_dgrad(jetq_recipe recipe,
+                            const uint8_t *qdy, const void *sdy,
+                            const uint8_t *qwt, const void *swt,
+                            int64_t n, int64_t d, int64_t c,
+                            void *dx, jetq_out_dtype dx_dtype, int64_t lddx,
+                            void *stream);
+
+/*
+ * WGrad.  Both operands are column copies along the token axis with the same
+ * segment layout: qdyc [d x ldk] (scales sdyc [k/128 x d]), qxc [c x ldk]
+ * (scales sxc [k/128 x c]); k = column-copy length (a multiple of 128, the
+ * zero-padded positions contribute nothing), ldk >= k a multiple of 16.
+ * MXFP8: the same codes with scale atoms (d, k) and (c, k).
+ * dw is FP32 [d x c], stride lddw; accumulate != 0 adds into it.
+ */
+JETQ_API jetq_status jetq_gemm_wgrad(jetq_recipe recipe,
+                            const uint8_t *qdyc, const void *sdyc,
+                            const uint8_t *qxc, const void *sxc,
+                            int64_t k, int64_t ldk, int64_t d, int64_t c,
+                            float *dw, int64_t lddw, int accumulate, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* JETQ_H */

@@ -1,0 +1,216 @@
+"""Python binding of the jetq C ABI (``include/jetq.h``).
+
+Argument marshalling only: every function passes device pointers, sizes and
+the current CUDA stream to ``_build/libjetq.so`` and raises ``JetqError`` on a
+non-OK status.  PyTorch supplies device memory and streams.  There is no CPU
+fallback: without the compiled library every call raises.
+
+The ``jetq_*`` functions mirror the C entry points one to one.  The short
+helpers below them (``quant_act``, ``quant_weight``, ``quant_mx``, ``fprop``,
+``dgrad``, ``wgrad``) only allocate the output tensors with torch and call the
+matching ``jetq_*`` function.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libjetq.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(7)
+RECIPE_BLOCK128, RECIPE_MXFP8 = 0, 1
+PATH_AUTO, PATH_TRAIN, PATH_DECODE = 0, 1, 2
+OUT_F32, OUT_BF16 = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class JetqError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)} (status {status})")
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"jetq CUDA library missing ({LIB_PATH}); build it with __graft_entry__.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        P, I64, I32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        sig = {
+            "jetq_status_string": (ctypes.c_char_p, [I32]),
+            "jetq_version": (I32, []),
+            "jetq_check_device_error": (I32, [P]),
+            "jetq_colcopy_capacity": (I64, [I64, I32]),
+            "jetq_mx_scale_bytes": (I64, [I64, I64]),
+            "jetq_quant_act_1x128": (I32, [P, I64, I64, I64, P, P, P, P, I64, P, I32, P]),
+            "jetq_quant_w_128x128": (I32, [P, I64, I64, I64, P, P, P, P, P]),
+            "jetq_quant_mx32": (I32, [P, I64, I64, I64, P, P, P, P, I64, P, I32, P]),
+            "jetq_gemm_fprop": (I32, [I32, P, P, P, P, I64, I64, I64, P, I32, I64, I32, P]),
+            "jetq_gemm_dgrad": (I32, [I32, P, P, P, P, I64, I64, I64, P, I32, I64, P]),
+            "jetq_gemm_wgrad": (I32, [I32, P, P, P, P, I64, I64, I64, I64, P, I64, I32, P]),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = L
+        return L
+
+
+def status_string(status: int) -> str:
+    try:
+        return lib().jetq_status_string(int(status)).decode()
+    except RuntimeError:
+        return "unknown"
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _s(stream):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(status: int, where: str):
+    if status != OK:
+        raise JetqError(status, where)
+
+
+# ------------------------------------------------------------------ C entry points
+
+def jetq_version() -> int:
+    return int(lib().jetq_version())
+
+
+def jetq_check_device_error(stream=None) -> int:
+    return int(lib().jetq_check_device_error(_s(stream)))
+
+
+def jetq_colcopy_capacity(n: int, nseg: int = 1) -> int:
+    return int(lib().jetq_colcopy_capacity(n, nseg))
+
+
+def jetq_mx_scale_bytes(rows: int, k: int) -> int:
+    return int(lib().jetq_mx_scale_bytes(rows, k))
+
+
+def jetq_quant_act_1x128(x, q_row, s_row, q_col, s_col, ldq_col, seg_offsets=None, nseg=0, stream=None):
+    n, c = x.shape
+    _check(lib().jetq_quant_act_1x128(_p(x), n, c, x.stride(0), _p(q_row), _p(s_row), _p(q_col), _p(s_col),
+                                      ldq_col, _p(seg_offsets), nseg, _s(stream)), "jetq_quant_act_1x128")
+
+
+def jetq_quant_w_128x128(w, q, s, qT=None, sT=None, stream=None):
+    d, c = w.shape
+    _check(lib().jetq_quant_w_128x128(_p(w), d, c, w.stride(0), _p(q), _p(s), _p(qT), _p(sT), _s(stream)),
+           "jetq_quant_w_128x128")
+
+
+def jetq_quant_mx32(x, q_row, e8_row, q_col, e8_col, ldq_col, seg_offsets=None, nseg=0, stream=None):
+    r, c = x.shape
+    _check(lib().jetq_quant_mx32(_p(x), r, c, x.stride(0), _p(q_row), _p(e8_row), _p(q_col), _p(e8_col),
+                                 ldq_col, _p(seg_offsets), nseg, _s(stream)), "jetq_quant_mx32")
+
+
+def _out_dtype(t):
+    return OUT_BF16 if t.dtype == torch.bfloat16 else OUT_F32
+
+
+def jetq_gemm_fprop(recipe, qx, sx, qw, sw, n, d, c, y, path=PATH_AUTO, stream=None):
+    _check(lib().jetq_gemm_fprop(recipe, _p(qx), _p(sx), _p(qw), _p(sw), n, d, c, _p(y), _out_dtype(y),
+                                 y.stride(0), path, _s(stream)), "jetq_gemm_fprop")
+
+
+def jetq_gemm_dgrad(recipe, qdy, sdy, qwt, swt, n, d, c, dx, stream=None):
+    _check(lib().jetq_gemm_dgrad(recipe, _p(qdy), _p(sdy), _p(qwt), _p(swt), n, d, c, _p(dx), _out_dtype(dx),
+                                 dx.stride(0), _s(stream)), "jetq_gemm_dgrad")
+
+
+def jetq_gemm_wgrad(recipe, qdyc, sdyc, qxc, sxc, k, ldk, d, c, dw, accumulate=False, stream=None):
+    _check(lib().jetq_gemm_wgrad(recipe, _p(qdyc), _p(sdyc), _p(qxc), _p(sxc), k, ldk, d, c, _p(dw),
+                                 dw.stride(0), 1 if accumulate else 0, _s(stream)), "jetq_gemm_wgrad")
+
+
+# ------------------------------------------------------------------ allocating helpers
+
+def quant_act(x, row=True, col=True, seg_offsets=None, stream=None):
+    """BF16 [n x c] -> dict(q_row, s_row, q_col, s_col, ldq_col) (absent copies are None)."""
+    n, c = x.shape
+    dev = x.device
+    nseg = 0 if seg_offsets is None else seg_offsets.numel() - 1
+    cap = jetq_colcopy_capacity(n, max(nseg, 1))
+    out = dict(q_row=None, s_row=None, q_col=None, s_col=None, ldq_col=cap)
+    if row:
+        out["q_row"] = torch.empty((n, c), dtype=torch.uint8, device=dev)
+        out["s_row"] = torch.empty((c // 128, n), dtype=torch.float32, device=dev)
+    if col:
+        out["q_col"] = torch.empty((c, cap), dtype=torch.uint8, device=dev)
+        out["s_col"] = torch.empty((max(cap, 128) // 128, c), dtype=torch.float32, device=dev)
+    jetq_quant_act_1x128(x, out["q_row"], out["s_row"], out["q_col"], out["s_col"], cap, seg_offsets, nseg, stream)
+    return out
+
+
+def quant_weight(w, transposed=True, stream=None):
+    """BF16 [d x c] -> (q [d x c], s [d/128 x c/128], qT [c x d] | None, sT | None)."""
+    d, c = w.shape
+    dev = w.device
+    q = torch.empty((d, c), dtype=torch.uint8, device=dev)
+    s = torch.empty((d // 128, c // 128), dtype=torch.float32, device=dev)
+    qT = torch.empty((c, d), dtype=torch.uint8, device=dev) if transposed else None
+    sT = torch.empty((c // 128, d // 128), dtype=torch.float32, device=dev) if transposed else None
+    jetq_quant_w_128x128(w, q, s, qT, sT, stream)
+    return q, s, qT, sT
+
+
+def quant_mx(x, row=True, col=True, seg_offsets=None, stream=None):
+    """MXFP8 copies: dict(q_row, e8_row, q_col, e8_col, ldq_col); scales in the atom layout."""
+    r, c = x.shape
+    dev = x.device
+    nseg = 0 if seg_offsets is None else seg_offsets.numel() - 1
+    cap = jetq_colcopy_capacity(r, max(nseg, 1))
+    out = dict(q_row=None, e8_row=None, q_col=None, e8_col=None, ldq_col=cap)
+    if row:
+        out["q_row"] = torch.empty((r, c), dtype=torch.uint8, device=dev)
+        out["e8_row"] = torch.zeros(jetq_mx_scale_bytes(r, c), dtype=torch.uint8, device=dev)
+    if col:
+        out["q_col"] = torch.empty((c, cap), dtype=torch.uint8, device=dev)
+        out["e8_col"] = torch.zeros(jetq_mx_scale_bytes(c, cap), dtype=torch.uint8, device=dev)
+    jetq_quant_mx32(x, out["q_row"], out["e8_row"], out["q_col"], out["e8_col"], cap, seg_offsets, nseg, stream)
+    return out
+
+
+def fprop(qx, sx, qw, sw, out_dtype=torch.float32, path=PATH_AUTO, recipe=RECIPE_BLOCK128, stream=None):
+    n, c = qx.shape
+    d = qw.shape[0]
+    y = torch.empty((n, d), dtype=out_dtype, device=qx.device)
+    jetq_gemm_fprop(recipe, qx, sx, qw, sw, n, d, c, y, path, stream)
+    return y
+
+
+def dgrad(qdy, sdy, qwt, swt, out_dtype=torch.float32, recipe=RECIPE_BLOCK128, stream=None):
+    n, d = qdy.shape
+    c = qwt.shape[0]
+    dx = torch.empty((n, c), dtype=out_dtype, device=qdy.device)
+    jetq_gemm_dgrad(recipe, qdy, sdy, qwt, swt, n, d, c, dx, stream)
+    return dx
+
+
+def wgrad(qdyc, sdyc, qxc, sxc, k, dw=None, accumulate=False, recipe=RECIPE_BLOCK128, stream=None):
+    d, ldk = qdyc.shape
+    c = qxc.shape[0]
+    if dw is None:
+        dw = torch.empty((d, c), dtype=torch.float32, device=qdyc.device)
+    jetq_gemm_wgrad(recipe, qdyc, sdyc, qxc, sxc, k, ldk, d, c, dw, accumulate, stream)
+    return dw

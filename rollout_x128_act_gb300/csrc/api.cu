@@ -1,0 +1,266 @@
+// The C ABI (include/jetq.h): host-side validation, then one launch on the
+// caller's stream.  Nothing here allocates, synchronizes (except
+// jetq_check_device_error) or keeps pointers.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+
+#include "jetq_internal.h"
+
+namespace jetq {
+
+int sm_count()
+{
+    static std::atomic<int> cached[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return 1;
+    int v = cached[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            v = 1;
+        cached[dev].store(v, std::memory_order_relaxed);
+    }
+    return v;
+}
+
+namespace {
+
+// 1 = sm_103, -1 = other, 0 = unknown yet
+std::atomic<int> g_arch_ok[64];
+
+jetq_status check_arch()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64)
+        return JETQ_ERR_CUDA;
+    int v = g_arch_ok[dev].load(std::memory_order_relaxed);
+    if (v == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return JETQ_ERR_CUDA;
+        v = (major == 10 && minor == 3) ? 1 : -1;
+        g_arch_ok[dev].store(v, std::memory_order_relaxed);
+    }
+    return v == 1 ? JETQ_OK : JETQ_ERR_ARCH;
+}
+
+bool aligned16(const void *p)
+{
+    return (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+jetq_status from_cuda(cudaError_t e)
+{
+    return e == cudaSuccess ? JETQ_OK : JETQ_ERR_CUDA;
+}
+
+#define JQ_REQUIRE(cond, code)                                                                                       \
+    do {                                                                                                             \
+        if (!(cond))                                                                                                 \
+            return (code);                                                                                           \
+    } while (0)
+
+jetq_status check_out(const void *out, jetq_out_dtype dt, int64_t ld, int64_t cols)
+{
+    JQ_REQUIRE(out != nullptr, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(dt == JETQ_OUT_F32 || dt == JETQ_OUT_BF16, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(ld >= cols, JETQ_ERR_UNSUPPORTED_SHAPE);
+    JQ_REQUIRE(aligned16(out) && ld % (dt == JETQ_OUT_F32 ? 4 : 8) == 0, JETQ_ERR_MISALIGNED);
+    return JETQ_OK;
+}
+
+} // namespace
+} // namespace jetq
+
+using namespace jetq;
+
+extern "C" {
+
+const char *jetq_status_string(jetq_status status)
+{
+    switch (status) {
+    case JETQ_OK: return "ok";
+    case JETQ_ERR_INVALID_ARG: return "invalid argument";
+    case JETQ_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case JETQ_ERR_MISALIGNED: return "pointer or stride not 16-byte aligned";
+    case JETQ_ERR_ARCH: return "device is not compute capability 10.3 (GB300)";
+    case JETQ_ERR_CUDA: return "CUDA runtime error";
+    case JETQ_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+    }
+    return "unknown status";
+}
+
+int jetq_version(void)
+{
+    return 100; // 0.1.0
+}
+
+int64_t jetq_colcopy_capacity(int64_t n, int nseg)
+{
+    if (n <= 0)
+        return 0;
+    const int64_t bound = nseg <= 1 ? n : n + 127 * (int64_t)nseg;
+    return (bound + 127) / 128 * 128;
+}
+
+int64_t jetq_mx_scale_bytes(int64_t rows, int64_t k)
+{
+    if (rows <= 0 || k <= 0)
+        return 0;
+    return (rows + 127) / 128 * ((k + 511) / 512) * 2048;
+}
+
+jetq_status jetq_check_device_error(void *stream)
+{
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    unsigned word = 0;
+    if (gemm_read_and_clear_error(st, &word) != cudaSuccess)
+        return JETQ_ERR_CUDA;
+    return word ? JETQ_ERR_TIMEOUT : JETQ_OK;
+}
+
+jetq_status jetq_quant_act_1x128(const uint16_t *x, int64_t n, int64_t c, int64_t ldx, uint8_t *q_row, float *s_row,
+                                 uint8_t *q_col, float *s_col, int64_t ldq_col, const int64_t *seg_offsets, int nseg,
+                                 void *stream)
+{
+    JQ_REQUIRE(n >= 0 && c > 0, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE((q_row == nullptr) == (s_row == nullptr), JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE((q_col == nullptr) == (s_col == nullptr), JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(seg_offsets == nullptr || nseg >= 1, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(c % 128 == 0 && ldx >= c, JETQ_ERR_UNSUPPORTED_SHAPE);
+    const int nseg_eff = seg_offsets ? nseg : 1;
+    if (q_col)
+        JQ_REQUIRE(ldq_col % 128 == 0 && ldq_col >= jetq_colcopy_capacity(n, nseg_eff), JETQ_ERR_UNSUPPORTED_SHAPE);
+    if (n == 0 || (!q_row && !q_col))
+        return JETQ_OK;
+    JQ_REQUIRE(x != nullptr, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(aligned16(x) && ldx % 8 == 0 && aligned16(q_row) && aligned16(s_row) && aligned16(q_col) &&
+                   aligned16(s_col) && (reinterpret_cast<uintptr_t>(seg_offsets) & 7u) == 0,
+               JETQ_ERR_MISALIGNED);
+    const jetq_status a = check_arch();
+    if (a != JETQ_OK)
+        return a;
+    ActQuantArgs args{x, n, c, ldx, q_row, s_row, q_col, s_col, ldq_col, seg_offsets, nseg_eff};
+    return from_cuda(launch_quant_act(args, static_cast<cudaStream_t>(stream)));
+}
+
+jetq_status jetq_quant_w_128x128(const uint16_t *w, int64_t d, int64_t c, int64_t ldw, uint8_t *q, float *s,
+                                 uint8_t *qT, float *sT, void *stream)
+{
+    JQ_REQUIRE(w != nullptr && q != nullptr && s != nullptr && d > 0 && c > 0, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE((qT == nullptr) == (sT == nullptr), JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(d % 128 == 0 && c % 128 == 0 && ldw >= c, JETQ_ERR_UNSUPPORTED_SHAPE);
+    JQ_REQUIRE(aligned16(w) && ldw % 8 == 0 && aligned16(q) && aligned16(qT) &&
+                   (reinterpret_cast<uintptr_t>(s) & 3u) == 0 && (reinterpret_cast<uintptr_t>(sT) & 3u) == 0,
+               JETQ_ERR_MISALIGNED);
+    const jetq_status a = check_arch();
+    if (a != JETQ_OK)
+        return a;
+    WeightQuantArgs args{w, d, c, ldw, q, s, qT, sT};
+    return from_cuda(launch_quant_weight(args, static_cast<cudaStream_t>(stream)));
+}
+
+jetq_status jetq_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q_row,
+                            uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, int64_t ldq_col,
+                            const int64_t *seg_offsets, int nseg, void *stream)
+{
+    JQ_REQUIRE(rows >= 0 && cols > 0, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE((q_row == nullptr) == (e8_row == nullptr), JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE((q_col == nullptr) == (e8_col == nullptr), JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(seg_offsets == nullptr || nseg >= 1, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(cols % 128 == 0 && ldx >= cols, JETQ_ERR_UNSUPPORTED_SHAPE);
+    const int nseg_eff = seg_offsets ? nseg : 1;
+    if (q_col)
+        JQ_REQUIRE(ldq_col % 128 == 0 && ldq_col >= jetq_colcopy_capacity(rows, nseg_eff), JETQ_ERR_UNSUPPORTED_SHAPE);
+    if (rows == 0 || (!q_row && !q_col))
+        return JETQ_OK;
+    JQ_REQUIRE(x != nullptr, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(aligned16(x) && ldx % 8 == 0 && aligned16(q_row) && aligned16(e8_row) && aligned16(q_col) &&
+                   aligned16(e8_col) && (reinterpret_cast<uintptr_t>(seg_offsets) & 7u) == 0,
+               JETQ_ERR_MISALIGNED);
+    const jetq_status a = check_arch();
+    if (a != JETQ_OK)
+        return a;
+    MxQuantArgs args{x, rows, cols, ldx, q_row, e8_row, q_col, e8_col, ldq_col, seg_offsets, nseg_eff};
+    return from_cuda(launch_quant_mx(args, static_cast<cudaStream_t>(stream)));
+}
+
+jetq_status jetq_gemm_fprop(jetq_recipe recipe, const uint8_t *qx, const void *sx, const uint8_t *qw, const void *sw,
+                            int64_t n, int64_t d, int64_t c, void *y, jetq_out_dtype y_dtype, int64_t ldy,
+                            jetq_path path, void *stream)
+{
+    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128 || recipe == JETQ_RECIPE_MXFP8, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(path == JETQ_PATH_AUTO || path == JETQ_PATH_TRAIN || path == JETQ_PATH_DECODE, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(n >= 0 && d > 0 && c > 0, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(d % 128 == 0 && c % 128 == 0, JETQ_ERR_UNSUPPORTED_SHAPE);
+    jetq_status st = check_out(y, y_dtype, ldy, d);
+    if (st != JETQ_OK)
+        return st;
+    if (n == 0)
+        return JETQ_OK;
+    JQ_REQUIRE(qx && sx && qw && sw, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(aligned16(qx) && aligned16(qw) && aligned16(sx) && aligned16(sw), JETQ_ERR_MISALIGNED);
+    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128, JETQ_ERR_INVALID_ARG); // MXFP8 GEMMs: not in this build
+    if ((st = check_arch()) != JETQ_OK)
+        return st;
+    GemmProblem g{qx, static_cast<const float *>(sx), qw, static_cast<const float *>(sw), n, d, c, c, c,
+                  BScale::Block128, y, ldy, y_dtype, 0};
+    const bool decode = path == JETQ_PATH_DECODE || (path == JETQ_PATH_AUTO && n <= 256);
+    return from_cuda(launch_gemm_block128(g, decode ? GemmShape::Decode : GemmShape::Train,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+jetq_status jetq_gemm_dgrad(jetq_recipe recipe, const uint8_t *qdy, const void *sdy, const uint8_t *qwt,
+                            const void *swt, int64_t n, int64_t d, int64_t c, void *dx, jetq_out_dtype dx_dtype,
+                            int64_t lddx, void *stream)
+{
+    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128 || recipe == JETQ_RECIPE_MXFP8, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(n >= 0 && d > 0 && c > 0, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(d % 128 == 0 && c % 128 == 0, JETQ_ERR_UNSUPPORTED_SHAPE);
+    jetq_status st = check_out(dx, dx_dtype, lddx, c);
+    if (st != JETQ_OK)
+        return st;
+    if (n == 0)
+        return JETQ_OK;
+    JQ_REQUIRE(qdy && sdy && qwt && swt, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(aligned16(qdy) && aligned16(qwt) && aligned16(sdy) && aligned16(swt), JETQ_ERR_MISALIGNED);
+    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128, JETQ_ERR_INVALID_ARG);
+    if ((st = check_arch()) != JETQ_OK)
+        return st;
+    GemmProblem g{qdy, static_cast<const float *>(sdy), qwt, static_cast<const float *>(swt), n, c, d, d, d,
+                  BScale::Block128, dx, lddx, dx_dtype, 0};
+    return from_cuda(launch_gemm_block128(g, n <= 256 ? GemmShape::Decode : GemmShape::Train,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+jetq_status jetq_gemm_wgrad(jetq_recipe recipe, const uint8_t *qdyc, const void *sdyc, const uint8_t *qxc,
+                            const void *sxc, int64_t k, int64_t ldk, int64_t d, int64_t c, float *dw, int64_t lddw,
+                            int accumulate, void *stream)
+{
+    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128 || recipe == JETQ_RECIPE_MXFP8, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(k >= 0 && d > 0 && c > 0, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(d % 128 == 0 && c % 128 == 0 && k % 128 == 0 && ldk >= k, JETQ_ERR_UNSUPPORTED_SHAPE);
+    jetq_status st = check_out(dw, JETQ_OUT_F32, lddw, c);
+    if (st != JETQ_OK)
+        return st;
+    if (k == 0) {
+        if (accumulate)
+            return JETQ_OK;
+        return from_cuda(cudaMemset2DAsync(dw, (size_t)lddw * 4, 0, (size_t)c * 4, (size_t)d,
+                                           static_cast<cudaStream_t>(stream)));
+    }
+    JQ_REQUIRE(qdyc && sdyc && qxc && sxc, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(aligned16(qdyc) && aligned16(qxc) && aligned16(sdyc) && aligned16(sxc) && ldk % 16 == 0,
+               JETQ_ERR_MISALIGNED);
+    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128, JETQ_ERR_INVALID_ARG);
+    if ((st = check_arch()) != JETQ_OK)
+        return st;
+    GemmProblem g{qdyc, static_cast<const float *>(sdyc), qxc, static_cast<const float *>(sxc), d, c, k, ldk, ldk,
+                  BScale::PerRow, dw, lddw, JETQ_OUT_F32, accumulate ? 1 : 0};
+    return from_cuda(launch_gemm_block128(g, GemmShape::Train, static_cast<cudaStream_t>(stream)));
+}
+
+} // extern "C"

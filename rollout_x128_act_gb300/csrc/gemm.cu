@@ -1,0 +1,426 @@
+// Block-scaled FP8 GEMM (128-block recipe) on sm_103a tensor cores.
+//
+//   out[m, n] = sum over K-blocks kb of  fl32(Sa[m,kb] * Sb[n,kb]) * P_kb[m, n]
+//   P_kb[m, n] = sum_{k in kb} qa[m, k] * qb[n, k]      (E4M3 x E4M3 -> FP32)
+//
+// Per-128-K-block FP32 scales (Jet-RL: 1x128 activation groups, 128x128
+// weight blocks; FP32 scales are applied outside the tensor core on
+// Blackwell, as the Miles Blackwell-recipes post notes) cannot ride the
+// native block-scaled MMA, so each K-block is one MMA group into a fresh TMEM
+// accumulator and the scale is applied ("promoted") by CUDA cores:
+//
+//   warp 0        TMA producer: A and B K-block tiles (128-byte swizzle) into
+//                 a STAGES-deep shared-memory ring
+//   warp 1        MMA issuer: 4 x tcgen05.mma (K = 32 each) per K-block into
+//                 TMEM buffer kb % TMEM_BUFS, then tcgen05.commit to release
+//                 the smem stage and to signal the epilogue
+//   warps 2..     epilogue: tcgen05.ld the K-block partial, acc = fma(P, s, acc)
+//                 in registers (packed f32x2), release the TMEM buffer; after
+//                 the last K-block, store the tile
+//
+// One CTA per SM, persistent over output tiles (grouped raster for L2 reuse).
+// The same template serves the training shape (BN = 256, 8 epilogue warps,
+// 2 TMEM buffers) and the decode shape (BN = 32, 4 epilogue warps, 16 TMEM
+// buffers, a narrow weight slice per CTA so the weight stream spreads over
+// every SM).  Both perform the identical per-element operation sequence, so a
+// decode row equals the corresponding training row bit for bit.
+//
+// Every mbarrier wait is bounded (wall clock); a CTA that gives up raises a
+// shared abort flag, records the fact in the device error word, drains its
+// own TMA copies and MMAs (again bounded) and frees its TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "jetq_internal.h"
+#include "ptx.cuh"
+
+namespace jetq {
+
+__device__ unsigned g_gemm_error;
+
+namespace {
+
+constexpr int kGroupM = 8;
+constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull; // 2 s per wait
+
+struct KParams {
+    const float *sa;
+    const float *sb;
+    int64_t M, N;
+    int num_kb;
+    int mt, nt;
+    int box_a_rows;
+    int box_b_rows;
+    void *out;
+    int64_t ldo;
+    int out_bf16;
+    int accumulate;
+    unsigned long long limit_ns;
+};
+
+__device__ __forceinline__ void tile_coords(int t, int mt, int nt, int &mi, int &ni)
+{
+    const int group = kGroupM * nt;
+    const int first_m = (t / group) * kGroupM;
+    const int gm = min(mt - first_m, kGroupM);
+    const int r = t % group;
+    mi = first_m + r % gm;
+    ni = r / gm;
+}
+
+template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS>
+struct Cfg {
+    static constexpr int kABytes = 128 * 128;
+    static constexpr int kBBytes = BN * 128;
+    static constexpr int kStage = kABytes + kBBytes;
+    // warpgroup 0: producer (warp 0), MMA issuer (warp 1), two idle warps;
+    // warpgroups 1..: epilogue
+    static constexpr int kThreads = 128 + 32 * EPI_WARPS;
+    static constexpr int kCols = BN / (EPI_WARPS / 4); // accumulator columns per epilogue thread
+    static constexpr int kTmemCols = 512;
+    static constexpr int kBars = 2 * STAGES + 2 * TMEM_BUFS + 1;
+    static constexpr size_t kSmem = 1024 + (size_t)STAGES * kStage + 1024;
+    static_assert(TMEM_BUFS * BN <= kTmemCols, "TMEM buffers exceed 512 columns");
+    static_assert(EPI_WARPS % 4 == 0 && kCols % 16 == 0, "epilogue split");
+    static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
+    static_assert(kBars * 8 + 16 <= 1024, "barrier area");
+};
+
+template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B>
+__global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
+    k_gemm_b128(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p)
+{
+    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(tiles + (size_t)STAGES * C::kStage);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const uint32_t bar0 = ptx::smem_addr(bars);
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
+    auto tempty = [&](int b) { return bar0 + 8u * (2 * STAGES + TMEM_BUFS + b); };
+    const uint32_t done = bar0 + 8u * (2 * STAGES + 2 * TMEM_BUFS);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int num_tiles = p.mt * p.nt;
+    unsigned *err = &g_gemm_error;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full(s), 1);
+            ptx::mbar_init(empty(s), 1);
+        }
+        for (int b = 0; b < TMEM_BUFS; ++b) {
+            ptx::mbar_init(tfull(b), 1);
+            ptx::mbar_init(tempty(b), EPI_WARPS);
+        }
+        ptx::mbar_init(done, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmA);
+        ptx::prefetch_tensormap(&tmB);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::kTmemCols);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    if (warp < 4) {
+    if (warp == 0) {
+        // ------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const uint32_t tx = (uint32_t)((p.box_a_rows + p.box_b_rows) * 128);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                int mi, ni;
+                tile_coords(tile, p.mt, p.nt, mi, ni);
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const int s = (int)(it % STAGES);
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!ptx::mbar_wait(empty(s), ph ^ 1u, abort_flag, err, kErrTimeout, p.limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(full(s), tx);
+                    const uint32_t dst = ptx::smem_addr(tiles + (size_t)s * C::kStage);
+                    ptx::tma_load_2d(dst, &tmA, full(s), kb * 128, mi * 128);
+                    ptx::tma_load_2d(dst + C::kABytes, &tmB, full(s), kb * 128, ni * BN);
+                }
+            }
+            // drain: every copy this thread started must have landed before exit
+            for (int s = 0; s < STAGES; ++s) {
+                if (it > (uint32_t)s) {
+                    const uint32_t last = (uint32_t)s + ((it - 1u - (uint32_t)s) / STAGES) * STAGES;
+                    ptx::mbar_wait(full(s), (last / STAGES) & 1u, abort_flag, err, kErrTimeout, p.limit_ns, false);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc = ptx::idesc_e4m3_f32(128, BN);
+            uint32_t it = 0, tb = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it, ++tb) {
+                    const int s = (int)(it % STAGES);
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    const int b = (int)(tb % TMEM_BUFS);
+                    const uint32_t tph = (tb / TMEM_BUFS) & 1u;
+                    if (!ptx::mbar_wait(tempty(b), tph ^ 1u, abort_flag, err, kErrTimeout, p.limit_ns) ||
+                        !ptx::mbar_wait(full(s), ph, abort_flag, err, kErrTimeout, p.limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    const uint32_t a_addr = ptx::smem_addr(tiles + (size_t)s * C::kStage);
+                    const uint64_t adesc = ptx::desc_kmajor_sw128(a_addr);
+                    const uint64_t bdesc = ptx::desc_kmajor_sw128(a_addr + C::kABytes);
+                    const uint32_t d = tmem_base + (uint32_t)(b * BN);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) // 4 x K=32 (32 bytes) inside the 128-byte swizzle row
+                        ptx::mma_f8f6f4(d, adesc + 2u * k, bdesc + 2u * k, idesc, k > 0 ? 1u : 0u);
+                    ptx::mma_commit(empty(s));
+                    ptx::mma_commit(tfull(b));
+                }
+            }
+            ptx::mma_commit(done);
+            ptx::mbar_wait(done, 0u, abort_flag, err, kErrTimeout, p.limit_ns, false);
+        }
+        __syncwarp();
+    }
+    } else {
+        // ------------------------------------------------------ epilogue
+        const int ew = warp - 4;
+        const int quarter = warp & 3; // TMEM lanes 32*quarter .. +31
+        const int col0 = (ew >> 2) * C::kCols;
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        uint32_t tb = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            int mi, ni;
+            tile_coords(tile, p.mt, p.nt, mi, ni);
+            const int64_t m = (int64_t)mi * 128 + quarter * 32 + lane;
+            const bool row_ok = m < p.M;
+            const int64_t n0 = (int64_t)ni * BN + col0;
+            const bool col_ok = n0 < p.N; // a slice past N (N % BN != 0) computes nothing it stores
+            float2 acc[C::kCols / 2];
+#pragma unroll
+            for (int j = 0; j < C::kCols / 2; ++j)
+                acc[j] = make_float2(0.0f, 0.0f);
+
+            for (int kb = 0; kb < p.num_kb; ++kb, ++tb) {
+                const int b = (int)(tb % TMEM_BUFS);
+                const uint32_t tph = (tb / TMEM_BUFS) & 1u;
+                const float sa = row_ok ? __ldg(p.sa + (int64_t)kb * p.M + m) : 0.0f;
+                float s = 0.0f;
+                if (!PER_ROW_B && col_ok)
+                    s = __fmul_rn(sa, __ldg(p.sb + (n0 >> 7) * p.num_kb + kb));
+                const bool got = ptx::mbar_wait(tfull(b), tph, abort_flag, err, kErrTimeout, p.limit_ns);
+                if (!__all_sync(0xFFFFFFFFu, got)) { // keep the warp converged for tcgen05.ld
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int ch = 0; ch < C::kCols / 16; ++ch) {
+                    uint32_t P[16];
+                    ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + (uint32_t)(b * BN + col0 + ch * 16), P);
+                    ptx::tmem_ld_wait();
+                    if (PER_ROW_B && col_ok) {
+                        const float4 *sbp = reinterpret_cast<const float4 *>(p.sb + (int64_t)kb * p.N + n0 + ch * 16);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            const float4 sb4 = __ldg(sbp + q);
+                            const float2 s01 = __fmul2_rn(make_float2(sa, sa), make_float2(sb4.x, sb4.y));
+                            const float2 s23 = __fmul2_rn(make_float2(sa, sa), make_float2(sb4.z, sb4.w));
+                            float2 &a0 = acc[ch * 8 + 2 * q];
+                            float2 &a1 = acc[ch * 8 + 2 * q + 1];
+                            a0 = __ffma2_rn(make_float2(__uint_as_float(P[4 * q]), __uint_as_float(P[4 * q + 1])), s01, a0);
+                            a1 = __ffma2_rn(make_float2(__uint_as_float(P[4 * q + 2]), __uint_as_float(P[4 * q + 3])), s23, a1);
+                        }
+                    } else if (!PER_ROW_B) {
+                        const float2 s2 = make_float2(s, s);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            acc[ch * 8 + j] = __ffma2_rn(
+                                make_float2(__uint_as_float(P[2 * j]), __uint_as_float(P[2 * j + 1])), s2, acc[ch * 8 + j]);
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(tempty(b));
+            }
+            if (!ok)
+                break;
+            if (row_ok && col_ok) {
+                if (p.out_bf16) {
+                    __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.out) + m * p.ldo + n0;
+#pragma unroll
+                    for (int j8 = 0; j8 < C::kCols / 8; ++j8) {
+                        uint4 v;
+                        uint32_t *w = reinterpret_cast<uint32_t *>(&v);
+#pragma unroll
+                        for (int h = 0; h < 4; ++h) {
+                            const __nv_bfloat162 b2 = __floats2bfloat162_rn(acc[4 * j8 + h].x, acc[4 * j8 + h].y);
+                            w[h] = *reinterpret_cast<const uint32_t *>(&b2);
+                        }
+                        *reinterpret_cast<uint4 *>(o + 8 * j8) = v;
+                    }
+                } else {
+                    float *o = reinterpret_cast<float *>(p.out) + m * p.ldo + n0;
+#pragma unroll
+                    for (int j4 = 0; j4 < C::kCols / 4; ++j4) {
+                        float4 v = make_float4(acc[2 * j4].x, acc[2 * j4].y, acc[2 * j4 + 1].x, acc[2 * j4 + 1].y);
+                        if (p.accumulate) {
+                            const float4 old = *reinterpret_cast<const float4 *>(o + 4 * j4);
+                            v.x = __fadd_rn(old.x, v.x);
+                            v.y = __fadd_rn(old.y, v.y);
+                            v.z = __fadd_rn(old.z, v.z);
+                            v.w = __fadd_rn(old.w, v.w);
+                        }
+                        *reinterpret_cast<float4 *>(o + 4 * j4) = v;
+                    }
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, C::kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    });
+    return fn;
+}
+
+// 2-D map over a K-major byte matrix [rows x k_extent] with row stride ld.
+cudaError_t make_map(CUtensorMap *map, const void *base, int64_t k_extent, int64_t rows, int64_t ld, int box_rows)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {(cuuint64_t)k_extent, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld};
+    const cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B>
+cudaError_t run(const GemmProblem &g, cudaStream_t st)
+{
+    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS>;
+    auto kern = k_gemm_b128<BN, EPI_WARPS, STAGES, TMEM_BUFS, PER_ROW_B>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (configured_device != dev) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
+        if (e != cudaSuccess)
+            return e;
+        configured_device = dev;
+    }
+    // boxes never taller than the tensor; rows of a stage past the box keep
+    // stale bytes, which only reach accumulator rows/columns that are not stored
+    const int box_a = g.M >= 128 ? 128 : (int)((g.M + 7) / 8 * 8);
+    const int box_b = g.N >= BN ? BN : (int)((g.N + 7) / 8 * 8);
+    CUtensorMap ta, tbm;
+    if ((e = make_map(&ta, g.a, g.K, g.M, g.lda, box_a)) != cudaSuccess)
+        return e;
+    if ((e = make_map(&tbm, g.b, g.K, g.N, g.ldb, box_b)) != cudaSuccess)
+        return e;
+    KParams kp;
+    kp.sa = g.sa;
+    kp.sb = g.sb;
+    kp.M = g.M;
+    kp.N = g.N;
+    kp.num_kb = (int)(g.K / 128);
+    kp.mt = (int)((g.M + 127) / 128);
+    kp.nt = (int)((g.N + BN - 1) / BN);
+    kp.box_a_rows = box_a;
+    kp.box_b_rows = box_b;
+    kp.out = g.out;
+    kp.ldo = g.ldo;
+    kp.out_bf16 = g.out_dtype == JETQ_OUT_BF16;
+    kp.accumulate = g.accumulate;
+    kp.limit_ns = kWaitLimitNs;
+    const int tiles = kp.mt * kp.nt;
+    const int grid = tiles < sm_count() ? tiles : sm_count();
+    kern<<<grid, C::kThreads, C::kSmem, st>>>(ta, tbm, kp);
+    return cudaGetLastError();
+}
+
+} // namespace
+
+cudaError_t launch_gemm_block128(const GemmProblem &g, GemmShape shape, cudaStream_t st)
+{
+    if (g.M == 0)
+        return cudaSuccess;
+    const bool per_row = g.bscale == BScale::PerRow;
+    if (shape == GemmShape::Train)
+        return per_row ? run<256, 8, 4, 2, true>(g, st) : run<256, 8, 4, 2, false>(g, st);
+    return per_row ? run<32, 4, 10, 16, true>(g, st) : run<32, 4, 10, 16, false>(g, st);
+}
+
+cudaError_t gemm_read_and_clear_error(cudaStream_t st, unsigned *out)
+{
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_gemm_error, sizeof v, 0, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess)
+        return e;
+    *out |= v;
+    if (v) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_gemm_error, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaStreamSynchronize(st);
+    }
+    return e;
+}
+
+} // namespace jetq

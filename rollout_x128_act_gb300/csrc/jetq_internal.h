@@ -1,0 +1,80 @@
+// Internal declarations shared by the jetq translation units (host side).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/jetq.h"
+
+namespace jetq {
+
+// ---------------------------------------------------------------- quantizers
+struct ActQuantArgs {
+    const uint16_t *x;
+    int64_t n, c, ldx;
+    uint8_t *q_row;
+    float *s_row;
+    uint8_t *q_col;
+    float *s_col;
+    int64_t ldq_col;
+    const int64_t *seg; // device, nseg + 1 entries, or nullptr
+    int nseg;
+};
+
+struct WeightQuantArgs {
+    const uint16_t *w;
+    int64_t d, c, ldw;
+    uint8_t *q;
+    float *s;
+    uint8_t *qT;
+    float *sT;
+};
+
+struct MxQuantArgs {
+    const uint16_t *x;
+    int64_t rows, cols, ldx;
+    uint8_t *q_row;
+    uint8_t *e8_row;
+    uint8_t *q_col;
+    uint8_t *e8_col;
+    int64_t ldq_col;
+    const int64_t *seg;
+    int nseg;
+};
+
+cudaError_t launch_quant_act(const ActQuantArgs &a, cudaStream_t st);
+cudaError_t launch_quant_weight(const WeightQuantArgs &a, cudaStream_t st);
+cudaError_t launch_quant_mx(const MxQuantArgs &a, cudaStream_t st);
+
+// --------------------------------------------------------------------- GEMMs
+// One block-scaled GEMM problem: out[M x N] = A[M x K] * B[N x K]^T, both
+// operands K-major FP8 with per-128-K-block scales.
+enum class BScale : int {
+    Block128 = 0, // sb[(n / 128) * (K / 128) + kb]           (128x128 weight blocks)
+    PerRow = 1    // sb[kb * N + n]                           (column copy along K)
+};
+
+struct GemmProblem {
+    const uint8_t *a;  // [M x lda] codes
+    const float *sa;   // [K/128 x M]
+    const uint8_t *b;  // [N x ldb] codes
+    const float *sb;   // see BScale
+    int64_t M, N, K;
+    int64_t lda, ldb;  // bytes
+    BScale bscale;
+    void *out;
+    int64_t ldo;       // elements
+    jetq_out_dtype out_dtype;
+    int accumulate;    // F32 only: out = out + acc
+};
+
+enum class GemmShape : int { Train = 0, Decode = 1 };
+
+cudaError_t launch_gemm_block128(const GemmProblem &p, GemmShape shape, cudaStream_t st);
+
+cudaError_t gemm_read_and_clear_error(cudaStream_t st, unsigned *out);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+} // namespace jetq

@@ -1,0 +1,575 @@
+// Fused FP8 (E4M3) quantizers for sm_103a: one pass over a BF16 tile emits
+// the row-wise copy, the transposed column-wise copy and their scales.
+//
+// Work unit: a 128-row x 128-column BF16 tile (32 KB), 256 threads.  Thread t
+// owns rows 8*(t/16) .. +7 and columns 8*(t%16) .. +7 of the tile as an 8x8
+// register block, loaded with eight coalesced 16-byte loads (a warp covers two
+// full 256-byte row segments per load).  Row maxima are warp shuffles over 16
+// lanes; column maxima are a shuffle plus an 8-warp shared-memory reduction.
+// The column copy is staged transposed in a swizzled 16 KB shared tile and
+// written out as coalesced 16-byte stores, so HBM sees each byte once.
+//
+// Quotient x / S (FP32-scale recipe).  The exact IEEE quotient fl32(x / S) is
+// obtained without a division per element: with r = RN(1/S) (one correctly
+// rounded reciprocal per group), q0 = RN(x * r), the FMA residual
+// e = x - S * q0 and one correction q1 = RN(q0 + e * r) (Markstein,
+// "Computation of elementary functions on the IBM RISC System/6000
+// processor", IBM J. R&D 1990) give RN(x / S) for every finite BF16 x with
+// |x| <= amax and every S = fl32(amax / 448) >= 2^-96; the sign of a zero
+// quotient is restored from x.  This was checked exhaustively over all BF16
+// pairs (tests/test_division_domain.py).  Groups with S < 2^-96 use the
+// IEEE division itself.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "jetq_internal.h"
+
+namespace jetq {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr float kE4M3Max = 448.0f;
+
+__device__ __forceinline__ uint4 ldg_stream(const uint16_t *p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &u, float (&v)[8])
+{
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        v[2 * k] = __uint_as_float(w[k] << 16);
+        v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+}
+
+// ------------------------------------------------------------ FP32 recipe
+
+struct Fp32Scale {
+    float s;   // the group scale, fl32(amax / 448)
+    float r;   // RN(1 / s)
+    bool zero; // all-zero group: codes 0x00
+    bool slow; // s < 2^-96: use the IEEE division
+};
+
+__device__ __forceinline__ Fp32Scale make_scale(float amax)
+{
+    Fp32Scale sc;
+    sc.s = __fdiv_rn(amax, kE4M3Max);
+    sc.zero = !(sc.s > 0.0f);
+    sc.slow = sc.s < 0x1p-96f;
+    sc.r = sc.zero ? 0.0f : __frcp_rn(sc.s);
+    return sc;
+}
+
+__device__ __forceinline__ float quotient(float x, const Fp32Scale &sc)
+{
+    if (sc.slow)
+        return __fdiv_rn(x, sc.s);
+    const float q0 = __fmul_rn(x, sc.r);
+    const float e = __fmaf_rn(-q0, sc.s, x);
+    const float q1 = __fmaf_rn(e, sc.r, q0);
+    return __uint_as_float((__float_as_uint(q1) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+}
+
+__device__ __forceinline__ uint32_t cvt4(float a, float b, float c, float d)
+{
+    const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+    const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+    return lo | (hi << 16);
+}
+
+// 8 values that share one scale -> 8 codes (byte k = value k)
+__device__ __forceinline__ uint2 quant8(const float (&v)[8], const Fp32Scale &sc)
+{
+    if (sc.zero)
+        return make_uint2(0u, 0u);
+    float q[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        q[k] = quotient(v[k], sc);
+    return make_uint2(cvt4(q[0], q[1], q[2], q[3]), cvt4(q[4], q[5], q[6], q[7]));
+}
+
+// ------------------------------------------------------------ MX recipe
+
+// Smallest e with amax <= 448 * 2^e, clamped to [-127, 127]; 0 for amax == 0.
+// 448 = 1.75 * 2^8: for amax = m * 2^E (m in [1, 2)), e = E - 8 + (m > 1.75).
+__device__ __forceinline__ int e8m0_exponent(float amax)
+{
+    uint32_t bits = __float_as_uint(amax);
+    if (bits == 0u)
+        return 0;
+    int E = (int)(bits >> 23) - 127;
+    uint32_t mant = bits & 0x7FFFFFu;
+    if ((bits >> 23) == 0u) { // subnormal amax = mant * 2^-149: normalise the significand
+        const int lz = __clz(mant); // top set bit at 31 - lz
+        E = -118 - lz;
+        mant = (mant << (lz - 8)) & 0x7FFFFFu;
+    }
+    int e = E - 8 + (mant > 0x600000u ? 1 : 0);
+    return max(-127, min(127, e));
+}
+
+__device__ __forceinline__ uint2 quant8_mx(const float (&v)[8], float mult, bool zero)
+{
+    if (zero)
+        return make_uint2(0u, 0u);
+    float q[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        q[k] = __fmul_rn(v[k], mult); // exact: a power of two in the normal range
+    return make_uint2(cvt4(q[0], q[1], q[2], q[3]), cvt4(q[4], q[5], q[6], q[7]));
+}
+
+// 2^-e as a float, e in [-127, 127] (2^127 .. 2^-127; 2^-127 is subnormal but
+// never needed: e <= 120 for finite inputs).
+__device__ __forceinline__ float exp2_neg(int e)
+{
+    const int be = 127 - e;
+    return be >= 1 && be <= 254 ? __uint_as_float((uint32_t)be << 23) : __uint_as_float(1u << (22 + be));
+}
+
+// byte offset of MX scale (row r, block j) in the 2048-byte atom layout
+__device__ __forceinline__ int64_t mx_atom_offset(int64_t r, int64_t j, int64_t ka)
+{
+    return ((r >> 7) * ka + (j >> 4)) * 2048 + (r & 127) * 16 + (j & 15);
+}
+
+// ------------------------------------------------------------ shared tiles
+
+// Transposed code tile: row = column of the source tile (128 B = 128 source
+// rows).  8-byte chunk k of row c is stored at chunk k ^ (c >> 3), which makes
+// the per-thread 8-byte stores and the 16-byte read-back conflict-free.
+__device__ __forceinline__ void tileT_put(uint8_t *tileT, int col, int chunk, uint2 v)
+{
+    *reinterpret_cast<uint2 *>(tileT + col * 128 + ((chunk ^ (col >> 3)) & 15) * 8) = v;
+}
+
+__device__ __forceinline__ uint4 tileT_get16(const uint8_t *tileT, int col, int u)
+{
+    const int s = (col >> 3) & 15;
+    uint4 v = *reinterpret_cast<const uint4 *>(tileT + col * 128 + (((2 * u) ^ (s & 14)) * 8));
+    if (s & 1) {
+        uint32_t t0 = v.x, t1 = v.y;
+        v.x = v.z;
+        v.y = v.w;
+        v.z = t0;
+        v.w = t1;
+    }
+    return v;
+}
+
+// ------------------------------------------------------------ group mapping
+
+struct Group {
+    int64_t t0;  // first source row of the tile
+    int cnt;     // valid rows (0 .. 128)
+    int64_t p0;  // position of the tile in the column copy
+};
+
+// Maps padded group index g to its source rows.  Segment e owns groups
+// G_e .. G_{e+1}-1 with G_e = sum_{j<e} ceil(n_j / 128).  Warp 0 computes it
+// and publishes through shared memory; cnt = 0 marks a group past the end.
+__device__ void map_group(int64_t g, int64_t n, const int64_t *seg, int nseg, Group *out)
+{
+    const int lane = threadIdx.x & 31;
+    if (threadIdx.x >= 32)
+        return;
+    if (seg == nullptr) {
+        if (lane == 0) {
+            out->t0 = g * 128;
+            const int64_t rem = n - g * 128;
+            out->cnt = rem <= 0 ? 0 : (rem >= 128 ? 128 : (int)rem);
+            out->p0 = g * 128;
+        }
+        return;
+    }
+    const int per = (nseg + 31) / 32;
+    const int e0 = min(nseg, lane * per), e1 = min(nseg, e0 + per);
+    auto clampo = [&](int64_t v) { return v < 0 ? (int64_t)0 : (v > n ? n : v); };
+    int64_t mine = 0;
+    for (int e = e0; e < e1; ++e) {
+        const int64_t ne = clampo(seg[e + 1]) - clampo(seg[e]);
+        if (ne > 0)
+            mine += (ne + 127) / 128;
+    }
+    int64_t incl = mine;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int64_t v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+        if (lane >= d)
+            incl += v;
+    }
+    const int64_t total = __shfl_sync(0xFFFFFFFFu, incl, 31);
+    if (lane == 0 && g >= total)
+        out->cnt = 0;
+    const int64_t excl = incl - mine;
+    if (g >= excl && g < incl) {
+        int64_t gg = excl;
+        for (int e = e0; e < e1; ++e) {
+            const int64_t lo = clampo(seg[e]), ne = clampo(seg[e + 1]) - lo;
+            if (ne <= 0)
+                continue;
+            const int64_t ge = (ne + 127) / 128;
+            if (g < gg + ge) {
+                const int64_t t = g - gg;
+                out->t0 = lo + t * 128;
+                const int64_t rem = ne - t * 128;
+                out->cnt = rem >= 128 ? 128 : (int)rem;
+                out->p0 = g * 128;
+                break;
+            }
+            gg += ge;
+        }
+    }
+}
+
+// loads the thread's 8x8 block (rows >= cnt read as +0)
+__device__ __forceinline__ void load_block(const uint16_t *x, int64_t ldx, int64_t row0, int64_t col0, int cnt,
+                                           int rg, int cc, float (&v)[8][8])
+{
+    uint4 raw[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = rg * 8 + i;
+        raw[i] = r < cnt ? ldg_stream(x + (row0 + r) * ldx + col0 + cc * 8) : make_uint4(0, 0, 0, 0);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        unpack8(raw[i], v[i]);
+}
+
+__device__ __forceinline__ float absmax8(const float (&v)[8])
+{
+    float m = fabsf(v[0]);
+#pragma unroll
+    for (int k = 1; k < 8; ++k)
+        m = fmaxf(m, fabsf(v[k]));
+    return m;
+}
+
+// writes the transposed tile (128 columns x 128 rows of codes) to qc
+__device__ __forceinline__ void store_tileT(const uint8_t *tileT, uint8_t *qc, int64_t ldq, int64_t ch0, int64_t pos0)
+{
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int L = threadIdx.x + kThreads * k;
+        const int ch = L >> 3, u = L & 7;
+        *reinterpret_cast<uint4 *>(qc + (ch0 + ch) * ldq + pos0 + u * 16) = tileT_get16(tileT, ch, u);
+    }
+}
+
+// ============================================================ kernels
+
+// Activation / gradient quantizer (1x128 row copy + 128x1 column copy).
+template <bool ROW, bool COL>
+__global__ void __launch_bounds__(kThreads, 2) k_quant_act(ActQuantArgs a)
+{
+    __shared__ __align__(16) float red[8][128];
+    __shared__ __align__(16) uint8_t tileT[128 * 128];
+    __shared__ Group grp;
+
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int rg = t >> 4, cc = t & 15;
+    const int64_t c0 = (int64_t)blockIdx.y * 128;
+
+    map_group(blockIdx.x, a.n, a.seg, a.nseg, &grp);
+    __syncthreads();
+    const int cnt = grp.cnt;
+    if (cnt == 0)
+        return;
+    const int64_t t0 = grp.t0, p0 = grp.p0;
+
+    float v[8][8];
+    load_block(a.x, a.ldx, t0, c0, cnt, rg, cc, v);
+
+    if (ROW) {
+        float rmax[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float m = absmax8(v[i]);
+#pragma unroll
+            for (int d = 1; d < 16; d <<= 1)
+                m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, d));
+            rmax[i] = m;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = rg * 8 + i;
+            const Fp32Scale sc = make_scale(rmax[i]);
+            const uint2 codes = quant8(v[i], sc);
+            if (r < cnt) {
+                *reinterpret_cast<uint2 *>(a.q_row + (t0 + r) * a.c + c0 + cc * 8) = codes;
+                if (cc == i)
+                    a.s_row[(c0 >> 7) * a.n + t0 + r] = sc.s;
+            }
+        }
+    }
+
+    if (COL) {
+        float cm[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float m = fabsf(v[0][j]);
+#pragma unroll
+            for (int i = 1; i < 8; ++i)
+                m = fmaxf(m, fabsf(v[i][j]));
+            cm[j] = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+        }
+        if (lane < 16) {
+            *reinterpret_cast<float4 *>(&red[warp][cc * 8]) = make_float4(cm[0], cm[1], cm[2], cm[3]);
+            *reinterpret_cast<float4 *>(&red[warp][cc * 8 + 4]) = make_float4(cm[4], cm[5], cm[6], cm[7]);
+        }
+        __syncthreads();
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            const float4 p = *reinterpret_cast<const float4 *>(&red[w][cc * 8]);
+            const float4 q = *reinterpret_cast<const float4 *>(&red[w][cc * 8 + 4]);
+            cm[0] = fmaxf(cm[0], p.x); cm[1] = fmaxf(cm[1], p.y);
+            cm[2] = fmaxf(cm[2], p.z); cm[3] = fmaxf(cm[3], p.w);
+            cm[4] = fmaxf(cm[4], q.x); cm[5] = fmaxf(cm[5], q.y);
+            cm[6] = fmaxf(cm[6], q.z); cm[7] = fmaxf(cm[7], q.w);
+        }
+        float scol[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const Fp32Scale sc = make_scale(cm[j]);
+            scol[j] = sc.s;
+            float col[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                col[i] = v[i][j];
+            tileT_put(tileT, cc * 8 + j, rg, quant8(col, sc));
+        }
+        if (rg == 0) {
+            float *dst = a.s_col + (p0 >> 7) * a.c + c0 + cc * 8;
+            *reinterpret_cast<float4 *>(dst) = make_float4(scol[0], scol[1], scol[2], scol[3]);
+            *reinterpret_cast<float4 *>(dst + 4) = make_float4(scol[4], scol[5], scol[6], scol[7]);
+        }
+        __syncthreads();
+        store_tileT(tileT, a.q_col, a.ldq_col, c0, p0);
+    }
+}
+
+// 8x8 byte transpose: in[i] holds bytes (row i, cols 0..7); out[j] holds
+// bytes (rows 0..7, col j).
+__device__ __forceinline__ void transpose8x8(const uint2 (&in)[8], uint2 (&out)[8])
+{
+    // interleave row pairs: p[k] = rows (2k, 2k+1)
+    uint32_t lo0[4], lo1[4], hi0[4], hi1[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        lo0[k] = __byte_perm(in[2 * k].x, in[2 * k + 1].x, 0x5140); // c0: r0 r1, c1: r0 r1
+        lo1[k] = __byte_perm(in[2 * k].x, in[2 * k + 1].x, 0x7362); // c2, c3
+        hi0[k] = __byte_perm(in[2 * k].y, in[2 * k + 1].y, 0x5140); // c4, c5
+        hi1[k] = __byte_perm(in[2 * k].y, in[2 * k + 1].y, 0x7362); // c6, c7
+    }
+    const uint32_t *src[4] = {lo0, lo1, hi0, hi1};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const uint32_t *p = src[h];
+        // column 2h: bytes 0,1 of each pair word; column 2h+1: bytes 2,3
+        out[2 * h].x = __byte_perm(p[0], p[1], 0x5410);
+        out[2 * h].y = __byte_perm(p[2], p[3], 0x5410);
+        out[2 * h + 1].x = __byte_perm(p[0], p[1], 0x7632);
+        out[2 * h + 1].y = __byte_perm(p[2], p[3], 0x7632);
+    }
+}
+
+// Weight quantizer: one scale per 128x128 block, codes + transposed codes.
+__global__ void __launch_bounds__(kThreads, 2) k_quant_weight(WeightQuantArgs a)
+{
+    __shared__ float red[8];
+    __shared__ __align__(16) uint8_t tileT[128 * 128];
+
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int rg = t >> 4, cc = t & 15;
+    const int64_t d0 = (int64_t)blockIdx.x * 128, c0 = (int64_t)blockIdx.y * 128;
+
+    float v[8][8];
+    load_block(a.w, a.ldw, d0, c0, 128, rg, cc, v);
+
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        m = fmaxf(m, absmax8(v[i]));
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, d));
+    if (lane == 0)
+        red[warp] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w)
+        m = fmaxf(m, red[w]);
+    const Fp32Scale sc = make_scale(m);
+
+    uint2 rows[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        rows[i] = quant8(v[i], sc);
+        *reinterpret_cast<uint2 *>(a.q + (d0 + rg * 8 + i) * a.c + c0 + cc * 8) = rows[i];
+    }
+    if (t == 0) {
+        a.s[(d0 >> 7) * (a.c >> 7) + (c0 >> 7)] = sc.s;
+        if (a.sT)
+            a.sT[(c0 >> 7) * (a.d >> 7) + (d0 >> 7)] = sc.s;
+    }
+    if (a.qT) {
+        uint2 cols[8];
+        transpose8x8(rows, cols);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            tileT_put(tileT, cc * 8 + j, rg, cols[j]);
+        __syncthreads();
+        store_tileT(tileT, a.qT, a.d, c0, d0);
+    }
+}
+
+// MXFP8 quantizer: 1x32 row blocks and 32x1 column blocks, E8M0 scales.
+template <bool ROW, bool COL>
+__global__ void __launch_bounds__(kThreads, 2) k_quant_mx(MxQuantArgs a)
+{
+    __shared__ __align__(16) float red[8][128];
+    __shared__ __align__(16) uint8_t tileT[128 * 128];
+    __shared__ __align__(16) uint32_t e8T[128];
+    __shared__ Group grp;
+
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int rg = t >> 4, cc = t & 15;
+    const int64_t c0 = (int64_t)blockIdx.y * 128;
+
+    map_group(blockIdx.x, a.rows, a.seg, a.nseg, &grp);
+    __syncthreads();
+    const int cnt = grp.cnt;
+    if (cnt == 0)
+        return;
+    const int64_t t0 = grp.t0, p0 = grp.p0;
+
+    float v[8][8];
+    load_block(a.x, a.ldx, t0, c0, cnt, rg, cc, v);
+
+    if (ROW) {
+        const int64_t ka = (a.cols + 511) / 512;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float m = absmax8(v[i]);
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+            const int e = e8m0_exponent(m);
+            const uint2 codes = quant8_mx(v[i], exp2_neg(e), m == 0.0f);
+            // the four 32-blocks of this row sit in lanes with cc = 0, 4, 8, 12 of the half-warp
+            const uint32_t byte = (uint32_t)(e + 127);
+            const int base = lane & 16;
+            const uint32_t b0 = __shfl_sync(0xFFFFFFFFu, byte, base + 0);
+            const uint32_t b1 = __shfl_sync(0xFFFFFFFFu, byte, base + 4);
+            const uint32_t b2 = __shfl_sync(0xFFFFFFFFu, byte, base + 8);
+            const uint32_t b3 = __shfl_sync(0xFFFFFFFFu, byte, base + 12);
+            const int r = rg * 8 + i;
+            if (r < cnt) {
+                const int64_t row = t0 + r;
+                *reinterpret_cast<uint2 *>(a.q_row + row * a.cols + c0 + cc * 8) = codes;
+                if (cc == i)
+                    *reinterpret_cast<uint32_t *>(a.e8_row + mx_atom_offset(row, c0 >> 5, ka)) =
+                        b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            }
+        }
+    }
+
+    if (COL) {
+        float cm[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            float m = fabsf(v[0][j]);
+#pragma unroll
+            for (int i = 1; i < 8; ++i)
+                m = fmaxf(m, fabsf(v[i][j]));
+            cm[j] = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16)); // rows 16w .. 16w+15
+        }
+        if (lane < 16) {
+            *reinterpret_cast<float4 *>(&red[warp][cc * 8]) = make_float4(cm[0], cm[1], cm[2], cm[3]);
+            *reinterpret_cast<float4 *>(&red[warp][cc * 8 + 4]) = make_float4(cm[4], cm[5], cm[6], cm[7]);
+        }
+        __syncthreads();
+        // 32-row block k = warp / 2 covers warps 2k and 2k+1
+        const int other = warp ^ 1;
+        const float4 p = *reinterpret_cast<const float4 *>(&red[other][cc * 8]);
+        const float4 q = *reinterpret_cast<const float4 *>(&red[other][cc * 8 + 4]);
+        cm[0] = fmaxf(cm[0], p.x); cm[1] = fmaxf(cm[1], p.y);
+        cm[2] = fmaxf(cm[2], p.z); cm[3] = fmaxf(cm[3], p.w);
+        cm[4] = fmaxf(cm[4], q.x); cm[5] = fmaxf(cm[5], q.y);
+        cm[6] = fmaxf(cm[6], q.z); cm[7] = fmaxf(cm[7], q.w);
+        const int k = warp >> 1;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int e = e8m0_exponent(cm[j]);
+            float col[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                col[i] = v[i][j];
+            tileT_put(tileT, cc * 8 + j, rg, quant8_mx(col, exp2_neg(e), cm[j] == 0.0f));
+            if ((warp & 1) == 0 && lane < 16)
+                reinterpret_cast<uint8_t *>(e8T)[(cc * 8 + j) * 4 + k] = (uint8_t)(e + 127);
+        }
+        __syncthreads();
+        store_tileT(tileT, a.q_col, a.ldq_col, c0, p0);
+        if (t < 128) {
+            const int64_t ka = (a.ldq_col + 511) / 512;
+            *reinterpret_cast<uint32_t *>(a.e8_col + mx_atom_offset(c0 + t, p0 >> 5, ka)) = e8T[t];
+        }
+    }
+}
+
+int64_t groups_upper_bound(int64_t n, const int64_t *seg, int nseg)
+{
+    const int64_t g = (n + 127) / 128;
+    return seg ? g + nseg : g;
+}
+
+} // namespace
+
+cudaError_t launch_quant_act(const ActQuantArgs &a, cudaStream_t st)
+{
+    if (a.n == 0 || (!a.q_row && !a.q_col))
+        return cudaSuccess;
+    dim3 grid((unsigned)groups_upper_bound(a.n, a.seg, a.nseg), (unsigned)(a.c / 128));
+    if (a.q_row && a.q_col)
+        k_quant_act<true, true><<<grid, kThreads, 0, st>>>(a);
+    else if (a.q_row)
+        k_quant_act<true, false><<<grid, kThreads, 0, st>>>(a);
+    else
+        k_quant_act<false, true><<<grid, kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_weight(const WeightQuantArgs &a, cudaStream_t st)
+{
+    dim3 grid((unsigned)(a.d / 128), (unsigned)(a.c / 128));
+    k_quant_weight<<<grid, kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_mx(const MxQuantArgs &a, cudaStream_t st)
+{
+    if (a.rows == 0 || (!a.q_row && !a.q_col))
+        return cudaSuccess;
+    dim3 grid((unsigned)groups_upper_bound(a.rows, a.seg, a.nseg), (unsigned)(a.cols / 128));
+    if (a.q_row && a.q_col)
+        k_quant_mx<true, true><<<grid, kThreads, 0, st>>>(a);
+    else if (a.q_row)
+        k_quant_mx<true, false><<<grid, kThreads, 0, st>>>(a);
+    else
+        k_quant_mx<false, true><<<grid, kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+} // namespace jetq

@@ -1,0 +1,80 @@
+"""The C ABI library: it builds, loads, exports every symbol include/jetq.h
+declares, and its host-side validation rejects bad arguments before any
+CUDA call (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "jetq.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from rollout_x128_act_gb300 import build
+
+    build.build()
+    import rollout_x128_act_gb300 as jq
+
+    return jq.lib()
+
+
+def declared_symbols():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"JETQ_API[^;(]*?\b(jetq_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_symbols()
+    for required in ("jetq_quant_act_1x128", "jetq_quant_w_128x128", "jetq_quant_mx32", "jetq_gemm_fprop",
+                     "jetq_gemm_dgrad", "jetq_gemm_wgrad", "jetq_check_device_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+
+
+def test_status_strings_and_sizes(L):
+    import rollout_x128_act_gb300 as jq
+
+    assert jq.status_string(0) == "ok"
+    assert "aligned" in jq.status_string(3)
+    assert jq.jetq_version() >= 100
+    assert jq.jetq_colcopy_capacity(0, 1) == 0
+    assert jq.jetq_colcopy_capacity(1, 1) == 128
+    assert jq.jetq_colcopy_capacity(8192, 1) == 8192
+    assert jq.jetq_colcopy_capacity(300, 4) >= 128 + 128 + 256  # worst case of 4 ragged segments
+    assert jq.jetq_mx_scale_bytes(1, 32) == 2048
+    assert jq.jetq_mx_scale_bytes(8192, 4096) == 64 * 8 * 2048
+    assert jq.jetq_mx_scale_bytes(2048, 768) == 16 * 2 * 2048
+
+
+def test_validation_happens_before_cuda(L):
+    P = ctypes.c_void_p
+    fake = P(4096)  # never dereferenced: every call below fails validation first
+    # C not a multiple of 128
+    assert L.jetq_quant_act_1x128(fake, 4, 100, 100, fake, fake, None, None, 0, None, 0, None) == 2
+    # q_row without s_row
+    assert L.jetq_quant_act_1x128(fake, 4, 128, 128, fake, None, None, None, 0, None, 0, None) == 1
+    # column copy too short
+    assert L.jetq_quant_act_1x128(fake, 300, 128, 128, None, None, fake, fake, 256, None, 0, None) == 2
+    # weight with D not a multiple of 128
+    assert L.jetq_quant_w_128x128(fake, 100, 128, 128, fake, fake, None, None, None) == 2
+    # misaligned weight pointer
+    assert L.jetq_quant_w_128x128(P(4097), 128, 128, 128, fake, fake, None, None, None) == 3
+    # GEMM: bad recipe, bad path, bad output stride, misaligned output
+    assert L.jetq_gemm_fprop(7, fake, fake, fake, fake, 8, 128, 128, fake, 0, 128, 0, None) == 1
+    assert L.jetq_gemm_fprop(0, fake, fake, fake, fake, 8, 128, 128, fake, 0, 128, 9, None) == 1
+    assert L.jetq_gemm_fprop(0, fake, fake, fake, fake, 8, 128, 128, fake, 0, 64, 0, None) == 2
+    assert L.jetq_gemm_fprop(0, fake, fake, fake, fake, 8, 128, 128, P(4100), 0, 128, 0, None) == 3
+    assert L.jetq_gemm_dgrad(0, fake, fake, fake, fake, 8, 100, 128, fake, 0, 128, None) == 2
+    # WGrad: K not a multiple of 128, ldk smaller than K
+    assert L.jetq_gemm_wgrad(0, fake, fake, fake, fake, 200, 256, 128, 128, fake, 128, 0, None) == 2
+    assert L.jetq_gemm_wgrad(0, fake, fake, fake, fake, 256, 128, 128, 128, fake, 128, 0, None) == 2
+    # MX: columns not a multiple of 128
+    assert L.jetq_quant_mx32(fake, 4, 96, 96, fake, fake, None, None, 0, None, 0, None) == 2
