@@ -1,0 +1,549 @@
+"""Benchmark: one dense-8B-shaped MLP training step through the FP8 path.
+
+Workload (per GPU, per step), all BF16 inputs resident in HBM:
+  X [8192 x 4096], H [8192 x 12288], W_gate, W_up [12288 x 4096],
+  W_down [4096 x 12288], dY_gate, dY_up [8192 x 12288], dY_down [8192 x 4096]
+  1. weight quantizers (128x128 blocks + transposed copies) on W_gate, W_up, W_down
+  2. activation quantizers (1x128 row + 128x1 column copies) on X and H
+  3. FProp  gate/up: X W^T, down: H W_down^T                     (BF16 out)
+  4. gradient quantizers on dY_gate, dY_up, dY_down
+  5. DGrad  dY W                                                 (BF16 out)
+  6. WGrad  dY^T X (gate, up), dY_down^T H (down)                (FP32 out)
+  = 17 kernel launches and 9 GEMMs of 2*8192*12288*4096 = 824.6 GFLOP each.
+
+value  = GEMM FLOPs of the step / wall time of the whole step (quantizers
+         included), TFLOP/s, inputs resident; every step touches ~1.07 GB of
+         inputs, several times the 129 MB L2.
+e2e    = the same through host buffers: each step copies its BF16 inputs from
+         pinned host memory and reads the three FP32 weight gradients back.
+roofline = the dominant kernel (the FProp/DGrad GEMM kernel) against the FP8
+         dense peak (measured BF16 cuBLAS peak x 2, the nominal FP8/BF16 ratio).
+
+--impl reference times the CPU oracle (oracle/) on a bounded sample of the same
+workload on the host cores.  Multi-GPU (torchrun): independent replicas, one
+per rank, no collective on the data path (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "block-scaled FP8 GEMM TFLOP/s (% dense FP8 peak); quantizer GB/s (% HBM)"
+N_TOK, C, D = 8192, 4096, 12288
+GEMM_FLOP = 2.0 * N_TOK * C * D
+GEMMS_PER_STEP = 9
+ACT_BYTES_PER_ELT = 2 + 2 * (1 + 4 / 128)      # BF16 in, two FP8 copies + FP32 scales
+W_BYTES_PER_ELT = 2 + 2 + 2 * 4 / (128 * 128)  # BF16 in, codes + transposed codes, scales
+CONFIG = {
+    "workload": "dense-8B MLP layer training step, 128-block FP8 recipe: N=8192 tokens, hidden 4096, "
+                "intermediate 12288; quantize X, H, W_gate/up/down, dY; FProp/DGrad/WGrad x3",
+    "tokens": N_TOK, "hidden": C, "intermediate": D,
+    "l2": "inputs larger than L2: ~1.07 GB of BF16 inputs read every step (L2 129 MB)",
+}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm": float(p["hbm_gbs"]), "bf16": float(p["bf16_tflops"]),
+                "bf16_sust": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "src": "measured"}
+    return {"hbm": 6800.0, "bf16": 1900.0, "bf16_sust": 1700.0, "src": "fallback"}
+
+
+def _profile_traffic(kernel_key: str, source: str):
+    """Per-launch DRAM bytes recorded by the committed ncu summary, if the kernel
+    source has not changed since it was captured (else None)."""
+    prof = os.path.join(ROOT, "profiles", f"{kernel_key}.md")
+    if not os.path.exists(prof):
+        return None
+    txt = open(prof).read()
+    m = re.search(r"traffic_bytes_per_launch:\s*([0-9.eE+]+)\s*\(source sha256 ([0-9a-f]+)\)", txt)
+    if not m:
+        return None
+    sha = hashlib.sha256(open(source, "rb").read()).hexdigest()
+    return float(m.group(1)) if sha.startswith(m.group(2)) else None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.idx}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        pass
+
+    def result(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- ours
+
+def _rank_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def _inputs_host(seed: int):
+    """The step's BF16 inputs as numpy uint16 arrays (synthetic, seeded)."""
+    import synth
+
+    return {
+        "x": synth.activation(N_TOK, C, seed=seed, stream="x"),
+        "h": synth.activation(N_TOK, D, seed=seed, stream="h"),
+        "w_gate": synth.weight(D, C, seed=seed, stream="w_gate"),
+        "w_up": synth.weight(D, C, seed=seed, stream="w_up"),
+        "w_down": synth.weight(C, D, seed=seed, stream="w_down"),
+        "dy_gate": synth.gradient(N_TOK, D, seed=seed, stream="dy_gate"),
+        "dy_up": synth.gradient(N_TOK, D, seed=seed, stream="dy_up"),
+        "dy_down": synth.gradient(N_TOK, C, seed=seed, stream="dy_down"),
+    }
+
+
+class Step:
+    """Preallocated buffers and the 17-launch step."""
+
+    def __init__(self, dev, inputs):
+        import torch
+
+        import rollout_x128_act_gb300 as jq
+
+        self.jq = jq
+        self.t = {k: torch.empty(v.shape, dtype=torch.bfloat16, device=dev) for k, v in inputs.items()}
+        e = lambda *s, dt=torch.uint8: torch.empty(s, dtype=dt, device=dev)  # noqa: E731
+        f32 = torch.float32
+        self.act = {}
+        for name, (n, c) in (("x", (N_TOK, C)), ("h", (N_TOK, D)), ("dy_gate", (N_TOK, D)), ("dy_up", (N_TOK, D)),
+                             ("dy_down", (N_TOK, C))):
+            cap = jq.jetq_colcopy_capacity(n, 1)
+            self.act[name] = dict(q_row=e(n, c), s_row=e(c // 128, n, dt=f32), q_col=e(c, cap),
+                                  s_col=e(cap // 128, c, dt=f32), cap=cap)
+        self.w = {}
+        for name, (d, c) in (("w_gate", (D, C)), ("w_up", (D, C)), ("w_down", (C, D))):
+            self.w[name] = (e(d, c), e(d // 128, c // 128, dt=f32), e(c, d), e(c // 128, d // 128, dt=f32))
+        bf = torch.bfloat16
+        self.y = {"gate": e(N_TOK, D, dt=bf), "up": e(N_TOK, D, dt=bf), "down": e(N_TOK, C, dt=bf)}
+        self.dx = {"gate": e(N_TOK, C, dt=bf), "up": e(N_TOK, C, dt=bf), "down": e(N_TOK, D, dt=bf)}
+        self.dw = {"gate": e(D, C, dt=f32), "up": e(D, C, dt=f32), "down": e(C, D, dt=f32)}
+        self.gemm_events = []
+
+    def load(self, inputs, non_blocking=False):
+        import numpy as np
+        import torch
+
+        for k, v in inputs.items():
+            src = v if isinstance(v, torch.Tensor) else torch.from_numpy(np.ascontiguousarray(v).view(np.int16))
+            self.t[k].view(torch.int16).copy_(src.view(torch.int16) if isinstance(v, torch.Tensor) else src,
+                                              non_blocking=non_blocking)
+
+    def run(self, stream=None, time_gemms=False):
+        import torch
+
+        jq = self.jq
+        launches = 0
+        for name in ("w_gate", "w_up", "w_down"):
+            q, s, qT, sT = self.w[name]
+            jq.jetq_quant_w_128x128(self.t[name], q, s, qT, sT, stream)
+            launches += 1
+
+        def qa(name):
+            a = self.act[name]
+            jq.jetq_quant_act_1x128(self.t[name], a["q_row"], a["s_row"], a["q_col"], a["s_col"], a["cap"],
+                                    None, 0, stream)
+
+        def timed(fn):
+            if time_gemms:
+                s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                st = stream or torch.cuda.current_stream()
+                s0.record(st)
+                fn()
+                s1.record(st)
+                self.gemm_events.append((s0, s1))
+            else:
+                fn()
+
+        qa("x")
+        qa("h")
+        launches += 2
+        X, H = self.act["x"], self.act["h"]
+        for g, (a, w) in (("gate", (X, "w_gate")), ("up", (X, "w_up")), ("down", (H, "w_down"))):
+            q, s, _, _ = self.w[w]
+            n, c = a["q_row"].shape
+            timed(lambda a=a, q=q, s=s, g=g, n=n, c=c: jq.jetq_gemm_fprop(
+                jq.RECIPE_BLOCK128, a["q_row"], a["s_row"], q, s, n, q.shape[0], c, self.y[g], jq.PATH_TRAIN, stream))
+            launches += 1
+        for name in ("dy_gate", "dy_up", "dy_down"):
+            qa(name)
+            launches += 1
+        for g, w in (("gate", "w_gate"), ("up", "w_up"), ("down", "w_down")):
+            a = self.act["dy_" + g]
+            _, _, qT, sT = self.w[w]
+            n, d = a["q_row"].shape
+            timed(lambda a=a, qT=qT, sT=sT, g=g, n=n, d=d: jq.jetq_gemm_dgrad(
+                jq.RECIPE_BLOCK128, a["q_row"], a["s_row"], qT, sT, n, d, qT.shape[0], self.dx[g], stream))
+            launches += 1
+        for g, xa in (("gate", X), ("up", X), ("down", H)):
+            a = self.act["dy_" + g]
+            d, c = a["q_col"].shape[0], xa["q_col"].shape[0]
+            timed(lambda a=a, xa=xa, g=g, d=d, c=c: jq.jetq_gemm_wgrad(
+                jq.RECIPE_BLOCK128, a["q_col"], a["s_col"], xa["q_col"], xa["s_col"], N_TOK, a["cap"], d, c,
+                self.dw[g], False, stream))
+            launches += 1
+        return launches
+
+
+def quant_bytes_per_step():
+    act_elts = N_TOK * C * 2 + N_TOK * D * 3  # X, dY_down ; H, dY_gate, dY_up
+    w_elts = 3 * D * C
+    return act_elts * ACT_BYTES_PER_ELT + w_elts * W_BYTES_PER_ELT
+
+
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    rank, world, local = _rank_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import __graft_entry__
+
+    __graft_entry__.build()
+    inputs = _inputs_host(seed=rank)
+    step = Step(dev, inputs)
+    step.load(inputs)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    if step.jq.jetq_check_device_error() != 0:
+        raise RuntimeError("device error word set during warm-up")
+
+    # ---- timed: inputs resident, per-GEMM events for the roofline
+    barrier()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        time.sleep(0.3)
+        ev0.record(stream)
+        launches = 0
+        for _ in range(args.steps):
+            launches += step.run(time_gemms=True)
+        ev1.record(stream)
+        torch.cuda.synchronize()
+    clocks = clk.result()
+    barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    if step.jq.jetq_check_device_error() != 0:
+        raise RuntimeError("device error word set during the timed steps")
+    gemm_ms = [a.elapsed_time(b) for a, b in step.gemm_events]
+    step.gemm_events.clear()
+
+    # ---- e2e: pinned host inputs in, weight gradients out, every step
+    pinned = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).pin_memory() for k, v in inputs.items()}
+    dw_host = {g: torch.empty(t.shape, dtype=t.dtype).pin_memory() for g, t in step.dw.items()}
+    h2d = sum(v.numel() * 2 for v in pinned.values())
+    d2h = sum(t.numel() * 4 for t in step.dw.values())
+    for _ in range(max(1, args.warmup // 2)):
+        step.load(pinned, non_blocking=True)
+        step.run()
+        for g, t in step.dw.items():
+            dw_host[g].copy_(t, non_blocking=True)
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step.load(pinned, non_blocking=True)
+        step.run()
+        for g, t in step.dw.items():
+            dw_host[g].copy_(t, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms_e2e = e0.elapsed_time(e1)
+
+    # ---- reduce over ranks (max time)
+    t = torch.tensor([ms_total, ms_e2e], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    ms_total, ms_e2e = float(t[0]), float(t[1])
+    flops = GEMM_FLOP * GEMMS_PER_STEP * args.steps * world
+    value = flops / (ms_total * 1e-3) / 1e12
+    e2e = flops / (ms_e2e * 1e-3) / 1e12
+
+    peaks = _peaks()
+    fp8_peak_sust = 2.0 * peaks["bf16_sust"]
+    # per GEMM kind: [fprop x3, dgrad x3, wgrad x3] per step
+    per = {"fprop": [], "dgrad": [], "wgrad": []}
+    kinds = ["fprop"] * 3 + ["dgrad"] * 3 + ["wgrad"] * 3
+    for i, ms in enumerate(gemm_ms):
+        per[kinds[i % 9]].append(ms)
+    blk = per["fprop"] + per["dgrad"]
+    avg_blk = statistics.mean(blk)
+    avg_wg = statistics.mean(per["wgrad"])
+    gemm_only_ms = sum(gemm_ms) / args.steps
+    achieved = GEMM_FLOP / (avg_blk * 1e-3) / 1e12
+    gemm_src = os.path.join(ROOT, "rollout_x128_act_gb300", "csrc", "gemm.cu")
+    traffic = _profile_traffic("gemm_block128_dense8b", gemm_src)
+    step_ms = ms_total / args.steps
+    quant_ms = max(step_ms - gemm_only_ms, 1e-9)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(step_ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e4m3",
+        "data": "synthetic (seeded SplitMix64 normals; 0.1% x50 outliers in activations)",
+        "config": CONFIG,
+        "roofline": {
+            "kernel": "k_gemm_b128<256,8,4,2,block-scaled B> (FProp/DGrad, training shape)",
+            "bound": "tensor",
+            "achieved": round(achieved, 1),
+            "peak": round(fp8_peak_sust, 1),
+            "unit": "TFLOP/s",
+            "frac": round(achieved / fp8_peak_sust, 4),
+            "traffic": traffic,
+            "peak_note": f"FP8 dense = 2 x {peaks['src']} sustained BF16 cuBLAS ({peaks['bf16_sust']} TFLOP/s), "
+                         "the nominal FP8/BF16 ratio",
+        },
+        "gemm": {
+            "fprop_dgrad_ms": round(avg_blk, 4), "wgrad_ms": round(avg_wg, 4),
+            "fprop_dgrad_tflops": round(achieved, 1),
+            "wgrad_tflops": round(GEMM_FLOP / (avg_wg * 1e-3) / 1e12, 1),
+            "gemm_only_tflops": round(GEMM_FLOP * GEMMS_PER_STEP / (gemm_only_ms * 1e-3) / 1e12, 1),
+            "frac_of_fp8_peak_burst": round(achieved / (2.0 * peaks["bf16"]), 4),
+        },
+        "quantizers": {
+            "bytes_per_step": quant_bytes_per_step(),
+            "ms_per_step_est": round(quant_ms, 4),
+            "gbs_est": round(quant_bytes_per_step() / (quant_ms * 1e-3) / 1e9, 1),
+            "hbm_peak_gbs": peaks["hbm"],
+            "note": "step time minus the event-timed GEMMs; per-kernel figures in profiles/",
+        },
+        "e2e": {"value": round(e2e, 2), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(args.cpu_sample_rows)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+# --------------------------------------------------------------------------- oracle
+
+_SAMPLE_CACHE = {}
+
+
+def _oracle_sample(rows: int, band: int = 1024, seed: int = 0):
+    """The oracle on a slice of the workload: quantize `rows` tokens of X (row and
+    column copies) and the first `band` output rows of W_up (128x128 blocks),
+    dequantize, FProp those tokens against that band.  Returns (seconds, flops)."""
+    import oracle
+    import synth
+
+    key = (seed, rows, band)
+    if key not in _SAMPLE_CACHE:
+        _SAMPLE_CACHE[key] = (synth.activation(N_TOK, C, seed=seed, stream="x")[:rows].copy(),
+                              synth.weight(D, C, seed=seed, stream="w_up")[:band].copy())
+    x, w = _SAMPLE_CACHE[key]
+    t0 = time.perf_counter()
+    qx, sx = oracle.quant_rowgroups(x)
+    oracle.quant_colgroups(x)
+    qw, sw, _, _ = oracle.quant_blocks(w)
+    oracle.fprop(oracle.dequant_rowgroups(qx, sx), oracle.dequant_blocks(qw, sw))
+    return time.perf_counter() - t0, 2.0 * rows * band * C
+
+
+def cpu_baseline(rows: int):
+    secs, flops = _oracle_sample(rows)
+    return {"value": round(flops / secs / 1e12, 8), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+            "sample": f"{rows} tokens of the step: 1x128 + 128x1 quantization of X[{rows}x4096], 128x128 "
+                      f"quantization of W_up[0:1024], FP64 FProp {rows}x1024x4096 "
+                      f"({secs:.1f} s, single-threaded C)"}
+
+
+def run_reference(args):
+    rank, world, _ = _rank_env()
+    if rank != 0:
+        return
+    import oracle
+
+    oracle.build()
+    for _ in range(args.warmup):
+        _oracle_sample(args.ref_rows)
+    total_s, total_f = 0.0, 0.0
+    for _ in range(args.steps):
+        s, f = _oracle_sample(args.ref_rows)
+        total_s += s
+        total_f += f
+    v = total_f / total_s / 1e12
+    sample = f"each step: {args.ref_rows} tokens of X quantized (row + column copies), W_up[0:1024] quantized " \
+             f"(128x128 blocks), FP64 FProp {args.ref_rows}x1024x4096, single-threaded C oracle"
+    line = {
+        "metric": METRIC, "value": round(v, 8), "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(1e3 * total_s / args.steps, 2), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": CONFIG,
+        "impl": "reference",
+        "cpu_baseline": {"value": round(v, 8), "unit": "TFLOP/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(v, 8), "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+PROFILE_CASES = {
+    # name: (description, inputs are all larger than the 129 MB L2)
+    "gemm_fprop": "FProp 4096 x 12288 x 4096 (training shape, BF16 out)",
+    "gemm_wgrad": "WGrad 12288 x 4096 x K=4096 (training shape, FP32 out)",
+    "decode": "FProp 8 tokens x 12288 x 12288 (decode shape, 151 MB of FP8 weight)",
+    "quant_act": "activation quantizer, X 8192 x 12288 BF16 (row + column copies)",
+    "quant_w": "weight quantizer, W 12288 x 12288 BF16 (+ transposed copy)",
+}
+
+
+def run_case(name: str, launches: int = 5):
+    """A few launches of one kernel on a mid-size case, for ncu captures."""
+    import torch
+
+    import __graft_entry__
+    import rollout_x128_act_gb300 as jq
+    import synth
+
+    __graft_entry__.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+
+    def bf16(a):
+        import numpy as np
+
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    if name in ("gemm_fprop", "gemm_wgrad", "decode"):
+        n, c, d = {"gemm_fprop": (4096, 4096, 12288), "gemm_wgrad": (4096, 4096, 12288),
+                   "decode": (8, 12288, 12288)}[name]
+        x = bf16(synth.activation(n, c, seed=0, stream="x"))
+        w = bf16(synth.weight(d, c, seed=0, stream="w_up"))
+        ax = jq.quant_act(x, col=(name == "gemm_wgrad"))
+        qw, sw, _, _ = jq.quant_weight(w, transposed=False)
+        if name == "gemm_wgrad":
+            dy = bf16(synth.gradient(n, d, seed=0, stream="dy_up"))
+            ady = jq.quant_act(dy, row=False)
+            out = torch.empty((d, c), dtype=torch.float32, device=dev)
+            fn = lambda: jq.wgrad(ady["q_col"], ady["s_col"], ax["q_col"], ax["s_col"], n, dw=out)  # noqa: E731
+        else:
+            path = jq.PATH_DECODE if name == "decode" else jq.PATH_TRAIN
+            out = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
+            fn = lambda: jq.jetq_gemm_fprop(jq.RECIPE_BLOCK128, ax["q_row"], ax["s_row"], qw, sw, n, d, c,  # noqa
+                                            out, path)
+    elif name == "quant_act":
+        x = bf16(synth.activation(8192, 12288, seed=0, stream="h"))
+        fn = lambda: jq.quant_act(x)  # noqa: E731
+    elif name == "quant_w":
+        w = bf16(synth.weight(12288, 12288, seed=0, stream="w"))
+        fn = lambda: jq.quant_weight(w)  # noqa: E731
+    else:
+        raise SystemExit(f"unknown case {name}; one of {sorted(PROFILE_CASES)}")
+    torch.cuda.synchronize()
+    for _ in range(launches):
+        fn()
+    torch.cuda.synchronize()
+    if jq.jetq_check_device_error() != 0:
+        raise RuntimeError("device error word set")
+    print(f"case {name}: {PROFILE_CASES[name]}: {launches} launches ok")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-sample-rows", type=int, default=2048)
+    ap.add_argument("--ref-rows", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default=None, help="profiling case: " + ", ".join(sorted(PROFILE_CASES)))
+    args = ap.parse_args()
+    if args.case:
+        run_case(args.case)
+        return
+    args.warmup = max(3, args.warmup)  # timing rule: at least 3 warm-up steps
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

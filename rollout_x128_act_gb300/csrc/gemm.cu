@@ -77,15 +77,17 @@ struct Cfg {
     static constexpr int kABytes = 128 * 128;
     static constexpr int kBBytes = BN * 128;
     static constexpr int kStage = kABytes + kBBytes;
-    // warpgroup 0: producer (warp 0), MMA issuer (warp 1), two idle warps;
-    // warpgroups 1..: epilogue
+    // warpgroup 0: TMA producer (warp 0), MMA issuer (warp 1), column-scale
+    // producer (warp 2, WGrad only), one idle warp; warpgroups 1..: epilogue
     static constexpr int kThreads = 128 + 32 * EPI_WARPS;
     static constexpr int kCols = BN / (EPI_WARPS / 4); // accumulator columns per epilogue thread
     static constexpr int kTmemCols = 512;
-    static constexpr int kBars = 2 * STAGES + 2 * TMEM_BUFS + 1;
-    static constexpr size_t kSmem = 1024 + (size_t)STAGES * kStage + 1024;
+    static constexpr int kSbSlots = 4;                 // column-scale ring (WGrad)
+    static constexpr int kBars = 2 * STAGES + 2 * TMEM_BUFS + 2 * kSbSlots + 1;
+    static constexpr size_t kSbBytes = (size_t)kSbSlots * BN * 4;
+    static constexpr size_t kSmem = 1024 + (size_t)STAGES * kStage + kSbBytes + 1024;
     static_assert(TMEM_BUFS * BN <= kTmemCols, "TMEM buffers exceed 512 columns");
-    static_assert(EPI_WARPS % 4 == 0 && kCols % 16 == 0, "epilogue split");
+    static_assert(EPI_WARPS % 4 == 0 && kCols % 32 == 0, "epilogue split");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
     static_assert(kBars * 8 + 16 <= 1024, "barrier area");
 };
@@ -95,9 +97,11 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     k_gemm_b128(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p)
 {
     using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS>;
+    constexpr int SB = C::kSbSlots;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(tiles + (size_t)STAGES * C::kStage);
+    float *sb_ring = reinterpret_cast<float *>(tiles + (size_t)STAGES * C::kStage);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sb_ring) + C::kSbBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
@@ -106,7 +110,9 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
     auto tfull = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto tempty = [&](int b) { return bar0 + 8u * (2 * STAGES + TMEM_BUFS + b); };
-    const uint32_t done = bar0 + 8u * (2 * STAGES + 2 * TMEM_BUFS);
+    auto sfull = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * TMEM_BUFS + s); };
+    auto sempty = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * TMEM_BUFS + SB + s); };
+    const uint32_t done = bar0 + 8u * (2 * STAGES + 2 * TMEM_BUFS + 2 * SB);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int num_tiles = p.mt * p.nt;
@@ -120,6 +126,10 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
         for (int b = 0; b < TMEM_BUFS; ++b) {
             ptx::mbar_init(tfull(b), 1);
             ptx::mbar_init(tempty(b), EPI_WARPS);
+        }
+        for (int s = 0; s < SB; ++s) {
+            ptx::mbar_init(sfull(s), 1);
+            ptx::mbar_init(sempty(s), EPI_WARPS);
         }
         ptx::mbar_init(done, 1);
         *abort_flag = 0;
@@ -139,9 +149,8 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp < 4) {
-    if (warp == 0) {
-        // ------------------------------------------------------ TMA producer
-        if (lane == 0) {
+        if (warp == 0 && lane == 0) {
+            // -------------------------------------------------- TMA producer
             const uint32_t tx = (uint32_t)((p.box_a_rows + p.box_b_rows) * 128);
             uint32_t it = 0;
             bool ok = true;
@@ -168,11 +177,8 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                     ptx::mbar_wait(full(s), (last / STAGES) & 1u, abort_flag, err, kErrTimeout, p.limit_ns, false);
                 }
             }
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        // ------------------------------------------------------ MMA issuer
-        if (lane == 0) {
+        } else if (warp == 1 && lane == 0) {
+            // -------------------------------------------------- MMA issuer
             constexpr uint32_t idesc = ptx::idesc_e4m3_f32(128, BN);
             uint32_t it = 0, tb = 0;
             bool ok = true;
@@ -201,15 +207,58 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             }
             ptx::mma_commit(done);
             ptx::mbar_wait(done, 0u, abort_flag, err, kErrTimeout, p.limit_ns, false);
+        } else if (PER_ROW_B && warp == 2 && lane == 0) {
+            // -------------------------------------------------- column-scale producer
+            // one bulk copy per K-block: Sb[kb, n0 .. n0 + BN) into a ring slot
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                int mi, ni;
+                tile_coords(tile, p.mt, p.nt, mi, ni);
+                const int64_t n0 = (int64_t)ni * BN;
+                const uint32_t bytes = (uint32_t)((p.N - n0 < BN ? p.N - n0 : BN) * 4);
+                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                    const int s = (int)(it % SB);
+                    const uint32_t ph = (it / SB) & 1u;
+                    if (!ptx::mbar_wait(sempty(s), ph ^ 1u, abort_flag, err, kErrTimeout, p.limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(sfull(s), bytes);
+                    ptx::bulk_load(ptx::smem_addr(sb_ring + (size_t)s * BN), p.sb + (int64_t)kb * p.N + n0, bytes,
+                                   sfull(s));
+                }
+            }
+            for (int s = 0; s < SB; ++s) {
+                if (it > (uint32_t)s) {
+                    const uint32_t last = (uint32_t)s + ((it - 1u - (uint32_t)s) / SB) * SB;
+                    ptx::mbar_wait(sfull(s), (last / SB) & 1u, abort_flag, err, kErrTimeout, p.limit_ns, false);
+                }
+            }
         }
         __syncwarp();
-    }
     } else {
         // ------------------------------------------------------ epilogue
+        constexpr int CH = BN >= 64 ? 16 : 32; // TMEM columns per load / wait
         const int ew = warp - 4;
         const int quarter = warp & 3; // TMEM lanes 32*quarter .. +31
         const int col0 = (ew >> 2) * C::kCols;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+
+        // scales of the next K-block (possibly of the next tile), loaded one K-block ahead
+        float sa_n = 0.0f, sb_n = 0.0f;
+        auto load_first = [&](int t) {
+            int mi, ni;
+            tile_coords(t, p.mt, p.nt, mi, ni);
+            const int64_t m = (int64_t)mi * 128 + quarter * 32 + lane;
+            const int64_t n0 = (int64_t)ni * BN + col0;
+            sa_n = m < p.M ? __ldg(p.sa + m) : 0.0f;
+            if (!PER_ROW_B)
+                sb_n = n0 < p.N ? __ldg(p.sb + (n0 >> 7) * p.num_kb) : 0.0f;
+        };
+        if ((int)blockIdx.x < num_tiles)
+            load_first(blockIdx.x);
+
         uint32_t tb = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
@@ -219,53 +268,70 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             const bool row_ok = m < p.M;
             const int64_t n0 = (int64_t)ni * BN + col0;
             const bool col_ok = n0 < p.N; // a slice past N (N % BN != 0) computes nothing it stores
+            const float *sa_ptr = p.sa + (row_ok ? m : 0);
+            const float *sb_ptr = p.sb + (col_ok ? (n0 >> 7) * p.num_kb : 0);
             float2 acc[C::kCols / 2];
 #pragma unroll
             for (int j = 0; j < C::kCols / 2; ++j)
                 acc[j] = make_float2(0.0f, 0.0f);
 
             for (int kb = 0; kb < p.num_kb; ++kb, ++tb) {
+                const float sa = sa_n;
+                const float s = PER_ROW_B ? 0.0f : __fmul_rn(sa, sb_n);
+                if (kb + 1 < p.num_kb) {
+                    sa_n = row_ok ? __ldg(sa_ptr + (int64_t)(kb + 1) * p.M) : 0.0f;
+                    if (!PER_ROW_B)
+                        sb_n = col_ok ? __ldg(sb_ptr + kb + 1) : 0.0f;
+                } else if (tile + (int)gridDim.x < num_tiles) {
+                    load_first(tile + gridDim.x);
+                }
                 const int b = (int)(tb % TMEM_BUFS);
                 const uint32_t tph = (tb / TMEM_BUFS) & 1u;
-                const float sa = row_ok ? __ldg(p.sa + (int64_t)kb * p.M + m) : 0.0f;
-                float s = 0.0f;
-                if (!PER_ROW_B && col_ok)
-                    s = __fmul_rn(sa, __ldg(p.sb + (n0 >> 7) * p.num_kb + kb));
-                const bool got = ptx::mbar_wait(tfull(b), tph, abort_flag, err, kErrTimeout, p.limit_ns);
+                const int slot = (int)(tb % SB);
+                bool got = ptx::mbar_wait(tfull(b), tph, abort_flag, err, kErrTimeout, p.limit_ns);
+                if (PER_ROW_B)
+                    got = got && ptx::mbar_wait(sfull(slot), (tb / SB) & 1u, abort_flag, err, kErrTimeout, p.limit_ns);
                 if (!__all_sync(0xFFFFFFFFu, got)) { // keep the warp converged for tcgen05.ld
                     ok = false;
                     break;
                 }
                 ptx::tc_fence_after();
+                const float *sbs = sb_ring + (size_t)slot * BN + col0;
 #pragma unroll
-                for (int ch = 0; ch < C::kCols / 16; ++ch) {
-                    uint32_t P[16];
-                    ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + (uint32_t)(b * BN + col0 + ch * 16), P);
+                for (int ch = 0; ch < C::kCols / CH; ++ch) {
+                    uint32_t P[CH];
+                    if constexpr (CH == 32)
+                        ptx::tmem_ld_32x32b_x32(tmem_base + lane_addr + (uint32_t)(b * BN + col0 + ch * CH), P);
+                    else
+                        ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + (uint32_t)(b * BN + col0 + ch * CH), P);
                     ptx::tmem_ld_wait();
-                    if (PER_ROW_B && col_ok) {
-                        const float4 *sbp = reinterpret_cast<const float4 *>(p.sb + (int64_t)kb * p.N + n0 + ch * 16);
+                    if constexpr (PER_ROW_B) {
 #pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            const float4 sb4 = __ldg(sbp + q);
+                        for (int q = 0; q < CH / 4; ++q) {
+                            const float4 sb4 = *reinterpret_cast<const float4 *>(sbs + ch * CH + 4 * q);
                             const float2 s01 = __fmul2_rn(make_float2(sa, sa), make_float2(sb4.x, sb4.y));
                             const float2 s23 = __fmul2_rn(make_float2(sa, sa), make_float2(sb4.z, sb4.w));
-                            float2 &a0 = acc[ch * 8 + 2 * q];
-                            float2 &a1 = acc[ch * 8 + 2 * q + 1];
+                            float2 &a0 = acc[ch * (CH / 2) + 2 * q];
+                            float2 &a1 = acc[ch * (CH / 2) + 2 * q + 1];
                             a0 = __ffma2_rn(make_float2(__uint_as_float(P[4 * q]), __uint_as_float(P[4 * q + 1])), s01, a0);
                             a1 = __ffma2_rn(make_float2(__uint_as_float(P[4 * q + 2]), __uint_as_float(P[4 * q + 3])), s23, a1);
                         }
-                    } else if (!PER_ROW_B) {
+                    } else {
                         const float2 s2 = make_float2(s, s);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            acc[ch * 8 + j] = __ffma2_rn(
-                                make_float2(__uint_as_float(P[2 * j]), __uint_as_float(P[2 * j + 1])), s2, acc[ch * 8 + j]);
+                        for (int j = 0; j < CH / 2; ++j)
+                            acc[ch * (CH / 2) + j] = __ffma2_rn(
+                                make_float2(__uint_as_float(P[2 * j]), __uint_as_float(P[2 * j + 1])), s2,
+                                acc[ch * (CH / 2) + j]);
                     }
                 }
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0)
+                if (lane == 0) {
                     ptx::mbar_arrive(tempty(b));
+                    if (PER_ROW_B)
+                        ptx::mbar_arrive(sempty(slot));
+                }
             }
             if (!ok)
                 break;

@@ -69,16 +69,6 @@ __device__ __forceinline__ Fp32Scale make_scale(float amax)
     return sc;
 }
 
-__device__ __forceinline__ float quotient(float x, const Fp32Scale &sc)
-{
-    if (sc.slow)
-        return __fdiv_rn(x, sc.s);
-    const float q0 = __fmul_rn(x, sc.r);
-    const float e = __fmaf_rn(-q0, sc.s, x);
-    const float q1 = __fmaf_rn(e, sc.r, q0);
-    return __uint_as_float((__float_as_uint(q1) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
-}
-
 __device__ __forceinline__ uint32_t cvt4(float a, float b, float c, float d)
 {
     const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
@@ -86,16 +76,38 @@ __device__ __forceinline__ uint32_t cvt4(float a, float b, float c, float d)
     return lo | (hi << 16);
 }
 
-// 8 values that share one scale -> 8 codes (byte k = value k)
-__device__ __forceinline__ uint2 quant8(const float (&v)[8], const Fp32Scale &sc)
+__device__ __forceinline__ float with_sign_of(float q, float x)
 {
-    if (sc.zero)
-        return make_uint2(0u, 0u);
+    return __uint_as_float((__float_as_uint(q) & 0x7FFFFFFFu) | (__float_as_uint(x) & 0x80000000u));
+}
+
+// 8 values with one scale each (s8[k], r8[k] per value) -> 8 codes, for scales
+// >= 2^-96: q0 = x*r, e = x - s*q0 (exact), q1 = q0 + e*r, two values at a time.
+__device__ __forceinline__ uint2 quant8_fast(const float (&v)[8], const float (&s8)[8], const float (&r8)[8])
+{
     float q[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-        q[k] = quotient(v[k], sc);
+    for (int k = 0; k < 8; k += 2) {
+        const float2 x2 = make_float2(v[k], v[k + 1]);
+        const float2 q0 = __fmul2_rn(x2, make_float2(r8[k], r8[k + 1]));
+        const float2 e = __ffma2_rn(q0, make_float2(-s8[k], -s8[k + 1]), x2);
+        const float2 q1 = __ffma2_rn(e, make_float2(r8[k], r8[k + 1]), q0);
+        q[k] = with_sign_of(q1.x, v[k]);
+        q[k + 1] = with_sign_of(q1.y, v[k + 1]);
+    }
     return make_uint2(cvt4(q[0], q[1], q[2], q[3]), cvt4(q[4], q[5], q[6], q[7]));
+}
+
+// One value, any scale: zero groups give 0x00, tiny scales use the IEEE division.
+__device__ __forceinline__ float quotient_general(float x, float s, float r)
+{
+    if (!(s > 0.0f))
+        return 0.0f;
+    if (s < 0x1p-96f)
+        return __fdiv_rn(x, s);
+    const float q0 = __fmul_rn(x, r);
+    const float e = __fmaf_rn(-q0, s, x);
+    return with_sign_of(__fmaf_rn(e, r, q0), x);
 }
 
 // ------------------------------------------------------------ MX recipe
@@ -124,8 +136,11 @@ __device__ __forceinline__ uint2 quant8_mx(const float (&v)[8], float mult, bool
         return make_uint2(0u, 0u);
     float q[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
-        q[k] = __fmul_rn(v[k], mult); // exact: a power of two in the normal range
+    for (int k = 0; k < 8; k += 2) { // exact: a power of two in the normal range
+        const float2 p = __fmul2_rn(make_float2(v[k], v[k + 1]), make_float2(mult, mult));
+        q[k] = p.x;
+        q[k + 1] = p.y;
+    }
     return make_uint2(cvt4(q[0], q[1], q[2], q[3]), cvt4(q[4], q[5], q[6], q[7]));
 }
 
@@ -269,18 +284,61 @@ __device__ __forceinline__ void store_tileT(const uint8_t *tileT, uint8_t *qc, i
 
 // ============================================================ kernels
 
-// Activation / gradient quantizer (1x128 row copy + 128x1 column copy).
-template <bool ROW, bool COL>
-__global__ void __launch_bounds__(kThreads, 2) k_quant_act(ActQuantArgs a)
+// The act tile again, element by element, for any scale (zero groups, scales
+// below 2^-96).  Reloads its inputs; scales come from shared memory.
+__device__ __noinline__ void quant_act_tile_general(const ActQuantArgs &a, int64_t t0, int cnt, int64_t p0,
+                                                    int64_t c0, bool row, bool col, const float *scS,
+                                                    const float *scR, uint8_t *tileT)
 {
-    __shared__ __align__(16) float red[8][128];
+    const int t = threadIdx.x, rg = t >> 4, cc = t & 15;
+    for (int i = 0; i < 8; ++i) {
+        const int r = rg * 8 + i;
+        float v[8];
+        unpack8(r < cnt ? ldg_stream(a.x + (t0 + r) * a.ldx + c0 + cc * 8) : make_uint4(0, 0, 0, 0), v);
+        if (row && r < cnt) {
+            float q[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                q[k] = quotient_general(v[k], scS[r], scR[r]);
+            *reinterpret_cast<uint2 *>(a.q_row + (t0 + r) * a.c + c0 + cc * 8) =
+                make_uint2(cvt4(q[0], q[1], q[2], q[3]), cvt4(q[4], q[5], q[6], q[7]));
+        }
+        if (col) {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int c = cc * 8 + k;
+                const float qv = quotient_general(v[k], scS[128 + c], scR[128 + c]);
+                const uint32_t code = __nv_cvt_float2_to_fp8x2(make_float2(qv, 0.0f), __NV_SATFINITE, __NV_E4M3) & 0xFFu;
+                tileT[c * 128 + ((rg ^ (c >> 3)) & 15) * 8 + i] = (uint8_t)code;
+            }
+        }
+    }
+    if (col) {
+        __syncthreads();
+        store_tileT(tileT, a.q_col, a.ldq_col, c0, p0);
+    }
+}
+
+// Activation / gradient quantizer (1x128 row copy + 128x1 column copy).
+// Each of the 256 scales of a tile (128 rows, 128 columns) is computed once,
+// by one thread, and published through shared memory.
+template <bool ROW, bool COL>
+__global__ void __launch_bounds__(kThreads, 2) k_quant_act(const __grid_constant__ ActQuantArgs a)
+{
+    __shared__ __align__(16) float redR[16][132]; // row partial maxima [column chunk][row]
+    __shared__ __align__(16) float redC[8][128];  // column partial maxima [warp][column]
+    __shared__ __align__(16) float scS[2][128];   // scales: [0] rows, [1] columns
+    __shared__ __align__(16) float scR[2][128];   // reciprocals
     __shared__ __align__(16) uint8_t tileT[128 * 128];
     __shared__ Group grp;
+    __shared__ int special; // some scale needs the general path
 
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int rg = t >> 4, cc = t & 15;
     const int64_t c0 = (int64_t)blockIdx.y * 128;
 
+    if (t == 0)
+        special = 0;
     map_group(blockIdx.x, a.n, a.seg, a.nseg, &grp);
     __syncthreads();
     const int cnt = grp.cnt;
@@ -291,29 +349,15 @@ __global__ void __launch_bounds__(kThreads, 2) k_quant_act(ActQuantArgs a)
     float v[8][8];
     load_block(a.x, a.ldx, t0, c0, cnt, rg, cc, v);
 
+    // ---- partial maxima
     if (ROW) {
-        float rmax[8];
+        float rm[8];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float m = absmax8(v[i]);
-#pragma unroll
-            for (int d = 1; d < 16; d <<= 1)
-                m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, d));
-            rmax[i] = m;
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = rg * 8 + i;
-            const Fp32Scale sc = make_scale(rmax[i]);
-            const uint2 codes = quant8(v[i], sc);
-            if (r < cnt) {
-                *reinterpret_cast<uint2 *>(a.q_row + (t0 + r) * a.c + c0 + cc * 8) = codes;
-                if (cc == i)
-                    a.s_row[(c0 >> 7) * a.n + t0 + r] = sc.s;
-            }
-        }
+        for (int i = 0; i < 8; ++i)
+            rm[i] = absmax8(v[i]);
+        *reinterpret_cast<float4 *>(&redR[cc][rg * 8]) = make_float4(rm[0], rm[1], rm[2], rm[3]);
+        *reinterpret_cast<float4 *>(&redR[cc][rg * 8 + 4]) = make_float4(rm[4], rm[5], rm[6], rm[7]);
     }
-
     if (COL) {
         float cm[8];
 #pragma unroll
@@ -325,34 +369,81 @@ __global__ void __launch_bounds__(kThreads, 2) k_quant_act(ActQuantArgs a)
             cm[j] = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
         }
         if (lane < 16) {
-            *reinterpret_cast<float4 *>(&red[warp][cc * 8]) = make_float4(cm[0], cm[1], cm[2], cm[3]);
-            *reinterpret_cast<float4 *>(&red[warp][cc * 8 + 4]) = make_float4(cm[4], cm[5], cm[6], cm[7]);
+            *reinterpret_cast<float4 *>(&redC[warp][cc * 8]) = make_float4(cm[0], cm[1], cm[2], cm[3]);
+            *reinterpret_cast<float4 *>(&redC[warp][cc * 8 + 4]) = make_float4(cm[4], cm[5], cm[6], cm[7]);
         }
-        __syncthreads();
+    }
+    __syncthreads();
+
+    // ---- one scale per thread: threads 0..127 rows, 128..255 columns
+    {
+        const bool is_row = t < 128;
+        const int k = t & 127;
+        if (is_row ? ROW : COL) {
+            float m = 0.0f;
+            if (is_row) {
 #pragma unroll
-        for (int w = 0; w < 8; ++w) {
-            const float4 p = *reinterpret_cast<const float4 *>(&red[w][cc * 8]);
-            const float4 q = *reinterpret_cast<const float4 *>(&red[w][cc * 8 + 4]);
-            cm[0] = fmaxf(cm[0], p.x); cm[1] = fmaxf(cm[1], p.y);
-            cm[2] = fmaxf(cm[2], p.z); cm[3] = fmaxf(cm[3], p.w);
-            cm[4] = fmaxf(cm[4], q.x); cm[5] = fmaxf(cm[5], q.y);
-            cm[6] = fmaxf(cm[6], q.z); cm[7] = fmaxf(cm[7], q.w);
+                for (int w = 0; w < 16; ++w)
+                    m = fmaxf(m, redR[w][k]);
+            } else {
+#pragma unroll
+                for (int w = 0; w < 8; ++w)
+                    m = fmaxf(m, redC[w][k]);
+            }
+            const Fp32Scale sc = make_scale(m);
+            scS[is_row ? 0 : 1][k] = sc.s;
+            scR[is_row ? 0 : 1][k] = sc.r;
+            if (sc.zero || sc.slow)
+                special = 1;
+            if (is_row) {
+                if (k < cnt)
+                    a.s_row[(c0 >> 7) * a.n + t0 + k] = sc.s;
+            } else {
+                a.s_col[(p0 >> 7) * a.c + c0 + k] = sc.s;
+            }
         }
-        float scol[8];
+    }
+    __syncthreads();
+    if (special) { // a zero or tiny scale somewhere in the tile (rare): slow, general path
+        quant_act_tile_general(a, t0, cnt, p0, c0, ROW, COL, &scS[0][0], &scR[0][0], tileT);
+        return;
+    }
+
+    // ---- row copy: codes straight to global (16 lanes write one 128-byte row)
+    if (ROW) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = rg * 8 + i;
+            const float s = scS[0][r], rc = scR[0][r];
+            float si[8], ri[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                si[k] = s;
+                ri[k] = rc;
+            }
+            const uint2 codes = quant8_fast(v[i], si, ri);
+            if (r < cnt)
+                *reinterpret_cast<uint2 *>(a.q_row + (t0 + r) * a.c + c0 + cc * 8) = codes;
+        }
+    }
+
+    // ---- column copy: codes transposed through shared memory
+    if (COL) {
+        float s8[8], r8[8];
+        *reinterpret_cast<float4 *>(s8) = *reinterpret_cast<const float4 *>(&scS[1][cc * 8]);
+        *reinterpret_cast<float4 *>(s8 + 4) = *reinterpret_cast<const float4 *>(&scS[1][cc * 8 + 4]);
+        *reinterpret_cast<float4 *>(r8) = *reinterpret_cast<const float4 *>(&scR[1][cc * 8]);
+        *reinterpret_cast<float4 *>(r8 + 4) = *reinterpret_cast<const float4 *>(&scR[1][cc * 8 + 4]);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            const Fp32Scale sc = make_scale(cm[j]);
-            scol[j] = sc.s;
-            float col[8];
+            float col[8], sj[8], rj[8];
 #pragma unroll
-            for (int i = 0; i < 8; ++i)
+            for (int i = 0; i < 8; ++i) {
                 col[i] = v[i][j];
-            tileT_put(tileT, cc * 8 + j, rg, quant8(col, sc));
-        }
-        if (rg == 0) {
-            float *dst = a.s_col + (p0 >> 7) * a.c + c0 + cc * 8;
-            *reinterpret_cast<float4 *>(dst) = make_float4(scol[0], scol[1], scol[2], scol[3]);
-            *reinterpret_cast<float4 *>(dst + 4) = make_float4(scol[4], scol[5], scol[6], scol[7]);
+                sj[i] = s8[j];
+                rj[i] = r8[j];
+            }
+            tileT_put(tileT, cc * 8 + j, rg, quant8_fast(col, sj, rj));
         }
         __syncthreads();
         store_tileT(tileT, a.q_col, a.ldq_col, c0, p0);
@@ -412,18 +503,36 @@ __global__ void __launch_bounds__(kThreads, 2) k_quant_weight(WeightQuantArgs a)
     for (int w = 1; w < 8; ++w)
         m = fmaxf(m, red[w]);
     const Fp32Scale sc = make_scale(m);
-
-    uint2 rows[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        rows[i] = quant8(v[i], sc);
-        *reinterpret_cast<uint2 *>(a.q + (d0 + rg * 8 + i) * a.c + c0 + cc * 8) = rows[i];
-    }
     if (t == 0) {
         a.s[(d0 >> 7) * (a.c >> 7) + (c0 >> 7)] = sc.s;
         if (a.sT)
             a.sT[(c0 >> 7) * (a.d >> 7) + (d0 >> 7)] = sc.s;
     }
+
+    uint2 rows[8];
+    if (sc.zero || sc.slow) { // rare: all-zero block or a scale below 2^-96
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float q[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                q[k] = quotient_general(v[i][k], sc.s, sc.r);
+            rows[i] = make_uint2(cvt4(q[0], q[1], q[2], q[3]), cvt4(q[4], q[5], q[6], q[7]));
+        }
+    } else {
+        float s8[8], r8[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            s8[k] = sc.s;
+            r8[k] = sc.r;
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            rows[i] = quant8_fast(v[i], s8, r8);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        *reinterpret_cast<uint2 *>(a.q + (d0 + rg * 8 + i) * a.c + c0 + cc * 8) = rows[i];
     if (a.qT) {
         uint2 cols[8];
         transpose8x8(rows, cols);
