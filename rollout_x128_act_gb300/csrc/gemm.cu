@@ -72,7 +72,7 @@ __device__ __forceinline__ void tile_coords(int t, int mt, int nt, int &mi, int 
     ni = r / gm;
 }
 
-template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS>
+template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, int CLUSTER>
 struct Cfg {
     static constexpr int kABytes = 128 * 128;
     static constexpr int kBBytes = BN * 128;
@@ -83,20 +83,32 @@ struct Cfg {
     static constexpr int kCols = BN / (EPI_WARPS / 4); // accumulator columns per epilogue thread
     static constexpr int kTmemCols = 512;
     static constexpr int kSbSlots = 4;                 // column-scale ring (WGrad)
-    static constexpr int kBars = 2 * STAGES + 2 * TMEM_BUFS + 2 * kSbSlots + 1;
+    static constexpr int kBars = 2 * STAGES + 2 * TMEM_BUFS + 2 * kSbSlots + 2;
     static constexpr size_t kSbBytes = (size_t)kSbSlots * BN * 4;
     static constexpr size_t kSmem = 1024 + (size_t)STAGES * kStage + kSbBytes + 1024;
     static_assert(TMEM_BUFS * BN <= kTmemCols, "TMEM buffers exceed 512 columns");
     static_assert(EPI_WARPS % 4 == 0 && kCols % 32 == 0, "epilogue split");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
     static_assert(kBars * 8 + 16 <= 1024, "barrier area");
+    static_assert(CLUSTER == 1 || (CLUSTER == 2 && BN % 16 == 0 && BN >= 32), "cluster pairs split B in halves");
 };
 
-template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B>
+// Work unit u (CLUSTER m-tiles sharing one n-tile) -> (first m-tile, n-tile),
+// grouped along M for L2 reuse.
+template <int CLUSTER>
+__device__ __forceinline__ void unit_coords(int u, int mt, int nt, int &mi0, int &ni)
+{
+    const int mu_count = (mt + CLUSTER - 1) / CLUSTER;
+    int mu;
+    tile_coords(u, mu_count, nt, mu, ni);
+    mi0 = mu * CLUSTER;
+}
+
+template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B, int CLUSTER>
 __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     k_gemm_b128(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p)
 {
-    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS>;
+    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS, CLUSTER>;
     constexpr int SB = C::kSbSlots;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -113,15 +125,19 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     auto sfull = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * TMEM_BUFS + s); };
     auto sempty = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * TMEM_BUFS + SB + s); };
     const uint32_t done = bar0 + 8u * (2 * STAGES + 2 * TMEM_BUFS + 2 * SB);
+    const uint32_t bye = done + 8u; // end-of-kernel handshake with the other CTA of the cluster
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int num_tiles = p.mt * p.nt;
+    const uint32_t rank = CLUSTER > 1 ? ptx::cluster_ctarank() : 0u;
+    // persistent loop over work units: CLUSTER m-tiles x one n-tile, one m-tile per CTA
+    const int num_units = ((p.mt + CLUSTER - 1) / CLUSTER) * p.nt;
+    const int unit0 = blockIdx.x / CLUSTER, unit_step = gridDim.x / CLUSTER;
     unsigned *err = &g_gemm_error;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(full(s), 1);
-            ptx::mbar_init(empty(s), 1);
+            ptx::mbar_init(empty(s), CLUSTER); // released by the MMA of every CTA that reads the stage
         }
         for (int b = 0; b < TMEM_BUFS; ++b) {
             ptx::mbar_init(tfull(b), 1);
@@ -132,6 +148,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             ptx::mbar_init(sempty(s), EPI_WARPS);
         }
         ptx::mbar_init(done, 1);
+        ptx::mbar_init(bye, 1);
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -144,19 +161,24 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
         ptx::tmem_relinquish();
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    if (CLUSTER > 1)
+        ptx::cluster_sync(); // the other CTA's barriers are initialised before any multicast
+    else
+        __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
 
     if (warp < 4) {
         if (warp == 0 && lane == 0) {
             // -------------------------------------------------- TMA producer
-            const uint32_t tx = (uint32_t)((p.box_a_rows + p.box_b_rows) * 128);
+            // B rows arriving per stage: the whole box, or both halves when paired
+            const uint32_t tx = (uint32_t)((p.box_a_rows + p.box_b_rows * CLUSTER) * 128);
             uint32_t it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                int mi, ni;
-                tile_coords(tile, p.mt, p.nt, mi, ni);
+            for (int u = unit0; u < num_units && ok; u += unit_step) {
+                int mi0, ni;
+                unit_coords<CLUSTER>(u, p.mt, p.nt, mi0, ni);
+                const int mi = mi0 + (int)rank;
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
                     const int s = (int)(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;
@@ -167,7 +189,14 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                     ptx::mbar_arrive_expect_tx(full(s), tx);
                     const uint32_t dst = ptx::smem_addr(tiles + (size_t)s * C::kStage);
                     ptx::tma_load_2d(dst, &tmA, full(s), kb * 128, mi * 128);
-                    ptx::tma_load_2d(dst + C::kABytes, &tmB, full(s), kb * 128, ni * BN);
+                    if (CLUSTER == 1) {
+                        ptx::tma_load_2d(dst + C::kABytes, &tmB, full(s), kb * 128, ni * BN);
+                    } else {
+                        // this CTA fetches one half of the shared B tile for both CTAs
+                        const int half = BN / 2;
+                        ptx::tma_load_2d_multicast(dst + C::kABytes + rank * half * 128, &tmB, full(s), kb * 128,
+                                                   ni * BN + (int)rank * half, (uint16_t)0x3);
+                    }
                 }
             }
             // drain: every copy this thread started must have landed before exit
@@ -182,7 +211,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             constexpr uint32_t idesc = ptx::idesc_e4m3_f32(128, BN);
             uint32_t it = 0, tb = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            for (int u = unit0; u < num_units && ok; u += unit_step) {
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it, ++tb) {
                     const int s = (int)(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;
@@ -201,7 +230,10 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) // 4 x K=32 (32 bytes) inside the 128-byte swizzle row
                         ptx::mma_f8f6f4(d, adesc + 2u * k, bdesc + 2u * k, idesc, k > 0 ? 1u : 0u);
-                    ptx::mma_commit(empty(s));
+                    if (CLUSTER == 1)
+                        ptx::mma_commit(empty(s));
+                    else
+                        ptx::mma_commit_multicast(empty(s), (uint16_t)0x3); // the stage holds the peer's B half too
                     ptx::mma_commit(tfull(b));
                 }
             }
@@ -212,9 +244,9 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             // one bulk copy per K-block: Sb[kb, n0 .. n0 + BN) into a ring slot
             uint32_t it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                int mi, ni;
-                tile_coords(tile, p.mt, p.nt, mi, ni);
+            for (int u = unit0; u < num_units && ok; u += unit_step) {
+                int mi0, ni;
+                unit_coords<CLUSTER>(u, p.mt, p.nt, mi0, ni);
                 const int64_t n0 = (int64_t)ni * BN;
                 const uint32_t bytes = (uint32_t)((p.N - n0 < BN ? p.N - n0 : BN) * 4);
                 for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
@@ -247,24 +279,24 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
 
         // scales of the next K-block (possibly of the next tile), loaded one K-block ahead
         float sa_n = 0.0f, sb_n = 0.0f;
-        auto load_first = [&](int t) {
-            int mi, ni;
-            tile_coords(t, p.mt, p.nt, mi, ni);
-            const int64_t m = (int64_t)mi * 128 + quarter * 32 + lane;
+        auto load_first = [&](int u) {
+            int mi0, ni;
+            unit_coords<CLUSTER>(u, p.mt, p.nt, mi0, ni);
+            const int64_t m = (int64_t)(mi0 + (int)rank) * 128 + quarter * 32 + lane;
             const int64_t n0 = (int64_t)ni * BN + col0;
             sa_n = m < p.M ? __ldg(p.sa + m) : 0.0f;
             if (!PER_ROW_B)
                 sb_n = n0 < p.N ? __ldg(p.sb + (n0 >> 7) * p.num_kb) : 0.0f;
         };
-        if ((int)blockIdx.x < num_tiles)
-            load_first(blockIdx.x);
+        if (unit0 < num_units)
+            load_first(unit0);
 
         uint32_t tb = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            int mi, ni;
-            tile_coords(tile, p.mt, p.nt, mi, ni);
-            const int64_t m = (int64_t)mi * 128 + quarter * 32 + lane;
+        for (int u = unit0; u < num_units && ok; u += unit_step) {
+            int mi0, ni;
+            unit_coords<CLUSTER>(u, p.mt, p.nt, mi0, ni);
+            const int64_t m = (int64_t)(mi0 + (int)rank) * 128 + quarter * 32 + lane;
             const bool row_ok = m < p.M;
             const int64_t n0 = (int64_t)ni * BN + col0;
             const bool col_ok = n0 < p.N; // a slice past N (N % BN != 0) computes nothing it stores
@@ -282,8 +314,8 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                     sa_n = row_ok ? __ldg(sa_ptr + (int64_t)(kb + 1) * p.M) : 0.0f;
                     if (!PER_ROW_B)
                         sb_n = col_ok ? __ldg(sb_ptr + kb + 1) : 0.0f;
-                } else if (tile + (int)gridDim.x < num_tiles) {
-                    load_first(tile + gridDim.x);
+                } else if (u + unit_step < num_units) {
+                    load_first(u + unit_step);
                 }
                 const int b = (int)(tb % TMEM_BUFS);
                 const uint32_t tph = (tb / TMEM_BUFS) & 1u;
@@ -374,6 +406,12 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, C::kTmemCols);
     }
+    if (CLUSTER > 1 && threadIdx.x == 0) {
+        // Both CTAs' MMA commits (which arrive on the other CTA's barriers) have
+        // completed; tell the peer, and stay resident until it says the same.
+        ptx::mbar_arrive_remote(ptx::map_to_cta(bye, rank ^ 1u));
+        ptx::mbar_wait(bye, 0u, abort_flag, err, kErrTimeout, p.limit_ns, false);
+    }
 }
 
 // ---------------------------------------------------------------- host side
@@ -413,12 +451,13 @@ cudaError_t make_map(CUtensorMap *map, const void *base, int64_t k_extent, int64
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B>
+template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B, int CLUSTER>
 cudaError_t run(const GemmProblem &g, cudaStream_t st)
 {
-    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS>;
-    auto kern = k_gemm_b128<BN, EPI_WARPS, STAGES, TMEM_BUFS, PER_ROW_B>;
+    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS, CLUSTER>;
+    auto kern = k_gemm_b128<BN, EPI_WARPS, STAGES, TMEM_BUFS, PER_ROW_B, CLUSTER>;
     static int configured_device = -1;
+    static int max_clusters = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
@@ -427,12 +466,29 @@ cudaError_t run(const GemmProblem &g, cudaStream_t st)
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
         if (e != cudaSuccess)
             return e;
+        if (CLUSTER > 1) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = CLUSTER;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.gridDim = dim3(CLUSTER * sm_count(), 1, 1);
+            cfg.blockDim = dim3(C::kThreads, 1, 1);
+            cfg.dynamicSmemBytes = C::kSmem;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            if ((e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg)) != cudaSuccess)
+                return e;
+            if (max_clusters <= 0)
+                return cudaErrorInvalidConfiguration;
+        }
         configured_device = dev;
     }
     // boxes never taller than the tensor; rows of a stage past the box keep
     // stale bytes, which only reach accumulator rows/columns that are not stored
     const int box_a = g.M >= 128 ? 128 : (int)((g.M + 7) / 8 * 8);
-    const int box_b = g.N >= BN ? BN : (int)((g.N + 7) / 8 * 8);
+    const int box_b = CLUSTER > 1 ? BN / 2 : (g.N >= BN ? BN : (int)((g.N + 7) / 8 * 8));
     CUtensorMap ta, tbm;
     if ((e = make_map(&ta, g.a, g.K, g.M, g.lda, box_a)) != cudaSuccess)
         return e;
@@ -453,10 +509,25 @@ cudaError_t run(const GemmProblem &g, cudaStream_t st)
     kp.out_bf16 = g.out_dtype == JETQ_OUT_BF16;
     kp.accumulate = g.accumulate;
     kp.limit_ns = kWaitLimitNs;
-    const int tiles = kp.mt * kp.nt;
-    const int grid = tiles < sm_count() ? tiles : sm_count();
-    kern<<<grid, C::kThreads, C::kSmem, st>>>(ta, tbm, kp);
-    return cudaGetLastError();
+    const int units = ((kp.mt + CLUSTER - 1) / CLUSTER) * kp.nt;
+    if (CLUSTER == 1) {
+        const int grid = units < sm_count() ? units : sm_count();
+        kern<<<grid, C::kThreads, C::kSmem, st>>>(ta, tbm, kp);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(CLUSTER * (units < max_clusters ? units : max_clusters), 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = st;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, ta, tbm, kp);
 }
 
 } // namespace
@@ -467,8 +538,8 @@ cudaError_t launch_gemm_block128(const GemmProblem &g, GemmShape shape, cudaStre
         return cudaSuccess;
     const bool per_row = g.bscale == BScale::PerRow;
     if (shape == GemmShape::Train)
-        return per_row ? run<256, 8, 4, 2, true>(g, st) : run<256, 8, 4, 2, false>(g, st);
-    return per_row ? run<32, 4, 10, 16, true>(g, st) : run<32, 4, 10, 16, false>(g, st);
+        return per_row ? run<256, 8, 4, 2, true, 1>(g, st) : run<256, 8, 4, 2, false, 1>(g, st);
+    return per_row ? run<32, 4, 10, 16, true, 1>(g, st) : run<32, 4, 10, 16, false, 1>(g, st);
 }
 
 cudaError_t gemm_read_and_clear_error(cudaStream_t st, unsigned *out)
