@@ -111,12 +111,14 @@ JETQ_API jetq_status jetq_check_device_error(void *stream);
  *   transposed copy (for DGrad): qT[c * D + d],  sT[(c / 128) * (D / 128) + d / 128]
  *
  * MXFP8 scale bytes of a K-major payload with R rows and K columns (one byte
- * per row and 32 columns) are kept in 2048-byte atoms of 128 rows x 16 scale
- * bytes, the unit the tensor-core block-scaled MMA consumes:
- *   KA = ceil(K / 512) atoms per 128-row band
- *   byte(r, j) at ((r / 128) * KA + j / 16) * 2048 + (r % 128) * 16 + j % 16,  j = k / 32
- *   size = ceil(R / 128) * KA * 2048 bytes (jetq_mx_scale_bytes)
- * Bytes for rows >= R or j >= K / 32 inside an atom are not written.
+ * per row and 32 columns, K a multiple of 128) are kept in 512-byte atoms,
+ * one per 128-row band and 128-column K-block: the unit the tensor core's
+ * block-scaled MMA reads (32 lanes x 16 bytes; lane r % 32 holds rows
+ * r % 32 + 32 * i, i = 0..3, four K sub-blocks each):
+ *   RB = ceil(R / 128) bands;  j = k / 32 (K sub-block), kb = j / 4
+ *   byte(r, j) at (kb * RB + r / 128) * 512 + (r % 32) * 16 + ((r % 128) / 32) * 4 + j % 4
+ *   size = RB * (K / 128) * 512 bytes (jetq_mx_scale_bytes)
+ * Bytes for rows >= R inside a band are not written.
  */
 
 /* Capacity (positions, a multiple of 128) a column copy of N tokens in nseg segments needs. */

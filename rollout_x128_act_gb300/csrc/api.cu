@@ -110,14 +110,14 @@ int64_t jetq_mx_scale_bytes(int64_t rows, int64_t k)
 {
     if (rows <= 0 || k <= 0)
         return 0;
-    return (rows + 127) / 128 * ((k + 511) / 512) * 2048;
+    return (rows + 127) / 128 * ((k + 127) / 128) * 512;
 }
 
 jetq_status jetq_check_device_error(void *stream)
 {
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned word = 0;
-    if (gemm_read_and_clear_error(st, &word) != cudaSuccess)
+    if (gemm_read_and_clear_error(st, &word) != cudaSuccess || gemm_mx_read_and_clear_error(st, &word) != cudaSuccess)
         return JETQ_ERR_CUDA;
     return word ? JETQ_ERR_TIMEOUT : JETQ_OK;
 }
@@ -203,9 +203,13 @@ jetq_status jetq_gemm_fprop(jetq_recipe recipe, const uint8_t *qx, const void *s
         return JETQ_OK;
     JQ_REQUIRE(qx && sx && qw && sw, JETQ_ERR_INVALID_ARG);
     JQ_REQUIRE(aligned16(qx) && aligned16(qw) && aligned16(sx) && aligned16(sw), JETQ_ERR_MISALIGNED);
-    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128, JETQ_ERR_INVALID_ARG); // MXFP8 GEMMs: not in this build
     if ((st = check_arch()) != JETQ_OK)
         return st;
+    if (recipe == JETQ_RECIPE_MXFP8) {
+        MxGemmProblem m{qx, static_cast<const uint8_t *>(sx), qw, static_cast<const uint8_t *>(sw), n, d, c, c, c,
+                        y, ldy, y_dtype, 0};
+        return from_cuda(launch_gemm_mx(m, static_cast<cudaStream_t>(stream)));
+    }
     GemmProblem g{qx, static_cast<const float *>(sx), qw, static_cast<const float *>(sw), n, d, c, c, c,
                   BScale::Block128, y, ldy, y_dtype, 0};
     const bool decode = path == JETQ_PATH_DECODE || (path == JETQ_PATH_AUTO && n <= 256);
@@ -227,9 +231,13 @@ jetq_status jetq_gemm_dgrad(jetq_recipe recipe, const uint8_t *qdy, const void *
         return JETQ_OK;
     JQ_REQUIRE(qdy && sdy && qwt && swt, JETQ_ERR_INVALID_ARG);
     JQ_REQUIRE(aligned16(qdy) && aligned16(qwt) && aligned16(sdy) && aligned16(swt), JETQ_ERR_MISALIGNED);
-    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128, JETQ_ERR_INVALID_ARG);
     if ((st = check_arch()) != JETQ_OK)
         return st;
+    if (recipe == JETQ_RECIPE_MXFP8) {
+        MxGemmProblem m{qdy, static_cast<const uint8_t *>(sdy), qwt, static_cast<const uint8_t *>(swt), n, c, d, d, d,
+                        dx, lddx, dx_dtype, 0};
+        return from_cuda(launch_gemm_mx(m, static_cast<cudaStream_t>(stream)));
+    }
     GemmProblem g{qdy, static_cast<const float *>(sdy), qwt, static_cast<const float *>(swt), n, c, d, d, d,
                   BScale::Block128, dx, lddx, dx_dtype, 0};
     return from_cuda(launch_gemm_block128(g, n <= 256 ? GemmShape::Decode : GemmShape::Train,
@@ -255,9 +263,13 @@ jetq_status jetq_gemm_wgrad(jetq_recipe recipe, const uint8_t *qdyc, const void 
     JQ_REQUIRE(qdyc && sdyc && qxc && sxc, JETQ_ERR_INVALID_ARG);
     JQ_REQUIRE(aligned16(qdyc) && aligned16(qxc) && aligned16(sdyc) && aligned16(sxc) && ldk % 16 == 0,
                JETQ_ERR_MISALIGNED);
-    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128, JETQ_ERR_INVALID_ARG);
     if ((st = check_arch()) != JETQ_OK)
         return st;
+    if (recipe == JETQ_RECIPE_MXFP8) {
+        MxGemmProblem m{qdyc, static_cast<const uint8_t *>(sdyc), qxc, static_cast<const uint8_t *>(sxc), d, c, k, ldk,
+                        ldk, dw, lddw, JETQ_OUT_F32, accumulate ? 1 : 0};
+        return from_cuda(launch_gemm_mx(m, static_cast<cudaStream_t>(stream)));
+    }
     GemmProblem g{qdyc, static_cast<const float *>(sdyc), qxc, static_cast<const float *>(sxc), d, c, k, ldk, ldk,
                   BScale::PerRow, dw, lddw, JETQ_OUT_F32, accumulate ? 1 : 0};
     return from_cuda(launch_gemm_block128(g, GemmShape::Train, static_cast<cudaStream_t>(stream)));

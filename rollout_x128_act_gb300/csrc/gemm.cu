@@ -435,8 +435,12 @@ EncodeTiledFn encode_fn()
     return fn;
 }
 
-// 2-D map over a K-major byte matrix [rows x k_extent] with row stride ld.
-cudaError_t make_map(CUtensorMap *map, const void *base, int64_t k_extent, int64_t rows, int64_t ld, int box_rows)
+} // namespace
+
+// 2-D map over a K-major byte matrix [rows x k_extent] with row stride ld:
+// boxes of 128 bytes (one K-block) x box_rows rows, 128-byte swizzle.
+cudaError_t make_kmajor_map(CUtensorMap *map, const void *base, int64_t k_extent, int64_t rows, int64_t ld,
+                            int box_rows)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
@@ -450,6 +454,8 @@ cudaError_t make_map(CUtensorMap *map, const void *base, int64_t k_extent, int64
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
+
+namespace {
 
 template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B, int CLUSTER>
 cudaError_t run(const GemmProblem &g, cudaStream_t st)
@@ -490,9 +496,9 @@ cudaError_t run(const GemmProblem &g, cudaStream_t st)
     const int box_a = g.M >= 128 ? 128 : (int)((g.M + 7) / 8 * 8);
     const int box_b = CLUSTER > 1 ? BN / 2 : (g.N >= BN ? BN : (int)((g.N + 7) / 8 * 8));
     CUtensorMap ta, tbm;
-    if ((e = make_map(&ta, g.a, g.K, g.M, g.lda, box_a)) != cudaSuccess)
+    if ((e = make_kmajor_map(&ta, g.a, g.K, g.M, g.lda, box_a)) != cudaSuccess)
         return e;
-    if ((e = make_map(&tbm, g.b, g.K, g.N, g.ldb, box_b)) != cudaSuccess)
+    if ((e = make_kmajor_map(&tbm, g.b, g.K, g.N, g.ldb, box_b)) != cudaSuccess)
         return e;
     KParams kp;
     kp.sa = g.sa;

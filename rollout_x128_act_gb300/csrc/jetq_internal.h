@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "../../include/jetq.h"
@@ -72,7 +73,30 @@ enum class GemmShape : int { Train = 0, Decode = 1 };
 
 cudaError_t launch_gemm_block128(const GemmProblem &p, GemmShape shape, cudaStream_t st);
 
+// MXFP8 GEMM: both operands K-major E4M3 with E8M0 scale atoms (include/jetq.h
+// layout; atom of (row band rb, K-block kb) at sf + (kb * RB + rb) * 512).
+struct MxGemmProblem {
+    const uint8_t *a;
+    const uint8_t *sfa; // atoms for (M rows, K)
+    const uint8_t *b;
+    const uint8_t *sfb; // atoms for (N rows, K)
+    int64_t M, N, K;
+    int64_t lda, ldb;
+    void *out;
+    int64_t ldo;
+    jetq_out_dtype out_dtype;
+    int accumulate;
+};
+
+cudaError_t launch_gemm_mx(const MxGemmProblem &p, cudaStream_t st);
+cudaError_t gemm_mx_read_and_clear_error(cudaStream_t st, unsigned *out);
+
 cudaError_t gemm_read_and_clear_error(cudaStream_t st, unsigned *out);
+
+// TMA descriptor for a K-major byte matrix [rows x k_extent], row stride ld,
+// boxes of 128 bytes x box_rows, 128-byte swizzle, zero fill out of bounds.
+cudaError_t make_kmajor_map(CUtensorMap *map, const void *base, int64_t k_extent, int64_t rows, int64_t ld,
+                            int box_rows);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

@@ -186,6 +186,48 @@ __device__ __forceinline__ void mma_f8f6f4(uint32_t d_tmem, uint64_t a_desc, uin
         : "memory");
 }
 
+// Block-scaled D[tmem] (+)= (A * 2^SFA)[smem] * (B * 2^SFB)[smem]^T, kind::mxf8f6f4,
+// one E8M0 scale per row and 32 K-elements, scale factors read from TMEM.
+__device__ __forceinline__ void mma_mxf8f6f4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Copies a 32-row x 16-byte shared-memory matrix into 4 TMEM columns of lanes
+// 0-31, replicated into each of the four 32-lane quarters.
+__device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
+// Descriptor of a K-major shared-memory matrix without swizzle whose rows are
+// 16 bytes apart (8-row core matrices 128 bytes apart).
+__device__ __forceinline__ uint64_t desc_kmajor_noswizzle_16b(uint32_t saddr)
+{
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(128 >> 4) << 16) | ((uint64_t)(128 >> 4) << 32) |
+           ((uint64_t)1 << 46);
+}
+
+// Instruction descriptor, kind::mxf8f6f4 block-scaled: E4M3 x E4M3 -> F32,
+// UE8M0 scales, both K-major; sf_id selects the byte of each 32-bit scale
+// column (the K sub-block of 32 inside a 128-wide K-block).
+__host__ __device__ constexpr uint32_t idesc_mx_e4m3(int m, int n, int sf_id)
+{
+    return ((uint32_t)sf_id << 4)           // B scale-factor id
+           | (0u << 7) | (0u << 10)         // A, B format: E4M3
+           | ((uint32_t)(n >> 3) << 17)     // N / 8
+           | (1u << 23)                     // scale format: UE8M0
+           | ((uint32_t)(m >> 4) << 24)     // M / 16
+           | ((uint32_t)sf_id << 29);       // A scale-factor id
+}
+
 // Arrives once on `bar` when every tcgen05 operation this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit(uint32_t bar)
 {

@@ -152,10 +152,10 @@ __device__ __forceinline__ float exp2_neg(int e)
     return be >= 1 && be <= 254 ? __uint_as_float((uint32_t)be << 23) : __uint_as_float(1u << (22 + be));
 }
 
-// byte offset of MX scale (row r, block j) in the 2048-byte atom layout
-__device__ __forceinline__ int64_t mx_atom_offset(int64_t r, int64_t j, int64_t ka)
+// byte offset of MX scale (row r, 32-block j) in the 512-byte atom layout; rb = bands
+__device__ __forceinline__ int64_t mx_atom_offset(int64_t r, int64_t j, int64_t rb)
 {
-    return ((r >> 7) * ka + (j >> 4)) * 2048 + (r & 127) * 16 + (j & 15);
+    return ((j >> 2) * rb + (r >> 7)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (j & 3);
 }
 
 // ------------------------------------------------------------ shared tiles
@@ -568,7 +568,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_quant_mx(MxQuantArgs a)
     load_block(a.x, a.ldx, t0, c0, cnt, rg, cc, v);
 
     if (ROW) {
-        const int64_t ka = (a.cols + 511) / 512;
+        const int64_t ka = (a.rows + 127) / 128; // row bands of the row copy
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             float m = absmax8(v[i]);
@@ -632,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_quant_mx(MxQuantArgs a)
         __syncthreads();
         store_tileT(tileT, a.q_col, a.ldq_col, c0, p0);
         if (t < 128) {
-            const int64_t ka = (a.ldq_col + 511) / 512;
+            const int64_t ka = (a.cols + 127) / 128; // row bands of the column copy (rows = channels)
             *reinterpret_cast<uint32_t *>(a.e8_col + mx_atom_offset(c0 + t, p0 >> 5, ka)) = e8T[t];
         }
     }

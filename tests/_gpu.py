@@ -19,15 +19,19 @@ def f32bits(t) -> np.ndarray:
     return np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
 
 
-def mx_atoms(e8_logical: np.ndarray, k: int) -> np.ndarray:
-    """Places logical MX scale bytes [R x K/32] into the documented 2048-byte atom layout."""
-    R, J = e8_logical.shape
-    ka = (k + 511) // 512
-    out = np.zeros(((R + 127) // 128) * ka * 2048, np.uint8)
+def mx_atom_offsets(R: int, J: int) -> np.ndarray:
+    """Byte offset of logical MX scale (r, j) in the documented 512-byte atom layout."""
+    rb = (R + 127) // 128
     r = np.arange(R)[:, None]
     j = np.arange(J)[None, :]
-    off = ((r // 128) * ka + j // 16) * 2048 + (r % 128) * 16 + j % 16
-    out[off] = e8_logical
+    return ((j // 4) * rb + r // 128) * 512 + (r % 32) * 16 + ((r % 128) // 32) * 4 + j % 4
+
+
+def mx_atoms(e8_logical: np.ndarray, k: int) -> np.ndarray:
+    """Places logical MX scale bytes [R x K/32] into the atom layout for a K-column payload."""
+    R, J = e8_logical.shape
+    out = np.zeros(((R + 127) // 128) * (k // 128) * 512, np.uint8)
+    out[mx_atom_offsets(R, J)] = e8_logical
     return out
 
 

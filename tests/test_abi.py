@@ -49,9 +49,9 @@ def test_status_strings_and_sizes(L):
     assert jq.jetq_colcopy_capacity(1, 1) == 128
     assert jq.jetq_colcopy_capacity(8192, 1) == 8192
     assert jq.jetq_colcopy_capacity(300, 4) >= 128 + 128 + 256  # worst case of 4 ragged segments
-    assert jq.jetq_mx_scale_bytes(1, 32) == 2048
-    assert jq.jetq_mx_scale_bytes(8192, 4096) == 64 * 8 * 2048
-    assert jq.jetq_mx_scale_bytes(2048, 768) == 16 * 2 * 2048
+    assert jq.jetq_mx_scale_bytes(1, 128) == 512
+    assert jq.jetq_mx_scale_bytes(8192, 4096) == 64 * 32 * 512
+    assert jq.jetq_mx_scale_bytes(2048, 768) == 16 * 6 * 512
 
 
 def test_validation_happens_before_cuda(L):
