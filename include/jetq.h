@@ -71,6 +71,12 @@ typedef enum {
 } jetq_path;
 
 typedef enum {
+    JETQ_GEMM_FPROP = 0,
+    JETQ_GEMM_DGRAD = 1,
+    JETQ_GEMM_WGRAD = 2
+} jetq_gemm_kind;
+
+typedef enum {
     JETQ_OUT_F32 = 0,
     JETQ_OUT_BF16 = 1 /* round-to-nearest-even of the FP32 result */
 } jetq_out_dtype;
@@ -244,6 +250,42 @@ JETQ_API jetq_status jetq_gemm_wgrad(jetq_recipe recipe,
                             const uint8_t *qxc, const void *sxc,
                             int64_t k, int64_t ldk, int64_t d, int64_t c,
                             float *dw, int64_t lddw, int accumulate, void *stream);
+
+/*
+ * Grouped GEMMs for MoE experts (Miles Blackwell post: MoE expert GEMMs are
+ * quantized like every other linear layer).  Routed rows are sorted by expert:
+ * expert e owns rows seg_offsets[e] .. seg_offsets[e+1]-1 (device int64
+ * [num_experts + 1], from 0 to the routed-row count; values are clamped on the
+ * device, so bad offsets give wrong sums but never out-of-bounds accesses).
+ * Every expert runs the same arithmetic as the matching dense GEMM.
+ *
+ *   FPROP  a = routed activations, row copy [m x ldk] (K = k);  b = expert
+ *          weights stacked [num_experts x n x ldk];  out [m x n], row r of
+ *          expert e = a[r] * W_e^T.
+ *   DGRAD  a = routed output gradients, row copy [m x ldk] (K = k = D);
+ *          b = expert transposed weights stacked [num_experts x n x ldk]
+ *          (n = C); out [m x n].
+ *   WGRAD  a = output-gradient column copy [m x ldk] (m = D), b = activation
+ *          column copy [n x ldk] (n = C), both made by the quantizers with
+ *          these segment offsets (k = column-copy length); out = FP32 expert
+ *          gradients stacked [num_experts x m x n] (expert stride m * ldo);
+ *          an expert with no rows gets zeros (or is left unchanged with
+ *          accumulate).
+ *
+ * Scales.  BLOCK128: FPROP/DGRAD sa [k/128 x m], sb [num_experts x n/128 x
+ * k/128] (each expert's 128x128 grid); WGRAD sa [k/128 x m], sb [k/128 x n].
+ * MXFP8: FPROP/DGRAD sa = atoms for (m, k), sb = each expert's atoms for
+ * (n, k) stacked jetq_mx_scale_bytes(n, k) apart; WGRAD sa, sb = atoms of the
+ * two column copies.
+ * Limits: 1 <= num_experts <= 256; n, k multiples of 128; ldk >= k, a
+ * multiple of 16.
+ */
+JETQ_API jetq_status jetq_gemm_grouped(jetq_gemm_kind kind, jetq_recipe recipe,
+                                       const uint8_t *a, const void *sa, const uint8_t *b, const void *sb,
+                                       int64_t m, int64_t n, int64_t k, int64_t ldk,
+                                       const int64_t *seg_offsets, int num_experts,
+                                       void *out, jetq_out_dtype out_dtype, int64_t ldo, int accumulate,
+                                       void *stream);
 
 #ifdef __cplusplus
 }

@@ -24,6 +24,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libjetq.so")
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(7)
 RECIPE_BLOCK128, RECIPE_MXFP8 = 0, 1
 PATH_AUTO, PATH_TRAIN, PATH_DECODE = 0, 1, 2
+GEMM_FPROP, GEMM_DGRAD, GEMM_WGRAD = 0, 1, 2
 OUT_F32, OUT_BF16 = 0, 1
 
 _lock = threading.Lock()
@@ -58,6 +59,7 @@ def lib() -> ctypes.CDLL:
             "jetq_gemm_fprop": (I32, [I32, P, P, P, P, I64, I64, I64, P, I32, I64, I32, P]),
             "jetq_gemm_dgrad": (I32, [I32, P, P, P, P, I64, I64, I64, P, I32, I64, P]),
             "jetq_gemm_wgrad": (I32, [I32, P, P, P, P, I64, I64, I64, I64, P, I64, I32, P]),
+            "jetq_gemm_grouped": (I32, [I32, I32, P, P, P, P, I64, I64, I64, I64, P, I32, P, I32, I64, I32, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -143,6 +145,13 @@ def jetq_gemm_wgrad(recipe, qdyc, sdyc, qxc, sxc, k, ldk, d, c, dw, accumulate=F
                                  dw.stride(0), 1 if accumulate else 0, _s(stream)), "jetq_gemm_wgrad")
 
 
+def jetq_gemm_grouped(kind, recipe, a, sa, b, sb, m, n, k, ldk, seg_offsets, num_experts, out, accumulate=False,
+                      stream=None):
+    _check(lib().jetq_gemm_grouped(kind, recipe, _p(a), _p(sa), _p(b), _p(sb), m, n, k, ldk, _p(seg_offsets),
+                                   num_experts, _p(out), _out_dtype(out), out.stride(-2), 1 if accumulate else 0,
+                                   _s(stream)), "jetq_gemm_grouped")
+
+
 # ------------------------------------------------------------------ allocating helpers
 
 def quant_act(x, row=True, col=True, seg_offsets=None, stream=None):
@@ -214,3 +223,21 @@ def wgrad(qdyc, sdyc, qxc, sxc, k, dw=None, accumulate=False, recipe=RECIPE_BLOC
         dw = torch.empty((d, c), dtype=torch.float32, device=qdyc.device)
     jetq_gemm_wgrad(recipe, qdyc, sdyc, qxc, sxc, k, ldk, d, c, dw, accumulate, stream)
     return dw
+
+
+def grouped(kind, a, sa, b, sb, seg_offsets, n, k, out_dtype=torch.float32, recipe=RECIPE_BLOCK128, out=None,
+            accumulate=False, stream=None):
+    """Per-expert GEMMs over routed rows (see jetq_gemm_grouped).
+
+    FPROP/DGRAD: a [m x k] routed row copy, b stacked [E*n x k] (or [E, n, k]); returns [m x n].
+    WGRAD: a, b column copies [m x ldk], [n x ldk]; k = column-copy length; returns [E x m x n] FP32.
+    """
+    E = seg_offsets.numel() - 1
+    m, ldk = a.shape[0], a.shape[1]
+    if out is None:
+        if kind == GEMM_WGRAD:
+            out = torch.empty((E, m, n), dtype=torch.float32, device=a.device)
+        else:
+            out = torch.empty((m, n), dtype=out_dtype, device=a.device)
+    jetq_gemm_grouped(kind, recipe, a, sa, b, sb, m, n, k, ldk, seg_offsets, E, out, accumulate, stream)
+    return out

@@ -275,4 +275,54 @@ jetq_status jetq_gemm_wgrad(jetq_recipe recipe, const uint8_t *qdyc, const void 
     return from_cuda(launch_gemm_block128(g, GemmShape::Train, static_cast<cudaStream_t>(stream)));
 }
 
+jetq_status jetq_gemm_grouped(jetq_gemm_kind kind, jetq_recipe recipe, const uint8_t *a, const void *sa,
+                              const uint8_t *b, const void *sb, int64_t m, int64_t n, int64_t k, int64_t ldk,
+                              const int64_t *seg_offsets, int num_experts, void *out, jetq_out_dtype out_dtype,
+                              int64_t ldo, int accumulate, void *stream)
+{
+    JQ_REQUIRE(kind == JETQ_GEMM_FPROP || kind == JETQ_GEMM_DGRAD || kind == JETQ_GEMM_WGRAD, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128 || recipe == JETQ_RECIPE_MXFP8, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(m >= 0 && n > 0 && k >= 0 && seg_offsets != nullptr, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(num_experts >= 1 && num_experts <= 256, JETQ_ERR_UNSUPPORTED_SHAPE);
+    JQ_REQUIRE(n % 128 == 0 && k % 128 == 0 && ldk >= k, JETQ_ERR_UNSUPPORTED_SHAPE);
+    const bool wgrad = kind == JETQ_GEMM_WGRAD;
+    JQ_REQUIRE(!wgrad || m % 128 == 0, JETQ_ERR_UNSUPPORTED_SHAPE);
+    JQ_REQUIRE(!(accumulate && (!wgrad || out_dtype != JETQ_OUT_F32)), JETQ_ERR_INVALID_ARG);
+    jetq_status st = check_out(out, wgrad ? JETQ_OUT_F32 : out_dtype, ldo, n);
+    if (st != JETQ_OK)
+        return st;
+    if (wgrad)
+        JQ_REQUIRE(out_dtype == JETQ_OUT_F32, JETQ_ERR_INVALID_ARG);
+    if (m == 0 || (k == 0 && !wgrad))
+        return JETQ_OK;
+    if (k == 0) { // WGrad over no tokens: every expert's gradient is zero
+        if (accumulate)
+            return JETQ_OK;
+        return from_cuda(cudaMemset2DAsync(out, (size_t)ldo * 4, 0, (size_t)n * 4, (size_t)(m * num_experts),
+                                           static_cast<cudaStream_t>(stream)));
+    }
+    JQ_REQUIRE(a && sa && b && sb, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(aligned16(a) && aligned16(b) && aligned16(sa) && aligned16(sb) && ldk % 16 == 0 &&
+                   (reinterpret_cast<uintptr_t>(seg_offsets) & 7u) == 0,
+               JETQ_ERR_MISALIGNED);
+    if ((st = check_arch()) != JETQ_OK)
+        return st;
+    const cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    if (recipe == JETQ_RECIPE_MXFP8) {
+        MxGemmProblem mp{a, static_cast<const uint8_t *>(sa), b, static_cast<const uint8_t *>(sb), m, n, k, ldk, ldk,
+                         out, ldo, wgrad ? JETQ_OUT_F32 : out_dtype, accumulate ? 1 : 0};
+        mp.group = wgrad ? GroupKind::K : GroupKind::Rows;
+        mp.seg = seg_offsets;
+        mp.num_experts = num_experts;
+        return from_cuda(launch_gemm_mx(mp, cs));
+    }
+    GemmProblem g{a, static_cast<const float *>(sa), b, static_cast<const float *>(sb), m, n, k, ldk, ldk,
+                  wgrad ? BScale::PerRow : BScale::Block128, out, ldo, wgrad ? JETQ_OUT_F32 : out_dtype,
+                  accumulate ? 1 : 0};
+    g.group = wgrad ? GroupKind::K : GroupKind::Rows;
+    g.seg = seg_offsets;
+    g.num_experts = num_experts;
+    return from_cuda(launch_gemm_block128(g, GemmShape::Train, cs));
+}
+
 } // extern "C"

@@ -14,16 +14,19 @@
 //   warp 1        MMA issuer: 4 x tcgen05.mma (K = 32 each) per K-block into
 //                 TMEM buffer kb % TMEM_BUFS, then tcgen05.commit to release
 //                 the smem stage and to signal the epilogue
-//   warps 2..     epilogue: tcgen05.ld the K-block partial, acc = fma(P, s, acc)
+//   warp 2        (WGrad) bulk copies of the per-column scales into a ring
+//   warp 3        builds the per-expert tile tables of a grouped launch
+//   warps 4..     epilogue: tcgen05.ld the K-block partial, acc = fma(P, s, acc)
 //                 in registers (packed f32x2), release the TMEM buffer; after
 //                 the last K-block, store the tile
 //
-// One CTA per SM, persistent over output tiles (grouped raster for L2 reuse).
-// The same template serves the training shape (BN = 256, 8 epilogue warps,
-// 2 TMEM buffers) and the decode shape (BN = 32, 4 epilogue warps, 16 TMEM
-// buffers, a narrow weight slice per CTA so the weight stream spreads over
-// every SM).  Both perform the identical per-element operation sequence, so a
-// decode row equals the corresponding training row bit for bit.
+// One CTA per SM, persistent over output tiles.  The same template serves the
+// training shape (BN = 256, 8 epilogue warps, 2 TMEM buffers) and the decode
+// shape (BN = 32, 4 epilogue warps, 16 TMEM buffers, a narrow weight slice per
+// CTA so the weight stream spreads over every SM).  Both perform the identical
+// per-element operation sequence, so a decode row equals the corresponding
+// training row bit for bit.  Grouped launches (MoE experts) run the same
+// loop over per-expert tiles (sched.cuh).
 //
 // Every mbarrier wait is bounded (wall clock); a CTA that gives up raises a
 // shared abort flag, records the fact in the device error word, drains its
@@ -36,6 +39,7 @@
 
 #include "jetq_internal.h"
 #include "ptx.cuh"
+#include "sched.cuh"
 
 namespace jetq {
 
@@ -43,72 +47,52 @@ __device__ unsigned g_gemm_error;
 
 namespace {
 
-constexpr int kGroupM = 8;
 constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull; // 2 s per wait
 
 struct KParams {
-    const float *sa;
-    const float *sb;
-    int64_t M, N;
-    int num_kb;
-    int mt, nt;
+    Sched sched;
+    const float *sa;        // [K-blocks x sa_ld]
+    const float *sb;        // Block128: [E x N/128 x kb_total]; PerRow: [K-blocks x N]
+    int64_t sa_ld;          // rows of the A scale grid
+    int kb_total;           // K-blocks of one weight's scale grid (Block128)
+    int64_t sb_e_stride;    // floats between experts' weight scales
     int box_a_rows;
     int box_b_rows;
     void *out;
     int64_t ldo;
+    int64_t out_e_stride;   // elements between experts' outputs (grouped K)
     int out_bf16;
     int accumulate;
     unsigned long long limit_ns;
 };
 
-__device__ __forceinline__ void tile_coords(int t, int mt, int nt, int &mi, int &ni)
-{
-    const int group = kGroupM * nt;
-    const int first_m = (t / group) * kGroupM;
-    const int gm = min(mt - first_m, kGroupM);
-    const int r = t % group;
-    mi = first_m + r % gm;
-    ni = r / gm;
-}
-
-template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, int CLUSTER>
+template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS>
 struct Cfg {
     static constexpr int kABytes = 128 * 128;
     static constexpr int kBBytes = BN * 128;
     static constexpr int kStage = kABytes + kBBytes;
     // warpgroup 0: TMA producer (warp 0), MMA issuer (warp 1), column-scale
-    // producer (warp 2, WGrad only), one idle warp; warpgroups 1..: epilogue
+    // producer (warp 2, WGrad), group tables (warp 3); warpgroups 1..: epilogue
     static constexpr int kThreads = 128 + 32 * EPI_WARPS;
     static constexpr int kCols = BN / (EPI_WARPS / 4); // accumulator columns per epilogue thread
     static constexpr int kTmemCols = 512;
     static constexpr int kSbSlots = 4;                 // column-scale ring (WGrad)
-    static constexpr int kBars = 2 * STAGES + 2 * TMEM_BUFS + 2 * kSbSlots + 2;
+    static constexpr int kBars = 2 * STAGES + 2 * TMEM_BUFS + 2 * kSbSlots + 1;
     static constexpr size_t kSbBytes = (size_t)kSbSlots * BN * 4;
-    static constexpr size_t kSmem = 1024 + (size_t)STAGES * kStage + kSbBytes + 1024;
+    static constexpr size_t kSmem =
+        1024 + (size_t)STAGES * kStage + kSbBytes + 1024 + sizeof(GroupTables);
     static_assert(TMEM_BUFS * BN <= kTmemCols, "TMEM buffers exceed 512 columns");
     static_assert(EPI_WARPS % 4 == 0 && kCols % 32 == 0, "epilogue split");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
     static_assert(kBars * 8 + 16 <= 1024, "barrier area");
-    static_assert(CLUSTER == 1 || (CLUSTER == 2 && BN % 16 == 0 && BN >= 32), "cluster pairs split B in halves");
 };
 
-// Work unit u (CLUSTER m-tiles sharing one n-tile) -> (first m-tile, n-tile),
-// grouped along M for L2 reuse.
-template <int CLUSTER>
-__device__ __forceinline__ void unit_coords(int u, int mt, int nt, int &mi0, int &ni)
-{
-    const int mu_count = (mt + CLUSTER - 1) / CLUSTER;
-    int mu;
-    tile_coords(u, mu_count, nt, mu, ni);
-    mi0 = mu * CLUSTER;
-}
-
-template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B, int CLUSTER>
+template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B>
 __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     k_gemm_b128(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p)
 {
-    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS, CLUSTER>;
+    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS>;
     constexpr int SB = C::kSbSlots;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -116,6 +100,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sb_ring) + C::kSbBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    GroupTables *gt = reinterpret_cast<GroupTables *>(reinterpret_cast<uint8_t *>(bars) + 1024);
 
     const uint32_t bar0 = ptx::smem_addr(bars);
     auto full = [&](int s) { return bar0 + 8u * s; };
@@ -125,19 +110,15 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     auto sfull = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * TMEM_BUFS + s); };
     auto sempty = [&](int s) { return bar0 + 8u * (2 * STAGES + 2 * TMEM_BUFS + SB + s); };
     const uint32_t done = bar0 + 8u * (2 * STAGES + 2 * TMEM_BUFS + 2 * SB);
-    const uint32_t bye = done + 8u; // end-of-kernel handshake with the other CTA of the cluster
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = CLUSTER > 1 ? ptx::cluster_ctarank() : 0u;
-    // persistent loop over work units: CLUSTER m-tiles x one n-tile, one m-tile per CTA
-    const int num_units = ((p.mt + CLUSTER - 1) / CLUSTER) * p.nt;
-    const int unit0 = blockIdx.x / CLUSTER, unit_step = gridDim.x / CLUSTER;
+    const Sched &sc = p.sched;
     unsigned *err = &g_gemm_error;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(full(s), 1);
-            ptx::mbar_init(empty(s), CLUSTER); // released by the MMA of every CTA that reads the stage
+            ptx::mbar_init(empty(s), 1);
         }
         for (int b = 0; b < TMEM_BUFS; ++b) {
             ptx::mbar_init(tfull(b), 1);
@@ -148,7 +129,6 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             ptx::mbar_init(sempty(s), EPI_WARPS);
         }
         ptx::mbar_init(done, 1);
-        ptx::mbar_init(bye, 1);
         *abort_flag = 0;
         ptx::fence_barrier_init();
     }
@@ -160,26 +140,23 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::kTmemCols);
         ptx::tmem_relinquish();
     }
+    if (warp == 3 && sc.mode != kDense)
+        build_group_tables(sc, gt);
     ptx::tc_fence_before();
-    if (CLUSTER > 1)
-        ptx::cluster_sync(); // the other CTA's barriers are initialised before any multicast
-    else
-        __syncthreads();
+    __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    const int num_tiles = total_tiles(sc, gt);
 
     if (warp < 4) {
         if (warp == 0 && lane == 0) {
             // -------------------------------------------------- TMA producer
-            // B rows arriving per stage: the whole box, or both halves when paired
-            const uint32_t tx = (uint32_t)((p.box_a_rows + p.box_b_rows * CLUSTER) * 128);
+            const uint32_t tx = (uint32_t)((p.box_a_rows + p.box_b_rows) * 128);
             uint32_t it = 0;
             bool ok = true;
-            for (int u = unit0; u < num_units && ok; u += unit_step) {
-                int mi0, ni;
-                unit_coords<CLUSTER>(u, p.mt, p.nt, mi0, ni);
-                const int mi = mi0 + (int)rank;
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const TileInfo ti = get_tile(sc, gt, t);
+                for (int kb = 0; kb < ti.num_kb; ++kb, ++it) {
                     const int s = (int)(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;
                     if (!ptx::mbar_wait(empty(s), ph ^ 1u, abort_flag, err, kErrTimeout, p.limit_ns)) {
@@ -188,15 +165,8 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                     }
                     ptx::mbar_arrive_expect_tx(full(s), tx);
                     const uint32_t dst = ptx::smem_addr(tiles + (size_t)s * C::kStage);
-                    ptx::tma_load_2d(dst, &tmA, full(s), kb * 128, mi * 128);
-                    if (CLUSTER == 1) {
-                        ptx::tma_load_2d(dst + C::kABytes, &tmB, full(s), kb * 128, ni * BN);
-                    } else {
-                        // this CTA fetches one half of the shared B tile for both CTAs
-                        const int half = BN / 2;
-                        ptx::tma_load_2d_multicast(dst + C::kABytes + rank * half * 128, &tmB, full(s), kb * 128,
-                                                   ni * BN + (int)rank * half, (uint16_t)0x3);
-                    }
+                    ptx::tma_load_2d(dst, &tmA, full(s), (ti.kb0 + kb) * 128, ti.a_row0);
+                    ptx::tma_load_2d(dst + C::kABytes, &tmB, full(s), (ti.kb0 + kb) * 128, ti.b_row0);
                 }
             }
             // drain: every copy this thread started must have landed before exit
@@ -211,8 +181,9 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             constexpr uint32_t idesc = ptx::idesc_e4m3_f32(128, BN);
             uint32_t it = 0, tb = 0;
             bool ok = true;
-            for (int u = unit0; u < num_units && ok; u += unit_step) {
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it, ++tb) {
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const TileInfo ti = get_tile(sc, gt, t);
+                for (int kb = 0; kb < ti.num_kb; ++kb, ++it, ++tb) {
                     const int s = (int)(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;
                     const int b = (int)(tb % TMEM_BUFS);
@@ -230,10 +201,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
 #pragma unroll
                     for (int k = 0; k < 4; ++k) // 4 x K=32 (32 bytes) inside the 128-byte swizzle row
                         ptx::mma_f8f6f4(d, adesc + 2u * k, bdesc + 2u * k, idesc, k > 0 ? 1u : 0u);
-                    if (CLUSTER == 1)
-                        ptx::mma_commit(empty(s));
-                    else
-                        ptx::mma_commit_multicast(empty(s), (uint16_t)0x3); // the stage holds the peer's B half too
+                    ptx::mma_commit(empty(s));
                     ptx::mma_commit(tfull(b));
                 }
             }
@@ -244,12 +212,10 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             // one bulk copy per K-block: Sb[kb, n0 .. n0 + BN) into a ring slot
             uint32_t it = 0;
             bool ok = true;
-            for (int u = unit0; u < num_units && ok; u += unit_step) {
-                int mi0, ni;
-                unit_coords<CLUSTER>(u, p.mt, p.nt, mi0, ni);
-                const int64_t n0 = (int64_t)ni * BN;
-                const uint32_t bytes = (uint32_t)((p.N - n0 < BN ? p.N - n0 : BN) * 4);
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const TileInfo ti = get_tile(sc, gt, t);
+                const uint32_t bytes = (uint32_t)((sc.N - ti.n0 < BN ? sc.N - ti.n0 : BN) * 4);
+                for (int kb = 0; kb < ti.num_kb; ++kb, ++it) {
                     const int s = (int)(it % SB);
                     const uint32_t ph = (it / SB) & 1u;
                     if (!ptx::mbar_wait(sempty(s), ph ^ 1u, abort_flag, err, kErrTimeout, p.limit_ns)) {
@@ -257,8 +223,8 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                         break;
                     }
                     ptx::mbar_arrive_expect_tx(sfull(s), bytes);
-                    ptx::bulk_load(ptx::smem_addr(sb_ring + (size_t)s * BN), p.sb + (int64_t)kb * p.N + n0, bytes,
-                                   sfull(s));
+                    ptx::bulk_load(ptx::smem_addr(sb_ring + (size_t)s * BN),
+                                   p.sb + (int64_t)(ti.kb0 + kb) * sc.N + ti.n0, bytes, sfull(s));
                 }
             }
             for (int s = 0; s < SB; ++s) {
@@ -279,43 +245,44 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
 
         // scales of the next K-block (possibly of the next tile), loaded one K-block ahead
         float sa_n = 0.0f, sb_n = 0.0f;
-        auto load_first = [&](int u) {
-            int mi0, ni;
-            unit_coords<CLUSTER>(u, p.mt, p.nt, mi0, ni);
-            const int64_t m = (int64_t)(mi0 + (int)rank) * 128 + quarter * 32 + lane;
-            const int64_t n0 = (int64_t)ni * BN + col0;
-            sa_n = m < p.M ? __ldg(p.sa + m) : 0.0f;
+        auto load_first = [&](const TileInfo &ti) {
+            const int64_t m = (int64_t)ti.a_row0 + quarter * 32 + lane;
+            const int n0 = ti.n0 + col0;
+            sa_n = (m < sc.M && ti.num_kb > 0) ? __ldg(p.sa + (int64_t)ti.kb0 * p.sa_ld + m) : 0.0f;
             if (!PER_ROW_B)
-                sb_n = n0 < p.N ? __ldg(p.sb + (n0 >> 7) * p.num_kb) : 0.0f;
+                sb_n = (n0 < sc.N && ti.num_kb > 0)
+                           ? __ldg(p.sb + ti.e * p.sb_e_stride + (int64_t)(n0 >> 7) * p.kb_total + ti.kb0)
+                           : 0.0f;
         };
-        if (unit0 < num_units)
-            load_first(unit0);
+        if ((int)blockIdx.x < num_tiles)
+            load_first(get_tile(sc, gt, blockIdx.x));
 
         uint32_t tb = 0;
         bool ok = true;
-        for (int u = unit0; u < num_units && ok; u += unit_step) {
-            int mi0, ni;
-            unit_coords<CLUSTER>(u, p.mt, p.nt, mi0, ni);
-            const int64_t m = (int64_t)(mi0 + (int)rank) * 128 + quarter * 32 + lane;
-            const bool row_ok = m < p.M;
-            const int64_t n0 = (int64_t)ni * BN + col0;
-            const bool col_ok = n0 < p.N; // a slice past N (N % BN != 0) computes nothing it stores
-            const float *sa_ptr = p.sa + (row_ok ? m : 0);
-            const float *sb_ptr = p.sb + (col_ok ? (n0 >> 7) * p.num_kb : 0);
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            const TileInfo ti = get_tile(sc, gt, t);
+            const int64_t m = (int64_t)ti.a_row0 + quarter * 32 + lane;
+            const bool row_ok = m < ti.m_end;
+            const bool load_ok = m < sc.M;
+            const int n0 = ti.n0 + col0;
+            const bool col_ok = n0 < sc.N; // a slice past N (N % BN != 0) computes nothing it stores
+            const float *sa_ptr = p.sa + (load_ok ? m : 0);
+            const float *sb_ptr = p.sb + ti.e * p.sb_e_stride + (col_ok ? (int64_t)(n0 >> 7) * p.kb_total : 0);
             float2 acc[C::kCols / 2];
 #pragma unroll
             for (int j = 0; j < C::kCols / 2; ++j)
                 acc[j] = make_float2(0.0f, 0.0f);
 
-            for (int kb = 0; kb < p.num_kb; ++kb, ++tb) {
+            for (int kb = 0; kb < ti.num_kb; ++kb, ++tb) {
                 const float sa = sa_n;
                 const float s = PER_ROW_B ? 0.0f : __fmul_rn(sa, sb_n);
-                if (kb + 1 < p.num_kb) {
-                    sa_n = row_ok ? __ldg(sa_ptr + (int64_t)(kb + 1) * p.M) : 0.0f;
+                if (kb + 1 < ti.num_kb) {
+                    const int kn = ti.kb0 + kb + 1;
+                    sa_n = load_ok ? __ldg(sa_ptr + (int64_t)kn * p.sa_ld) : 0.0f;
                     if (!PER_ROW_B)
-                        sb_n = col_ok ? __ldg(sb_ptr + kb + 1) : 0.0f;
-                } else if (u + unit_step < num_units) {
-                    load_first(u + unit_step);
+                        sb_n = col_ok ? __ldg(sb_ptr + kn) : 0.0f;
+                } else if (t + (int)gridDim.x < num_tiles) {
+                    load_first(get_tile(sc, gt, t + gridDim.x));
                 }
                 const int b = (int)(tb % TMEM_BUFS);
                 const uint32_t tph = (tb / TMEM_BUFS) & 1u;
@@ -382,7 +349,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                         *reinterpret_cast<uint4 *>(o + 8 * j8) = v;
                     }
                 } else {
-                    float *o = reinterpret_cast<float *>(p.out) + m * p.ldo + n0;
+                    float *o = reinterpret_cast<float *>(p.out) + ti.e * p.out_e_stride + m * p.ldo + n0;
 #pragma unroll
                     for (int j4 = 0; j4 < C::kCols / 4; ++j4) {
                         float4 v = make_float4(acc[2 * j4].x, acc[2 * j4].y, acc[2 * j4 + 1].x, acc[2 * j4 + 1].y);
@@ -406,15 +373,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem_base, C::kTmemCols);
     }
-    if (CLUSTER > 1 && threadIdx.x == 0) {
-        // Both CTAs' MMA commits (which arrive on the other CTA's barriers) have
-        // completed; tell the peer, and stay resident until it says the same.
-        ptx::mbar_arrive_remote(ptx::map_to_cta(bye, rank ^ 1u));
-        ptx::mbar_wait(bye, 0u, abort_flag, err, kErrTimeout, p.limit_ns, false);
-    }
 }
-
-// ---------------------------------------------------------------- host side
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
@@ -437,8 +396,6 @@ EncodeTiledFn encode_fn()
 
 } // namespace
 
-// 2-D map over a K-major byte matrix [rows x k_extent] with row stride ld:
-// boxes of 128 bytes (one K-block) x box_rows rows, 128-byte swizzle.
 cudaError_t make_kmajor_map(CUtensorMap *map, const void *base, int64_t k_extent, int64_t rows, int64_t ld,
                             int box_rows)
 {
@@ -457,83 +414,69 @@ cudaError_t make_kmajor_map(CUtensorMap *map, const void *base, int64_t k_extent
 
 namespace {
 
-template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B, int CLUSTER>
+template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B>
 cudaError_t run(const GemmProblem &g, cudaStream_t st)
 {
-    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS, CLUSTER>;
-    auto kern = k_gemm_b128<BN, EPI_WARPS, STAGES, TMEM_BUFS, PER_ROW_B, CLUSTER>;
+    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS>;
+    auto kern = k_gemm_b128<BN, EPI_WARPS, STAGES, TMEM_BUFS, PER_ROW_B>;
     static int configured_device = -1;
-    static int max_clusters = 0;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess)
         return e;
     if (configured_device != dev) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem);
-        if (e != cudaSuccess)
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem)) !=
+            cudaSuccess)
             return e;
-        if (CLUSTER > 1) {
-            cudaLaunchConfig_t cfg = {};
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeClusterDimension;
-            attr[0].val.clusterDim.x = CLUSTER;
-            attr[0].val.clusterDim.y = 1;
-            attr[0].val.clusterDim.z = 1;
-            cfg.gridDim = dim3(CLUSTER * sm_count(), 1, 1);
-            cfg.blockDim = dim3(C::kThreads, 1, 1);
-            cfg.dynamicSmemBytes = C::kSmem;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            if ((e = cudaOccupancyMaxActiveClusters(&max_clusters, kern, &cfg)) != cudaSuccess)
-                return e;
-            if (max_clusters <= 0)
-                return cudaErrorInvalidConfiguration;
-        }
         configured_device = dev;
     }
+    // B rows the map covers: one weight, or every expert's stacked
+    const int64_t b_rows = g.group == GroupKind::Rows ? g.N * g.num_experts : g.N;
     // boxes never taller than the tensor; rows of a stage past the box keep
     // stale bytes, which only reach accumulator rows/columns that are not stored
     const int box_a = g.M >= 128 ? 128 : (int)((g.M + 7) / 8 * 8);
-    const int box_b = CLUSTER > 1 ? BN / 2 : (g.N >= BN ? BN : (int)((g.N + 7) / 8 * 8));
+    const int box_b = b_rows >= BN ? BN : (int)((b_rows + 7) / 8 * 8);
     CUtensorMap ta, tbm;
     if ((e = make_kmajor_map(&ta, g.a, g.K, g.M, g.lda, box_a)) != cudaSuccess)
         return e;
-    if ((e = make_kmajor_map(&tbm, g.b, g.K, g.N, g.ldb, box_b)) != cudaSuccess)
+    if ((e = make_kmajor_map(&tbm, g.b, g.K, b_rows, g.ldb, box_b)) != cudaSuccess)
         return e;
     KParams kp;
+    Sched &s = kp.sched;
+    s.mode = g.group == GroupKind::None ? kDense : (g.group == GroupKind::Rows ? kGroupedRows : kGroupedK);
+    s.mt = (int)((g.M + 127) / 128);
+    s.nt = (int)((g.N + BN - 1) / BN);
+    s.num_kb = (int)(g.K / 128);
+    s.M = g.M;
+    s.N = (int)g.N;
+    s.bn = BN;
+    s.seg = g.seg;
+    // routed rows for FProp/DGrad; column-copy positions (>= routed rows) for WGrad
+    s.seg_max = g.group == GroupKind::K ? g.K : g.M;
+    s.E = g.num_experts;
     kp.sa = g.sa;
     kp.sb = g.sb;
-    kp.M = g.M;
-    kp.N = g.N;
-    kp.num_kb = (int)(g.K / 128);
-    kp.mt = (int)((g.M + 127) / 128);
-    kp.nt = (int)((g.N + BN - 1) / BN);
+    kp.sa_ld = g.M;
+    kp.kb_total = (int)(g.K / 128);
+    kp.sb_e_stride = g.group == GroupKind::Rows ? (g.N / 128) * (g.K / 128) : 0;
     kp.box_a_rows = box_a;
     kp.box_b_rows = box_b;
     kp.out = g.out;
     kp.ldo = g.ldo;
+    kp.out_e_stride = g.group == GroupKind::K ? g.M * g.ldo : 0;
     kp.out_bf16 = g.out_dtype == JETQ_OUT_BF16;
     kp.accumulate = g.accumulate;
     kp.limit_ns = kWaitLimitNs;
-    const int units = ((kp.mt + CLUSTER - 1) / CLUSTER) * kp.nt;
-    if (CLUSTER == 1) {
-        const int grid = units < sm_count() ? units : sm_count();
-        kern<<<grid, C::kThreads, C::kSmem, st>>>(ta, tbm, kp);
-        return cudaGetLastError();
+    int grid = sm_count();
+    if (g.group == GroupKind::None) {
+        const int tiles = s.mt * s.nt;
+        grid = tiles < grid ? tiles : grid;
+    } else if (g.group == GroupKind::K) {
+        const int tiles = s.mt * s.nt * g.num_experts;
+        grid = tiles < grid ? tiles : grid;
     }
-    cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CLUSTER;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.gridDim = dim3(CLUSTER * (units < max_clusters ? units : max_clusters), 1, 1);
-    cfg.blockDim = dim3(C::kThreads, 1, 1);
-    cfg.dynamicSmemBytes = C::kSmem;
-    cfg.stream = st;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, ta, tbm, kp);
+    kern<<<grid, C::kThreads, C::kSmem, st>>>(ta, tbm, kp);
+    return cudaGetLastError();
 }
 
 } // namespace
@@ -544,8 +487,8 @@ cudaError_t launch_gemm_block128(const GemmProblem &g, GemmShape shape, cudaStre
         return cudaSuccess;
     const bool per_row = g.bscale == BScale::PerRow;
     if (shape == GemmShape::Train)
-        return per_row ? run<256, 8, 4, 2, true, 1>(g, st) : run<256, 8, 4, 2, false, 1>(g, st);
-    return per_row ? run<32, 4, 10, 16, true, 1>(g, st) : run<32, 4, 10, 16, false, 1>(g, st);
+        return per_row ? run<256, 8, 4, 2, true>(g, st) : run<256, 8, 4, 2, false>(g, st);
+    return per_row ? run<32, 4, 10, 16, true>(g, st) : run<32, 4, 10, 16, false>(g, st);
 }
 
 cudaError_t gemm_read_and_clear_error(cudaStream_t st, unsigned *out)

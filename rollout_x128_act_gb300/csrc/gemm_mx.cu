@@ -14,6 +14,10 @@
 //             4 x tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32, scale byte =
 //             sub-block) into the tile accumulator; tcgen05.commit releases the
 //             stage, and after the last K-block signals the epilogue
+//   warp 2    grouped FProp/DGrad only: an expert's rows need not start on a
+//             128-row scale band, so the A scale words of the tile's 128 rows
+//             are gathered into an atom in shared memory
+//   warp 3    builds the per-expert tile tables of a grouped launch
 //   warps 4.. epilogue: TMEM -> registers, release the accumulator (the next
 //             tile's MMAs start), convert and store
 //
@@ -26,6 +30,7 @@
 
 #include "jetq_internal.h"
 #include "ptx.cuh"
+#include "sched.cuh"
 
 namespace jetq {
 
@@ -33,34 +38,23 @@ __device__ unsigned g_gemm_mx_error;
 
 namespace {
 
-constexpr int kGroupM = 8;
 constexpr unsigned kErrTimeout = 1u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 struct MxParams {
+    Sched sched;
     const uint8_t *sfa;
     const uint8_t *sfb;
-    int64_t M, N;
-    int num_kb;
-    int mt, nt;
-    int rba, rbb; // row bands of A and B (atoms per K-block)
+    int rba, rbb;          // row bands of A and B (atoms per K-block)
+    int64_t sfb_e_stride;  // bytes between experts' B scale atoms (grouped rows)
     int box_a_rows, box_b_rows;
     void *out;
     int64_t ldo;
+    int64_t out_e_stride;  // elements between experts' outputs (grouped K)
     int out_bf16;
     int accumulate;
     unsigned long long limit_ns;
 };
-
-__device__ __forceinline__ void tile_coords(int t, int mt, int nt, int &mi, int &ni)
-{
-    const int group = kGroupM * nt;
-    const int first_m = (t / group) * kGroupM;
-    const int gm = min(mt - first_m, kGroupM);
-    const int r = t % group;
-    mi = first_m + r % gm;
-    ni = r / gm;
-}
 
 template <int BN, int EPI_WARPS, int STAGES>
 struct MxCfg {
@@ -75,7 +69,8 @@ struct MxCfg {
     static constexpr int kSfCols = 4 + 4 * (BN / 128); // TMEM columns per stage
     static constexpr int kTmemCols = 512;
     static constexpr int kBars = 2 * STAGES + 3;
-    static constexpr size_t kSmem = 1024 + (size_t)STAGES * kStage + (size_t)STAGES * kSfStage + 1024;
+    static constexpr size_t kSmem =
+        1024 + (size_t)STAGES * kStage + (size_t)STAGES * kSfStage + 1024 + sizeof(GroupTables);
     static_assert(BN % 128 == 0 && BN <= 256, "B tile is whole 128-row scale bands");
     static_assert(BN + STAGES * kSfCols <= kTmemCols, "TMEM budget");
     static_assert(kCols % 32 == 0, "epilogue split");
@@ -92,6 +87,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sf + (size_t)STAGES * C::kSfStage);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+    GroupTables *gt = reinterpret_cast<GroupTables *>(reinterpret_cast<uint8_t *>(bars) + 1024);
 
     const uint32_t bar0 = ptx::smem_addr(bars);
     auto full = [&](int s) { return bar0 + 8u * s; };
@@ -101,12 +97,13 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     const uint32_t done = acc_full + 16u;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int num_tiles = p.mt * p.nt;
+    const Sched &sc = p.sched;
+    const bool gather_a = sc.mode == kGroupedRows; // A scale atoms are assembled by warp 2
     unsigned *err = &g_gemm_mx_error;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
-            ptx::mbar_init(full(s), 1);
+            ptx::mbar_init(full(s), gather_a ? 2 : 1);
             ptx::mbar_init(empty(s), 1);
         }
         ptx::mbar_init(acc_full, 1);
@@ -123,35 +120,42 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::kTmemCols);
         ptx::tmem_relinquish();
     }
+    if (warp == 3 && sc.mode != kDense)
+        build_group_tables(sc, gt);
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    const int num_tiles = total_tiles(sc, gt);
 
     if (warp < 4) {
         if (warp == 0 && lane == 0) {
             // -------------------------------------------------- TMA producer
             uint32_t it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-                int mi, ni;
-                tile_coords(tile, p.mt, p.nt, mi, ni);
-                const int b_bands = min(BN / 128, p.rbb - ni * (BN / 128)); // scale atoms that exist
-                const uint32_t tx = (uint32_t)((p.box_a_rows + p.box_b_rows) * 128 + 512 + b_bands * 512);
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const TileInfo ti = get_tile(sc, gt, t);
+                const int brb0 = ti.n0 / 128; // first B scale band inside the (expert's) B operand
+                const int b_bands = min(BN / 128, p.rbb - brb0);
+                const uint8_t *sfb_e = p.sfb + (int64_t)ti.e * p.sfb_e_stride;
+                const uint32_t tx = (uint32_t)((p.box_a_rows + p.box_b_rows) * 128 + (gather_a ? 0 : 512) +
+                                               b_bands * 512);
+                for (int kb = 0; kb < ti.num_kb; ++kb, ++it) {
                     const int s = (int)(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;
                     if (!ptx::mbar_wait(empty(s), ph ^ 1u, abort_flag, err, kErrTimeout, p.limit_ns)) {
                         ok = false;
                         break;
                     }
+                    const int kg = ti.kb0 + kb;
                     ptx::mbar_arrive_expect_tx(full(s), tx);
                     const uint32_t dst = ptx::smem_addr(tiles + (size_t)s * C::kStage);
-                    ptx::tma_load_2d(dst, &tmA, full(s), kb * 128, mi * 128);
-                    ptx::tma_load_2d(dst + C::kABytes, &tmB, full(s), kb * 128, ni * BN);
+                    ptx::tma_load_2d(dst, &tmA, full(s), kg * 128, ti.a_row0);
+                    ptx::tma_load_2d(dst + C::kABytes, &tmB, full(s), kg * 128, ti.b_row0);
                     const uint32_t sdst = ptx::smem_addr(sf + (size_t)s * C::kSfStage);
-                    ptx::bulk_load(sdst, p.sfa + ((int64_t)kb * p.rba + mi) * 512, 512u, full(s));
-                    ptx::bulk_load(sdst + C::kSfaBytes, p.sfb + ((int64_t)kb * p.rbb + ni * (BN / 128)) * 512,
+                    if (!gather_a)
+                        ptx::bulk_load(sdst, p.sfa + ((int64_t)kg * p.rba + ti.a_row0 / 128) * 512, 512u, full(s));
+                    ptx::bulk_load(sdst + C::kSfaBytes, sfb_e + ((int64_t)kg * p.rbb + brb0) * 512,
                                    (uint32_t)b_bands * 512u, full(s));
                 }
             }
@@ -165,11 +169,12 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             // -------------------------------------------------- MMA issuer
             uint32_t it = 0, tc = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++tc) {
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x, ++tc) {
+                const TileInfo ti = get_tile(sc, gt, t);
                 if (!ptx::mbar_wait(acc_empty, (tc & 1u) ^ 1u, abort_flag, err, kErrTimeout, p.limit_ns))
                     break;
                 ptx::tc_fence_after();
-                for (int kb = 0; kb < p.num_kb; ++kb, ++it) {
+                for (int kb = 0; kb < ti.num_kb; ++kb, ++it) {
                     const int s = (int)(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;
                     if (!ptx::mbar_wait(full(s), ph, abort_flag, err, kErrTimeout, p.limit_ns)) {
@@ -196,10 +201,41 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                 }
                 if (!ok)
                     break;
-                ptx::mma_commit(acc_full);
+                ptx::mma_commit(acc_full); // also for an empty expert: the epilogue writes zeros
             }
             ptx::mma_commit(done);
             ptx::mbar_wait(done, 0u, abort_flag, err, kErrTimeout, p.limit_ns, false);
+        } else if (warp == 2 && gather_a) {
+            // -------------------------------------------------- A scale gather (grouped rows)
+            // row a_row0 + i (i = lane + 32 j) of the tile -> byte lane * 16 + j * 4 of the atom
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+                const TileInfo ti = get_tile(sc, gt, t);
+                for (int kb = 0; kb < ti.num_kb; ++kb, ++it) {
+                    const int s = (int)(it % STAGES);
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    const bool got = ptx::mbar_wait(empty(s), ph ^ 1u, abort_flag, err, kErrTimeout, p.limit_ns);
+                    if (!__all_sync(0xFFFFFFFFu, got)) {
+                        ok = false;
+                        break;
+                    }
+                    const int64_t kg = ti.kb0 + kb;
+                    uint32_t w[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int64_t r = (int64_t)ti.a_row0 + lane + 32 * j;
+                        w[j] = r < sc.M ? __ldg(reinterpret_cast<const uint32_t *>(
+                                              p.sfa + (kg * p.rba + (r >> 7)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4))
+                                        : 0u;
+                    }
+                    *reinterpret_cast<uint4 *>(sf + (size_t)s * C::kSfStage + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); // visible to tcgen05.cp
+                    __syncwarp();
+                    if (lane == 0)
+                        ptx::mbar_arrive(full(s));
+                }
+            }
         }
         __syncwarp();
     } else {
@@ -209,11 +245,10 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
         const int col0 = (ew >> 2) * C::kCols;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
         uint32_t tc = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tc) {
-            int mi, ni;
-            tile_coords(tile, p.mt, p.nt, mi, ni);
-            const int64_t m = (int64_t)mi * 128 + quarter * 32 + lane;
-            const int64_t n0 = (int64_t)ni * BN + col0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++tc) {
+            const TileInfo ti = get_tile(sc, gt, t);
+            const int64_t m = (int64_t)ti.a_row0 + quarter * 32 + lane;
+            const int n0 = ti.n0 + col0;
             const bool got = ptx::mbar_wait(acc_full, tc & 1u, abort_flag, err, kErrTimeout, p.limit_ns);
             if (!__all_sync(0xFFFFFFFFu, got))
                 break;
@@ -228,7 +263,12 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             __syncwarp();
             if (lane == 0)
                 ptx::mbar_arrive(acc_empty); // the MMA may start the next tile
-            if (m < p.M && n0 < p.N) {
+            if (ti.num_kb == 0) {            // an expert without rows: its gradient is zero
+#pragma unroll
+                for (int j = 0; j < C::kCols; ++j)
+                    v[j] = 0u;
+            }
+            if (m < ti.m_end && n0 < sc.N) {
                 if (p.out_bf16) {
                     __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.out) + m * p.ldo + n0;
 #pragma unroll
@@ -244,7 +284,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                         *reinterpret_cast<uint4 *>(o + 8 * j8) = w;
                     }
                 } else {
-                    float *o = reinterpret_cast<float *>(p.out) + m * p.ldo + n0;
+                    float *o = reinterpret_cast<float *>(p.out) + ti.e * p.out_e_stride + m * p.ldo + n0;
 #pragma unroll
                     for (int j4 = 0; j4 < C::kCols / 4; ++j4) {
                         float4 w = make_float4(__uint_as_float(v[4 * j4]), __uint_as_float(v[4 * j4 + 1]),
@@ -287,32 +327,48 @@ cudaError_t run_mx(const MxGemmProblem &g, cudaStream_t st)
             return e;
         configured_device = dev;
     }
+    const int64_t b_rows = g.group == GroupKind::Rows ? g.N * g.num_experts : g.N;
     const int box_a = g.M >= 128 ? 128 : (int)((g.M + 7) / 8 * 8);
-    const int box_b = g.N >= BN ? BN : (int)((g.N + 7) / 8 * 8);
+    const int box_b = b_rows >= BN ? BN : (int)((b_rows + 7) / 8 * 8);
     CUtensorMap ta, tbm;
     if ((e = make_kmajor_map(&ta, g.a, g.K, g.M, g.lda, box_a)) != cudaSuccess)
         return e;
-    if ((e = make_kmajor_map(&tbm, g.b, g.K, g.N, g.ldb, box_b)) != cudaSuccess)
+    if ((e = make_kmajor_map(&tbm, g.b, g.K, b_rows, g.ldb, box_b)) != cudaSuccess)
         return e;
     MxParams kp;
+    Sched &s = kp.sched;
+    s.mode = g.group == GroupKind::None ? kDense : (g.group == GroupKind::Rows ? kGroupedRows : kGroupedK);
+    s.mt = (int)((g.M + 127) / 128);
+    s.nt = (int)((g.N + BN - 1) / BN);
+    s.num_kb = (int)(g.K / 128);
+    s.M = g.M;
+    s.N = (int)g.N;
+    s.bn = BN;
+    s.seg = g.seg;
+    // routed rows for FProp/DGrad; column-copy positions (>= routed rows) for WGrad
+    s.seg_max = g.group == GroupKind::K ? g.K : g.M;
+    s.E = g.num_experts;
     kp.sfa = g.sfa;
     kp.sfb = g.sfb;
-    kp.M = g.M;
-    kp.N = g.N;
-    kp.num_kb = (int)(g.K / 128);
-    kp.mt = (int)((g.M + 127) / 128);
-    kp.nt = (int)((g.N + BN - 1) / BN);
     kp.rba = (int)((g.M + 127) / 128);
     kp.rbb = (int)((g.N + 127) / 128);
+    kp.sfb_e_stride = g.group == GroupKind::Rows ? (int64_t)kp.rbb * (g.K / 128) * 512 : 0;
     kp.box_a_rows = box_a;
     kp.box_b_rows = box_b;
     kp.out = g.out;
     kp.ldo = g.ldo;
+    kp.out_e_stride = g.group == GroupKind::K ? g.M * g.ldo : 0;
     kp.out_bf16 = g.out_dtype == JETQ_OUT_BF16;
     kp.accumulate = g.accumulate;
     kp.limit_ns = kWaitLimitNs;
-    const int tiles = kp.mt * kp.nt;
-    const int grid = tiles < sm_count() ? tiles : sm_count();
+    int grid = sm_count();
+    if (g.group == GroupKind::None) {
+        const int tiles = s.mt * s.nt;
+        grid = tiles < grid ? tiles : grid;
+    } else if (g.group == GroupKind::K) {
+        const int tiles = s.mt * s.nt * g.num_experts;
+        grid = tiles < grid ? tiles : grid;
+    }
     kern<<<grid, C::kThreads, C::kSmem, st>>>(ta, tbm, kp);
     return cudaGetLastError();
 }

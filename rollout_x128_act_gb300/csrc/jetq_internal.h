@@ -55,6 +55,12 @@ enum class BScale : int {
     PerRow = 1    // sb[kb * N + n]                           (column copy along K)
 };
 
+enum class GroupKind : int {
+    None = 0, // one problem
+    Rows = 1, // per-expert FProp/DGrad: A rows split by segments, B = experts' weights stacked [E*N x K]
+    K = 2     // per-expert WGrad: K-blocks split by segments (column copies), out = experts stacked [E x M x N]
+};
+
 struct GemmProblem {
     const uint8_t *a;  // [M x lda] codes
     const float *sa;   // [K/128 x M]
@@ -67,6 +73,9 @@ struct GemmProblem {
     int64_t ldo;       // elements
     jetq_out_dtype out_dtype;
     int accumulate;    // F32 only: out = out + acc
+    GroupKind group = GroupKind::None;
+    const int64_t *seg = nullptr; // device [num_experts + 1]
+    int num_experts = 1;
 };
 
 enum class GemmShape : int { Train = 0, Decode = 1 };
@@ -86,6 +95,9 @@ struct MxGemmProblem {
     int64_t ldo;
     jetq_out_dtype out_dtype;
     int accumulate;
+    GroupKind group = GroupKind::None;
+    const int64_t *seg = nullptr;
+    int num_experts = 1;
 };
 
 cudaError_t launch_gemm_mx(const MxGemmProblem &p, cudaStream_t st);
