@@ -245,10 +245,194 @@ class Step:
         return launches
 
 
+# --------------------------------------------------------------------------- other configurations
+
+def _dev_inputs(dev, seed):
+    """Seeded device-side generator for the secondary measurements (speed only;
+    same distributions as synth/: N(0,1) + 0.1% x50 activations, N(0,0.02)
+    weights, N(0,1e-3) gradients, BF16 by round-to-nearest)."""
+    import torch
+
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+
+    def act(r, c):
+        x = torch.randn(r, c, generator=g, device=dev)
+        k = int(round(0.001 * r * c))
+        idx = torch.randint(0, r * c, (k,), generator=g, device=dev)
+        x.view(-1)[idx] *= 50.0
+        return x.to(torch.bfloat16)
+
+    def weight(r, c):
+        return (torch.randn(r, c, generator=g, device=dev) * 0.02).to(torch.bfloat16)
+
+    def grad(r, c):
+        return (torch.randn(r, c, generator=g, device=dev) * 1e-3).to(torch.bfloat16)
+
+    return act, weight, grad
+
+
+def _time(fn, iters, warm=3):
+    import torch
+
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(iters):
+        fn()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / iters  # ms
+
+
+def measure_decode(dev, peaks):
+    """Rollout decode FProp (DECODE path) against the dense-8B weights: N tokens
+    x 4096 vs W_up 12288x4096 and N x 12288 vs W_down 4096x12288.  Eight weight
+    copies (402 MB) rotate so each call streams its weight from HBM."""
+    import torch
+
+    import rollout_x128_act_gb300 as jq
+
+    act, weight, _ = _dev_inputs(dev, 7)
+    out = {}
+    for name, (d, c) in (("up", (D, C)), ("down", (C, D))):
+        ws = [jq.quant_weight(weight(d, c), transposed=False) for _ in range(8)]
+        x = act(256, c)
+        for n in (1, 8, 64, 256):
+            a = jq.quant_act(x[:n], col=False)
+            y = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
+            i = [0]
+
+            def call():
+                q, s, _, _ = ws[i[0] % 8]
+                i[0] += 1
+                jq.jetq_gemm_fprop(jq.RECIPE_BLOCK128, a["q_row"], a["s_row"], q, s, n, d, c, y, jq.PATH_DECODE)
+
+            ms = _time(call, 40)
+            # CUDA-graph replay of 8 calls (one per weight copy), as a decode step replays
+            st = torch.cuda.Stream()
+            st.wait_stream(torch.cuda.current_stream())
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(st):
+                for _ in range(2):
+                    call()
+                torch.cuda.synchronize()
+                with torch.cuda.graph(graph, stream=st):
+                    for _ in range(8):
+                        call()
+            ms_graph = _time(graph.replay, 10) / 8
+            byts = d * c + (d // 128) * (c // 128) * 4 + n * c * (1 + 4 / 128) + n * d * 2
+            flops = 2.0 * n * d * c
+            t_roof = max(byts / (peaks["hbm"] * 1e9), flops / (2.0 * peaks["bf16"] * 1e12))
+            out[f"{name}_n{n}"] = {
+                "us": round(ms * 1e3, 2), "us_graph": round(ms_graph * 1e3, 2),
+                "gbs": round(byts / (ms * 1e-3) / 1e9, 1),
+                "frac_of_roofline": round(t_roof / (ms * 1e-3), 3),
+                "frac_of_roofline_graph": round(t_roof / (ms_graph * 1e-3), 3),
+            }
+        del ws
+    return out
+
+
+def measure_mxfp8(dev):
+    """MXFP8 recipe on the dense-8B gate shapes: quantizer GB/s and the three GEMMs."""
+    import torch
+
+    import rollout_x128_act_gb300 as jq
+
+    act, weight, grad = _dev_inputs(dev, 8)
+    x, w, dy = act(N_TOK, C), weight(D, C), grad(N_TOK, D)
+    ms_q = _time(lambda: jq.quant_mx(dy), 10)
+    gx, gw, gdy = jq.quant_mx(x), jq.quant_mx(w), jq.quant_mx(dy)
+    y = torch.empty((N_TOK, D), dtype=torch.bfloat16, device=dev)
+    dx = torch.empty((N_TOK, C), dtype=torch.bfloat16, device=dev)
+    dw = torch.empty((D, C), dtype=torch.float32, device=dev)
+    R = jq.RECIPE_MXFP8
+    t = {
+        "fprop": _time(lambda: jq.jetq_gemm_fprop(R, gx["q_row"], gx["e8_row"], gw["q_row"], gw["e8_row"], N_TOK, D,
+                                                  C, y, jq.PATH_TRAIN), 10),
+        "dgrad": _time(lambda: jq.jetq_gemm_dgrad(R, gdy["q_row"], gdy["e8_row"], gw["q_col"], gw["e8_col"], N_TOK, D,
+                                                  C, dx), 10),
+        "wgrad": _time(lambda: jq.jetq_gemm_wgrad(R, gdy["q_col"], gdy["e8_col"], gx["q_col"], gx["e8_col"], N_TOK,
+                                                  gx["ldq_col"], D, C, dw), 10),
+    }
+    res = {k: {"ms": round(v, 4), "tflops": round(GEMM_FLOP / (v * 1e-3) / 1e12, 1)} for k, v in t.items()}
+    res["quant_mx_dy_gbs"] = round(N_TOK * D * ACT_BYTES_PER_ELT / (ms_q * 1e-3) / 1e9, 1)
+    return res
+
+
+def measure_moe(dev):
+    """MoE grouped GEMMs, 30B-A3B shapes: 128 experts, 16384 tokens top-8 with
+    Zipf(1.2) load (131072 routed rows), hidden 2048, expert intermediate 768
+    (gate/up fused 1536); FProp/DGrad/WGrad of the gate/up projection, both recipes."""
+    import torch
+
+    import rollout_x128_act_gb300 as jq
+    import synth
+
+    E, Cm, Dm = 128, 2048, 1536
+    off, _ = synth.zipf_topk_routing(16384, E, 8, 1.2, seed=0)
+    R = int(off[-1])
+    seg = torch.tensor(off, dtype=torch.int64, device=dev)
+    act, weight, grad = _dev_inputs(dev, 9)
+    x, dy = act(R, Cm), grad(R, Dm)
+    wst = weight(E * Dm, Cm)
+    flops = 2.0 * R * Dm * Cm
+    res = {"routed_rows": R, "expert_rows_min": int((off[1:] - off[:-1]).min()),
+           "expert_rows_max": int((off[1:] - off[:-1]).max())}
+    # 128-block recipe
+    ax, ady = jq.quant_act(x, seg_offsets=seg), jq.quant_act(dy, seg_offsets=seg)
+    qs = [jq.quant_weight(wst[e * Dm:(e + 1) * Dm]) for e in range(E)]
+    qw, sw = torch.stack([q[0] for q in qs]), torch.stack([q[1] for q in qs])
+    qwt, swt = torch.stack([q[2] for q in qs]), torch.stack([q[3] for q in qs])
+    del qs
+    P = ax["ldq_col"]
+    y = torch.empty((R, Dm), dtype=torch.bfloat16, device=dev)
+    dx = torch.empty((R, Cm), dtype=torch.bfloat16, device=dev)
+    dw = torch.empty((E, Dm, Cm), dtype=torch.float32, device=dev)
+    B = jq.RECIPE_BLOCK128
+    t = {
+        "b128_fprop": _time(lambda: jq.grouped(jq.GEMM_FPROP, ax["q_row"], ax["s_row"], qw, sw, seg, n=Dm, k=Cm,
+                                               out=y), 10),
+        "b128_dgrad": _time(lambda: jq.grouped(jq.GEMM_DGRAD, ady["q_row"], ady["s_row"], qwt, swt, seg, n=Cm, k=Dm,
+                                               out=dx), 10),
+        "b128_wgrad": _time(lambda: jq.grouped(jq.GEMM_WGRAD, ady["q_col"], ady["s_col"], ax["q_col"], ax["s_col"],
+                                               seg, n=Cm, k=P, out=dw), 5),
+    }
+    del ax, ady, qw, sw, qwt, swt
+    # MXFP8 recipe
+    gx, gdy = jq.quant_mx(x, seg_offsets=seg), jq.quant_mx(dy, seg_offsets=seg)
+    gws = [jq.quant_mx(wst[e * Dm:(e + 1) * Dm]) for e in range(E)]
+    qw, ew = torch.stack([g["q_row"] for g in gws]), torch.cat([g["e8_row"] for g in gws])
+    qwc, ewc = torch.stack([g["q_col"] for g in gws]), torch.cat([g["e8_col"] for g in gws])
+    del gws
+    M = jq.RECIPE_MXFP8
+    t.update({
+        "mx_fprop": _time(lambda: jq.grouped(jq.GEMM_FPROP, gx["q_row"], gx["e8_row"], qw, ew, seg, n=Dm, k=Cm,
+                                             out=y, recipe=M), 10),
+        "mx_dgrad": _time(lambda: jq.grouped(jq.GEMM_DGRAD, gdy["q_row"], gdy["e8_row"], qwc, ewc, seg, n=Cm, k=Dm,
+                                             out=dx, recipe=M), 10),
+        "mx_wgrad": _time(lambda: jq.grouped(jq.GEMM_WGRAD, gdy["q_col"], gdy["e8_col"], gx["q_col"], gx["e8_col"],
+                                             seg, n=Cm, k=P, out=dw, recipe=M), 5),
+    })
+    for k, v in t.items():
+        res[k] = {"ms": round(v, 4), "tflops": round(flops / (v * 1e-3) / 1e12, 1)}
+    del B
+    return res
+
+
 def quant_bytes_per_step():
     act_elts = N_TOK * C * 2 + N_TOK * D * 3  # X, dY_down ; H, dY_gate, dY_up
     w_elts = 3 * D * C
     return act_elts * ACT_BYTES_PER_ELT + w_elts * W_BYTES_PER_ELT
+
+
+def step_error() -> bool:
+    import rollout_x128_act_gb300 as jq
+
+    return jq.jetq_check_device_error() != 0
 
 
 def run_ours(args):
@@ -395,6 +579,15 @@ def run_ours(args):
         "clocks": clocks,
     }
     if rank == 0:
+        if not args.no_extras:
+            del step, pinned, dw_host
+            torch.cuda.empty_cache()
+            peaks_now = _peaks()
+            line["decode"] = measure_decode(dev, peaks_now)
+            line["mxfp8"] = measure_mxfp8(dev)
+            line["moe"] = measure_moe(dev)
+            if step_error():
+                raise RuntimeError("device error word set during the secondary measurements")
         if not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(args.cpu_sample_rows)
         print(json.dumps(line), flush=True)
@@ -470,6 +663,9 @@ PROFILE_CASES = {
     "decode": "FProp 8 tokens x 12288 x 12288 (decode shape, 151 MB of FP8 weight)",
     "quant_act": "activation quantizer, X 8192 x 12288 BF16 (row + column copies)",
     "quant_w": "weight quantizer, W 12288 x 12288 BF16 (+ transposed copy)",
+    "quant_mx": "MXFP8 quantizer, X 8192 x 12288 BF16 (row + column copies)",
+    "gemm_mx_fprop": "MXFP8 FProp 4096 x 12288 x 4096 (BF16 out)",
+    "grouped_fprop": "grouped FProp, 32 experts x 1536 x 2048, 16384 routed rows (Zipf 1.2), BF16 out",
 }
 
 
@@ -507,6 +703,27 @@ def run_case(name: str, launches: int = 5):
             out = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
             fn = lambda: jq.jetq_gemm_fprop(jq.RECIPE_BLOCK128, ax["q_row"], ax["s_row"], qw, sw, n, d, c,  # noqa
                                             out, path)
+    elif name == "gemm_mx_fprop":
+        n, c, d = 4096, 4096, 12288
+        gx = jq.quant_mx(bf16(synth.activation(n, c, seed=0, stream="x")), col=False)
+        gw = jq.quant_mx(bf16(synth.weight(d, c, seed=0, stream="w_up")), col=False)
+        out = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
+        fn = lambda: jq.jetq_gemm_fprop(jq.RECIPE_MXFP8, gx["q_row"], gx["e8_row"], gw["q_row"], gw["e8_row"],  # noqa
+                                        n, d, c, out, jq.PATH_TRAIN)
+    elif name == "grouped_fprop":
+        E, c, d = 32, 2048, 1536
+        off, _ = synth.zipf_topk_routing(2048, E, 8, 1.2, seed=0)
+        R = int(off[-1])
+        seg = torch.tensor(off, dtype=torch.int64, device=dev)
+        ax = jq.quant_act(bf16(synth.activation(R, c, seed=0, stream="x")), col=False)
+        ws = bf16(synth.weight(E * d, c, seed=0, stream="w_gate"))
+        qs = [jq.quant_weight(ws[e * d:(e + 1) * d], transposed=False) for e in range(E)]
+        qw, sw = torch.stack([q[0] for q in qs]), torch.stack([q[1] for q in qs])
+        out = torch.empty((R, d), dtype=torch.bfloat16, device=dev)
+        fn = lambda: jq.grouped(jq.GEMM_FPROP, ax["q_row"], ax["s_row"], qw, sw, seg, n=d, k=c, out=out)  # noqa
+    elif name == "quant_mx":
+        x = bf16(synth.activation(8192, 12288, seed=0, stream="h"))
+        fn = lambda: jq.quant_mx(x)  # noqa: E731
     elif name == "quant_act":
         x = bf16(synth.activation(8192, 12288, seed=0, stream="h"))
         fn = lambda: jq.quant_act(x)  # noqa: E731
@@ -533,6 +750,7 @@ def main():
     ap.add_argument("--cpu-sample-rows", type=int, default=2048)
     ap.add_argument("--ref-rows", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-extras", action="store_true", help="skip the decode / MXFP8 / MoE measurements")
     ap.add_argument("--case", default=None, help="profiling case: " + ", ".join(sorted(PROFILE_CASES)))
     args = ap.parse_args()
     if args.case:
