@@ -60,6 +60,33 @@ def test_three_gemms_against_oracle(N, D, C):
     assert_gemm_close(dw, *oracle.wgrad(DYc, Xc))
 
 
+@pytest.mark.parametrize("recipe", [jq.RECIPE_BLOCK128, jq.RECIPE_MXFP8])
+def test_repeated_launches_are_bitwise_identical(recipe):
+    """Every GEMM is deterministic: repeated launches on the same operands give the
+    same bits (a pipeline race would show up here as a rare mismatch)."""
+    N, D, C = 2048, 4096, 2048
+    x, w, dy = _layer(N, D, C, seed=11)
+    if recipe == jq.RECIPE_BLOCK128:
+        ax, ady, (qw, sw, qwt, swt) = _gpu_quant(x, w, dy)
+        f = lambda: jq.fprop(ax["q_row"], ax["s_row"], qw, sw, path=jq.PATH_TRAIN)  # noqa: E731
+        g = lambda: jq.dgrad(ady["q_row"], ady["s_row"], qwt, swt)  # noqa: E731
+        h = lambda: jq.wgrad(ady["q_col"], ady["s_col"], ax["q_col"], ax["s_col"], ax["ldq_col"])  # noqa: E731
+    else:
+        gx, gw, gdy = jq.quant_mx(to_dev_bf16(x)), jq.quant_mx(to_dev_bf16(w)), jq.quant_mx(to_dev_bf16(dy))
+        R = jq.RECIPE_MXFP8
+        f = lambda: jq.fprop(gx["q_row"], gx["e8_row"], gw["q_row"], gw["e8_row"], recipe=R)  # noqa: E731
+        g = lambda: jq.dgrad(gdy["q_row"], gdy["e8_row"], gw["q_col"], gw["e8_col"], recipe=R)  # noqa: E731
+        h = lambda: jq.wgrad(gdy["q_col"], gdy["e8_col"], gx["q_col"], gx["e8_col"], gx["ldq_col"],  # noqa: E731
+                             recipe=R)
+    for fn in (f, g, h):
+        first = fn()
+        for _ in range(4):
+            again = fn()
+            torch.cuda.synchronize()
+            assert torch.equal(first.view(torch.int32), again.view(torch.int32))
+    assert jq.jetq_check_device_error() == jq.OK
+
+
 def test_bf16_output_is_rne_of_f32():
     x, w, _ = _layer(300, 512, 256, 3)
     ax = jq.quant_act(to_dev_bf16(x), col=False)
