@@ -59,6 +59,8 @@ struct KParams {
     int64_t sb_e_stride;    // floats between experts' weight scales
     int box_a_rows;
     int box_b_rows;
+    int a_stride;           // bytes between A K-block tiles
+    int b_stride;           // bytes between B K-block tiles
     void *out;
     int64_t ldo;
     int64_t out_e_stride;   // elements between experts' outputs (grouped K)
@@ -67,11 +69,21 @@ struct KParams {
     unsigned long long limit_ns;
 };
 
-template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS>
+__host__ __device__ constexpr int gcd_int(int a, int b) { return b ? gcd_int(b, a % b) : a; }
+__host__ __device__ constexpr int lcm_int(int a, int b) { return a / gcd_int(a, b) * b; }
+
+template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, int A_STRIDE_MAX = 16384, int KBP = 1>
 struct Cfg {
     static constexpr int kABytes = 128 * 128;
     static constexpr int kBBytes = BN * 128;
-    static constexpr int kStage = kABytes + kBBytes;
+    // A stage holds KBP K-blocks and B stage KBP K-blocks (one TMA box each when
+    // KBP > 1: a decode slice of 32 weight rows moves 4 KB per K-block, too little
+    // per copy to keep HBM busy).  A K-blocks sit A_STRIDE_MAX (or less, for a
+    // decode batch of <= A_STRIDE_MAX/128 rows) apart; an M = 128 MMA reads 16 KB
+    // from a K-block's base, so the rows past a short A tile are the next
+    // K-blocks' bytes: don't-care rows whose results are never stored.  The
+    // region keeps every such read inside it.
+    static constexpr int kARegion = (STAGES * KBP - 1) * A_STRIDE_MAX + kABytes;
     // warpgroup 0: TMA producer (warp 0), MMA issuer (warp 1), column-scale
     // producer (warp 2, WGrad), group tables (warp 3); warpgroups 1..: epilogue
     static constexpr int kThreads = 128 + 32 * EPI_WARPS;
@@ -81,22 +93,25 @@ struct Cfg {
     static constexpr int kBars = 2 * STAGES + 2 * TMEM_BUFS + 2 * kSbSlots + 1;
     static constexpr size_t kSbBytes = (size_t)kSbSlots * BN * 4;
     static constexpr size_t kSmem =
-        1024 + (size_t)STAGES * kStage + kSbBytes + 1024 + sizeof(GroupTables);
+        1024 + (size_t)kARegion + (size_t)STAGES * KBP * kBBytes + kSbBytes + 1024 + sizeof(GroupTables);
     static_assert(TMEM_BUFS * BN <= kTmemCols, "TMEM buffers exceed 512 columns");
     static_assert(EPI_WARPS % 4 == 0 && kCols % 32 == 0, "epilogue split");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
     static_assert(kBars * 8 + 16 <= 1024, "barrier area");
+    static_assert(A_STRIDE_MAX % 1024 == 0 && A_STRIDE_MAX <= kABytes, "A stages on 1024-byte swizzle atoms");
+    static_assert(kSmem <= 232448, "shared memory");
 };
 
-template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B>
+template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B, int A_STRIDE_MAX, int KBP, int PF>
 __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     k_gemm_b128(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p)
 {
-    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS>;
+    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS, A_STRIDE_MAX, KBP>;
     constexpr int SB = C::kSbSlots;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-    float *sb_ring = reinterpret_cast<float *>(tiles + (size_t)STAGES * C::kStage);
+    uint8_t *tiles_a = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *tiles_b = tiles_a + C::kARegion;
+    float *sb_ring = reinterpret_cast<float *>(tiles_b + (size_t)STAGES * KBP * C::kBBytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sb_ring) + C::kSbBytes);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -151,12 +166,13 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     if (warp < 4) {
         if (warp == 0 && lane == 0) {
             // -------------------------------------------------- TMA producer
-            const uint32_t tx = (uint32_t)((p.box_a_rows + p.box_b_rows) * 128);
+            // a box past the last K-block is zero-filled and still counts in full
+            const uint32_t tx = (uint32_t)(KBP * (p.box_a_rows + p.box_b_rows) * 128);
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 const TileInfo ti = get_tile(sc, gt, t);
-                for (int kb = 0; kb < ti.num_kb; ++kb, ++it) {
+                for (int kb = 0; kb < ti.num_kb; kb += KBP, ++it) {
                     const int s = (int)(it % STAGES);
                     const uint32_t ph = (it / STAGES) & 1u;
                     if (!ptx::mbar_wait(empty(s), ph ^ 1u, abort_flag, err, kErrTimeout, p.limit_ns)) {
@@ -164,9 +180,15 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                         break;
                     }
                     ptx::mbar_arrive_expect_tx(full(s), tx);
-                    const uint32_t dst = ptx::smem_addr(tiles + (size_t)s * C::kStage);
-                    ptx::tma_load_2d(dst, &tmA, full(s), (ti.kb0 + kb) * 128, ti.a_row0);
-                    ptx::tma_load_2d(dst + C::kABytes, &tmB, full(s), (ti.kb0 + kb) * 128, ti.b_row0);
+                    const uint32_t da = ptx::smem_addr(tiles_a + (size_t)s * KBP * p.a_stride);
+                    const uint32_t db = ptx::smem_addr(tiles_b + (size_t)s * KBP * p.b_stride);
+                    if constexpr (KBP == 1) {
+                        ptx::tma_load_2d(da, &tmA, full(s), (ti.kb0 + kb) * 128, ti.a_row0);
+                        ptx::tma_load_2d(db, &tmB, full(s), (ti.kb0 + kb) * 128, ti.b_row0);
+                    } else {
+                        ptx::tma_load_3d(da, &tmA, full(s), 0, ti.a_row0, ti.kb0 + kb);
+                        ptx::tma_load_3d(db, &tmB, full(s), 0, ti.b_row0, ti.kb0 + kb);
+                    }
                 }
             }
             // drain: every copy this thread started must have landed before exit
@@ -178,31 +200,68 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             }
         } else if (warp == 1 && lane == 0) {
             // -------------------------------------------------- MMA issuer
+            // Every operand an MMA takes (stage descriptors, accumulator
+            // columns) is computed once, here, and the loop below is unrolled
+            // so that each MMA picks its operands by a compile-time index: an
+            // operand computed inside the loop costs the issue a few hundred
+            // cycles, more than a narrow MMA takes to run.
             constexpr uint32_t idesc = ptx::idesc_e4m3_f32(128, BN);
-            uint32_t it = 0, tb = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const TileInfo ti = get_tile(sc, gt, t);
-                for (int kb = 0; kb < ti.num_kb; ++kb, ++it, ++tb) {
-                    const int s = (int)(it % STAGES);
-                    const uint32_t ph = (it / STAGES) & 1u;
-                    const int b = (int)(tb % TMEM_BUFS);
-                    const uint32_t tph = (tb / TMEM_BUFS) & 1u;
-                    if (!ptx::mbar_wait(tempty(b), tph ^ 1u, abort_flag, err, kErrTimeout, p.limit_ns) ||
-                        !ptx::mbar_wait(full(s), ph, abort_flag, err, kErrTimeout, p.limit_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    ptx::tc_fence_after();
-                    const uint32_t a_addr = ptx::smem_addr(tiles + (size_t)s * C::kStage);
-                    const uint64_t adesc = ptx::desc_kmajor_sw128(a_addr);
-                    const uint64_t bdesc = ptx::desc_kmajor_sw128(a_addr + C::kABytes);
-                    const uint32_t d = tmem_base + (uint32_t)(b * BN);
+            constexpr int NG = TMEM_BUFS / KBP; // buffer groups of KBP buffers, one group per stage
+            constexpr int U = lcm_int(STAGES, NG);
+            static_assert(TMEM_BUFS % KBP == 0, "buffer groups");
+            uint64_t adesc[STAGES * KBP], bdesc[STAGES * KBP];
+            uint32_t dcol[TMEM_BUFS];
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) // 4 x K=32 (32 bytes) inside the 128-byte swizzle row
-                        ptx::mma_f8f6f4(d, adesc + 2u * k, bdesc + 2u * k, idesc, k > 0 ? 1u : 0u);
-                    ptx::mma_commit(empty(s));
-                    ptx::mma_commit(tfull(b));
+            for (int i = 0; i < STAGES * KBP; ++i) {
+                adesc[i] = ptx::desc_kmajor_sw128(ptx::smem_addr(tiles_a + (size_t)i * p.a_stride));
+                bdesc[i] = ptx::desc_kmajor_sw128(ptx::smem_addr(tiles_b + (size_t)i * p.b_stride));
+            }
+#pragma unroll
+            for (int b = 0; b < TMEM_BUFS; ++b)
+                dcol[b] = tmem_base + (uint32_t)(b * BN);
+            // the stages this CTA consumes, in order; with KBP > 1 (dense
+            // problems only) every tile takes spt stages, the last holding
+            // last_nk K-blocks, and the buffers of the missing K-blocks are
+            // passed through (committed with no MMA) to keep the rotation fixed
+            int total = 0;
+            for (int t = blockIdx.x; t < num_tiles; t += gridDim.x)
+                total += (get_tile(sc, gt, t).num_kb + KBP - 1) / KBP;
+            const int spt = (sc.num_kb + KBP - 1) / KBP;
+            const int last_nk = sc.num_kb - (spt - 1) * KBP;
+            bool ok = true;
+            for (int q0 = 0; q0 < total && ok; q0 += U) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int q = q0 + u;
+                    if (q < total && ok) {
+                        const int s = u % STAGES;
+                        const int g = u % NG;
+                        const int nk = KBP == 1 ? 1 : (q % spt == spt - 1 ? last_nk : KBP);
+                        bool got = ptx::mbar_wait(full(s), ((uint32_t)q / STAGES) & 1u, abort_flag, err, kErrTimeout,
+                                                  p.limit_ns);
+#pragma unroll
+                        for (int j = 0; j < KBP; ++j) {
+                            const uint32_t tb = (uint32_t)q * KBP + j;
+                            got = got && ptx::mbar_wait(tempty(g * KBP + j), ((tb / TMEM_BUFS) & 1u) ^ 1u, abort_flag,
+                                                        err, kErrTimeout, p.limit_ns);
+                        }
+                        if (!got) {
+                            ok = false;
+                        } else {
+                            ptx::tc_fence_after();
+#pragma unroll
+                            for (int j = 0; j < KBP; ++j) {
+                                if (j < nk) {
+#pragma unroll
+                                    for (int k = 0; k < 4; ++k) // 4 x K=32 (32 bytes) in the 128-byte swizzle row
+                                        ptx::mma_f8f6f4(dcol[g * KBP + j], adesc[s * KBP + j] + 2u * k,
+                                                        bdesc[s * KBP + j] + 2u * k, idesc, k > 0 ? 1u : 0u);
+                                }
+                                ptx::mma_commit(tfull(g * KBP + j));
+                            }
+                            ptx::mma_commit(empty(s));
+                        }
+                    }
                 }
             }
             ptx::mma_commit(done);
@@ -254,7 +313,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                            ? __ldg(p.sb + ti.e * p.sb_e_stride + (int64_t)(n0 >> 7) * p.kb_total + ti.kb0)
                            : 0.0f;
         };
-        if ((int)blockIdx.x < num_tiles)
+        if (PF == 1 && (int)blockIdx.x < num_tiles)
             load_first(get_tile(sc, gt, blockIdx.x));
 
         uint32_t tb = 0;
@@ -273,29 +332,21 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             for (int j = 0; j < C::kCols / 2; ++j)
                 acc[j] = make_float2(0.0f, 0.0f);
 
-            for (int kb = 0; kb < ti.num_kb; ++kb, ++tb) {
-                const float sa = sa_n;
-                const float s = PER_ROW_B ? 0.0f : __fmul_rn(sa, sb_n);
-                if (kb + 1 < ti.num_kb) {
-                    const int kn = ti.kb0 + kb + 1;
-                    sa_n = load_ok ? __ldg(sa_ptr + (int64_t)kn * p.sa_ld) : 0.0f;
-                    if (!PER_ROW_B)
-                        sb_n = col_ok ? __ldg(sb_ptr + kn) : 0.0f;
-                } else if (t + (int)gridDim.x < num_tiles) {
-                    load_first(get_tile(sc, gt, t + gridDim.x));
-                }
+            // fold one K-block's accumulator buffer into acc with scale s (row scale sa for PER_ROW_B)
+            // (use = false: a K-block past the tile's end, whose buffer only passes through)
+            auto fold = [&](float sa, float s, bool use) -> bool {
                 const int b = (int)(tb % TMEM_BUFS);
                 const uint32_t tph = (tb / TMEM_BUFS) & 1u;
                 const int slot = (int)(tb % SB);
                 bool got = ptx::mbar_wait(tfull(b), tph, abort_flag, err, kErrTimeout, p.limit_ns);
                 if (PER_ROW_B)
                     got = got && ptx::mbar_wait(sfull(slot), (tb / SB) & 1u, abort_flag, err, kErrTimeout, p.limit_ns);
-                if (!__all_sync(0xFFFFFFFFu, got)) { // keep the warp converged for tcgen05.ld
-                    ok = false;
-                    break;
-                }
+                if (!__all_sync(0xFFFFFFFFu, got)) // keep the warp converged for tcgen05.ld
+                    return false;
                 ptx::tc_fence_after();
                 const float *sbs = sb_ring + (size_t)slot * BN + col0;
+                // decode slices: a warp whose 32 rows are all past the tile's rows has nothing to keep
+                if (use && (BN > 64 || ti.a_row0 + quarter * 32 < ti.m_end))
 #pragma unroll
                 for (int ch = 0; ch < C::kCols / CH; ++ch) {
                     uint32_t P[CH];
@@ -331,6 +382,58 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                     if (PER_ROW_B)
                         ptx::mbar_arrive(sempty(slot));
                 }
+                ++tb;
+                return true;
+            };
+            if constexpr (PF == 1) {
+                for (int kb = 0; kb < ti.num_kb; ++kb) {
+                    const float sa = sa_n;
+                    const float s = PER_ROW_B ? 0.0f : __fmul_rn(sa, sb_n);
+                    if (kb + 1 < ti.num_kb) {
+                        const int kn = ti.kb0 + kb + 1;
+                        sa_n = load_ok ? __ldg(sa_ptr + (int64_t)kn * p.sa_ld) : 0.0f;
+                        if (!PER_ROW_B)
+                            sb_n = col_ok ? __ldg(sb_ptr + kn) : 0.0f;
+                    } else if (t + (int)gridDim.x < num_tiles) {
+                        load_first(get_tile(sc, gt, t + gridDim.x));
+                    }
+                    if (!fold(sa, s, true)) {
+                        ok = false;
+                        break;
+                    }
+                }
+            } else {
+                // the scales of PF K-blocks in flight: a decode slice spends too little
+                // time per K-block to hide one global load behind the next
+                float qa[PF], qb[PF];
+#pragma unroll
+                for (int u = 0; u < PF; ++u) {
+                    const bool in = u < ti.num_kb;
+                    qa[u] = in && load_ok ? __ldg(sa_ptr + (int64_t)(ti.kb0 + u) * p.sa_ld) : 0.0f;
+                    qb[u] = !PER_ROW_B && in && col_ok ? __ldg(sb_ptr + ti.kb0 + u) : 0.0f;
+                }
+                for (int kb0 = 0; kb0 < ti.num_kb && ok; kb0 += PF) {
+#pragma unroll
+                    for (int u = 0; u < PF; ++u) {
+                        const int kb = kb0 + u;
+                        if (kb < ti.num_kb && ok) {
+                            const float sa = qa[u];
+                            const float s = PER_ROW_B ? 0.0f : __fmul_rn(sa, qb[u]);
+                            const int kn = kb + PF;
+                            if (kn < ti.num_kb) {
+                                qa[u] = load_ok ? __ldg(sa_ptr + (int64_t)(ti.kb0 + kn) * p.sa_ld) : 0.0f;
+                                if (!PER_ROW_B)
+                                    qb[u] = col_ok ? __ldg(sb_ptr + ti.kb0 + kn) : 0.0f;
+                            }
+                            ok = fold(sa, s, true);
+                        }
+                    }
+                }
+            }
+            if constexpr (KBP > 1) {
+                const int padded = (ti.num_kb + KBP - 1) / KBP * KBP;
+                for (int kb = ti.num_kb; kb < padded && ok; ++kb)
+                    ok = fold(0.0f, 0.0f, false);
             }
             if (!ok)
                 break;
@@ -397,28 +500,47 @@ EncodeTiledFn encode_fn()
 } // namespace
 
 cudaError_t make_kmajor_map(CUtensorMap *map, const void *base, int64_t k_extent, int64_t rows, int64_t ld,
-                            int box_rows)
+                            int box_rows, int kb_per_box)
 {
     EncodeTiledFn fn = encode_fn();
     if (!fn)
         return cudaErrorNotSupported;
-    const cuuint64_t dims[2] = {(cuuint64_t)k_extent, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)ld};
-    const cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
-    const cuuint32_t estr[2] = {1u, 1u};
-    const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r;
+    if (kb_per_box <= 1) {
+        const cuuint64_t dims[2] = {(cuuint64_t)k_extent, (cuuint64_t)rows};
+        const cuuint64_t strides[1] = {(cuuint64_t)ld};
+        const cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+        const cuuint32_t estr[2] = {1u, 1u};
+        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    } else {
+        // (128 bytes of a K-block, row, K-block): the K-block axis steps 128 bytes
+        // along the row, so one box lands as kb_per_box consecutive 128-byte-wide
+        // swizzled tiles, each the layout a single K-block box would give
+        if (k_extent % 128 != 0)
+            return cudaErrorInvalidValue;
+        const cuuint64_t dims[3] = {128u, (cuuint64_t)rows, (cuuint64_t)(k_extent / 128)};
+        const cuuint64_t strides[2] = {(cuuint64_t)ld, 128u};
+        const cuuint32_t box[3] = {128u, (cuuint32_t)box_rows, (cuuint32_t)kb_per_box};
+        const cuuint32_t estr[3] = {1u, 1u, 1u};
+        r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(base), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    }
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 namespace {
 
-template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B>
+template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B, int A_STRIDE_MAX = 16384, int KBP = 1,
+          int PF = 1>
 cudaError_t run(const GemmProblem &g, cudaStream_t st)
 {
-    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS>;
-    auto kern = k_gemm_b128<BN, EPI_WARPS, STAGES, TMEM_BUFS, PER_ROW_B>;
+    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS, A_STRIDE_MAX, KBP>;
+    auto kern = k_gemm_b128<BN, EPI_WARPS, STAGES, TMEM_BUFS, PER_ROW_B, A_STRIDE_MAX, KBP, PF>;
+    if (KBP > 1 && g.group != GroupKind::None)
+        return cudaErrorInvalidValue; // multi-K-block boxes serve dense problems only
     static int configured_device = -1;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -437,9 +559,9 @@ cudaError_t run(const GemmProblem &g, cudaStream_t st)
     const int box_a = g.M >= 128 ? 128 : (int)((g.M + 7) / 8 * 8);
     const int box_b = b_rows >= BN ? BN : (int)((b_rows + 7) / 8 * 8);
     CUtensorMap ta, tbm;
-    if ((e = make_kmajor_map(&ta, g.a, g.K, g.M, g.lda, box_a)) != cudaSuccess)
+    if ((e = make_kmajor_map(&ta, g.a, g.K, g.M, g.lda, box_a, KBP)) != cudaSuccess)
         return e;
-    if ((e = make_kmajor_map(&tbm, g.b, g.K, b_rows, g.ldb, box_b)) != cudaSuccess)
+    if ((e = make_kmajor_map(&tbm, g.b, g.K, b_rows, g.ldb, box_b, KBP)) != cudaSuccess)
         return e;
     KParams kp;
     Sched &s = kp.sched;
@@ -461,6 +583,12 @@ cudaError_t run(const GemmProblem &g, cudaStream_t st)
     kp.sb_e_stride = g.group == GroupKind::Rows ? (g.N / 128) * (g.K / 128) : 0;
     kp.box_a_rows = box_a;
     kp.box_b_rows = box_b;
+    kp.a_stride = A_STRIDE_MAX < 16384 ? box_a * 128 : 16384;
+    // a multi-K-block box packs its K-blocks box-height apart (an N below BN
+    // reads rows past the box as don't-care columns, never stored)
+    kp.b_stride = KBP > 1 ? box_b * 128 : C::kBBytes;
+    if (kp.a_stride > A_STRIDE_MAX)
+        return cudaErrorInvalidValue; // a batch too tall for this instance
     kp.out = g.out;
     kp.ldo = g.ldo;
     kp.out_e_stride = g.group == GroupKind::K ? g.M * g.ldo : 0;
@@ -485,10 +613,19 @@ cudaError_t launch_gemm_block128(const GemmProblem &g, GemmShape shape, cudaStre
 {
     if (g.M == 0)
         return cudaSuccess;
-    const bool per_row = g.bscale == BScale::PerRow;
+    // per-row B scales come with WGrad, which always runs the training shape
+    if (g.bscale == BScale::PerRow)
+        return run<256, 8, 4, 2, true>(g, st);
     if (shape == GemmShape::Train)
-        return per_row ? run<256, 8, 4, 2, true>(g, st) : run<256, 8, 4, 2, false>(g, st);
-    return per_row ? run<32, 4, 10, 16, true>(g, st) : run<32, 4, 10, 16, false>(g, st);
+        return run<256, 8, 4, 2, false>(g, st);
+    // decode: 32 weight rows per tile, four K-blocks per copy, scales eight
+    // K-blocks ahead; a batch of up to 32 (64) tokens packs its A K-blocks
+    // 4 KB (8 KB) apart
+    if (g.M <= 32)
+        return run<32, 4, 6, 8, false, 4096, 4, 8>(g, st);
+    if (g.M <= 64)
+        return run<32, 4, 4, 8, false, 8192, 4, 8>(g, st);
+    return run<32, 4, 8, 8, false, 16384, 1, 8>(g, st);
 }
 
 cudaError_t gemm_read_and_clear_error(cudaStream_t st, unsigned *out)

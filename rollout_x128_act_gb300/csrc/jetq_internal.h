@@ -106,9 +106,10 @@ cudaError_t gemm_mx_read_and_clear_error(cudaStream_t st, unsigned *out);
 cudaError_t gemm_read_and_clear_error(cudaStream_t st, unsigned *out);
 
 // TMA descriptor for a K-major byte matrix [rows x k_extent], row stride ld,
-// boxes of 128 bytes x box_rows, 128-byte swizzle, zero fill out of bounds.
+// boxes of 128 bytes x box_rows (x kb_per_box consecutive K-blocks, as a 3-D
+// map, when kb_per_box > 1), 128-byte swizzle, zero fill out of bounds.
 cudaError_t make_kmajor_map(CUtensorMap *map, const void *base, int64_t k_extent, int64_t rows, int64_t ld,
-                            int box_rows);
+                            int box_rows, int kb_per_box = 1);
 
 // Number of SMs of the current device (cached per device).
 int sm_count();

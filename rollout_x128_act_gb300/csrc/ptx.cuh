@@ -104,6 +104,15 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
 
 // Tiled 2-D load delivered to the same shared-memory offset, and completed on
 // the same mbarrier offset, in every CTA of the cluster named in cta_mask.
+// 3-D tiled load: coordinates (x, y, z) in the map's element units
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y, int z)
+{
+    asm volatile("cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+                 "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y,
                                                       uint16_t cta_mask)
 {

@@ -43,7 +43,10 @@ def _oracle_operands(x, w, dy):
     return X, W, DY, Xc, DYc
 
 
-@pytest.mark.parametrize("N,D,C", [(256, 512, 512), (300, 512, 384), (1, 256, 256), (129, 768, 128)])
+# (20, 384, 640) and (48, 256, 896): decode batches whose K-block counts (5, 3;
+# 7, 2) leave a partly out-of-range multi-K-block copy at the end of each tile
+@pytest.mark.parametrize("N,D,C", [(256, 512, 512), (300, 512, 384), (1, 256, 256), (129, 768, 128),
+                                   (20, 384, 640), (48, 256, 896)])
 def test_three_gemms_against_oracle(N, D, C):
     x, w, dy = _layer(N, D, C, seed=N + D)
     ax, ady, (qw, sw, qwt, swt) = _gpu_quant(x, w, dy)
@@ -128,7 +131,7 @@ def test_rollout_fprop_equals_training_fprop_bitwise():
     qw, sw, _, _ = jq.quant_weight(to_dev_bf16(w), transposed=False)
     ax = jq.quant_act(tx, col=False)
     y_train = jq.fprop(ax["q_row"], ax["s_row"], qw, sw, path=jq.PATH_TRAIN)
-    for n in (1, 8, 64, 256):
+    for n in (1, 8, 20, 33, 64, 256):
         a = jq.quant_act(tx[:n], col=False)  # rollout quantizes its own batch
         assert torch.equal(a["q_row"], ax["q_row"][:n])
         y_dec = jq.fprop(a["q_row"], a["s_row"], qw, sw, path=jq.PATH_DECODE)
