@@ -59,8 +59,6 @@ struct KParams {
     int64_t sb_e_stride;    // floats between experts' weight scales
     int box_a_rows;
     int box_b_rows;
-    int a_stride;           // bytes between A K-block tiles
-    int b_stride;           // bytes between B K-block tiles
     void *out;
     int64_t ldo;
     int64_t out_e_stride;   // elements between experts' outputs (grouped K)
@@ -180,8 +178,8 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                         break;
                     }
                     ptx::mbar_arrive_expect_tx(full(s), tx);
-                    const uint32_t da = ptx::smem_addr(tiles_a + (size_t)s * KBP * p.a_stride);
-                    const uint32_t db = ptx::smem_addr(tiles_b + (size_t)s * KBP * p.b_stride);
+                    const uint32_t da = ptx::smem_addr(tiles_a + (size_t)s * KBP * A_STRIDE_MAX);
+                    const uint32_t db = ptx::smem_addr(tiles_b + (size_t)s * KBP * C::kBBytes);
                     if constexpr (KBP == 1) {
                         ptx::tma_load_2d(da, &tmA, full(s), (ti.kb0 + kb) * 128, ti.a_row0);
                         ptx::tma_load_2d(db, &tmB, full(s), (ti.kb0 + kb) * 128, ti.b_row0);
@@ -200,29 +198,19 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             }
         } else if (warp == 1 && lane == 0) {
             // -------------------------------------------------- MMA issuer
-            // Every operand an MMA takes (stage descriptors, accumulator
-            // columns) is computed once, here, and the loop below is unrolled
-            // so that each MMA picks its operands by a compile-time index: an
-            // operand computed inside the loop costs the issue a few hundred
-            // cycles, more than a narrow MMA takes to run.
+            // Every MMA operand is a base register plus a compile-time offset
+            // (the loop below is unrolled so that stage and buffer indices are
+            // constants): an operand computed inside the loop costs the issue a
+            // few hundred cycles, more than a narrow MMA takes to run.
             constexpr uint32_t idesc = ptx::idesc_e4m3_f32(128, BN);
-            constexpr int NG = TMEM_BUFS / KBP; // buffer groups of KBP buffers, one group per stage
+            constexpr int NG = TMEM_BUFS / KBP; // accumulator groups: one per stage, KBP buffers each
             constexpr int U = lcm_int(STAGES, NG);
             static_assert(TMEM_BUFS % KBP == 0, "buffer groups");
-            uint64_t adesc[STAGES * KBP], bdesc[STAGES * KBP];
-            uint32_t dcol[TMEM_BUFS];
-#pragma unroll
-            for (int i = 0; i < STAGES * KBP; ++i) {
-                adesc[i] = ptx::desc_kmajor_sw128(ptx::smem_addr(tiles_a + (size_t)i * p.a_stride));
-                bdesc[i] = ptx::desc_kmajor_sw128(ptx::smem_addr(tiles_b + (size_t)i * p.b_stride));
-            }
-#pragma unroll
-            for (int b = 0; b < TMEM_BUFS; ++b)
-                dcol[b] = tmem_base + (uint32_t)(b * BN);
+            const uint64_t adesc0 = ptx::desc_kmajor_sw128(ptx::smem_addr(tiles_a));
+            const uint64_t bdesc0 = ptx::desc_kmajor_sw128(ptx::smem_addr(tiles_b));
             // the stages this CTA consumes, in order; with KBP > 1 (dense
             // problems only) every tile takes spt stages, the last holding
-            // last_nk K-blocks, and the buffers of the missing K-blocks are
-            // passed through (committed with no MMA) to keep the rotation fixed
+            // last_nk K-blocks; the buffers of missing K-blocks stay unused
             int total = 0;
             for (int t = blockIdx.x; t < num_tiles; t += gridDim.x)
                 total += (get_tile(sc, gt, t).num_kb + KBP - 1) / KBP;
@@ -235,31 +223,29 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                     const int q = q0 + u;
                     if (q < total && ok) {
                         const int s = u % STAGES;
-                        const int g = u % NG;
+                        const int gi = u % NG;
                         const int nk = KBP == 1 ? 1 : (q % spt == spt - 1 ? last_nk : KBP);
-                        bool got = ptx::mbar_wait(full(s), ((uint32_t)q / STAGES) & 1u, abort_flag, err, kErrTimeout,
-                                                  p.limit_ns);
-#pragma unroll
-                        for (int j = 0; j < KBP; ++j) {
-                            const uint32_t tb = (uint32_t)q * KBP + j;
-                            got = got && ptx::mbar_wait(tempty(g * KBP + j), ((tb / TMEM_BUFS) & 1u) ^ 1u, abort_flag,
-                                                        err, kErrTimeout, p.limit_ns);
-                        }
-                        if (!got) {
+                        if (!ptx::mbar_wait(tempty(gi), (((uint32_t)q / NG) & 1u) ^ 1u, abort_flag, err, kErrTimeout,
+                                            p.limit_ns) ||
+                            !ptx::mbar_wait(full(s), ((uint32_t)q / STAGES) & 1u, abort_flag, err, kErrTimeout,
+                                            p.limit_ns)) {
                             ok = false;
                         } else {
                             ptx::tc_fence_after();
 #pragma unroll
                             for (int j = 0; j < KBP; ++j) {
                                 if (j < nk) {
+                                    // descriptors address 16-byte units
+                                    const uint64_t ad = adesc0 + (uint64_t)(((s * KBP + j) * A_STRIDE_MAX) >> 4);
+                                    const uint64_t bd = bdesc0 + (uint64_t)(((s * KBP + j) * C::kBBytes) >> 4);
+                                    const uint32_t d = tmem_base + (uint32_t)((gi * KBP + j) * BN);
 #pragma unroll
                                     for (int k = 0; k < 4; ++k) // 4 x K=32 (32 bytes) in the 128-byte swizzle row
-                                        ptx::mma_f8f6f4(dcol[g * KBP + j], adesc[s * KBP + j] + 2u * k,
-                                                        bdesc[s * KBP + j] + 2u * k, idesc, k > 0 ? 1u : 0u);
+                                        ptx::mma_f8f6f4(d, ad + 2u * k, bd + 2u * k, idesc, k > 0 ? 1u : 0u);
                                 }
-                                ptx::mma_commit(tfull(g * KBP + j));
                             }
                             ptx::mma_commit(empty(s));
+                            ptx::mma_commit(tfull(gi));
                         }
                     }
                 }
@@ -332,13 +318,19 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             for (int j = 0; j < C::kCols / 2; ++j)
                 acc[j] = make_float2(0.0f, 0.0f);
 
-            // fold one K-block's accumulator buffer into acc with scale s (row scale sa for PER_ROW_B)
+            // fold one K-block's accumulator buffer into acc with scale s (row scale sa for PER_ROW_B);
+            // buffers come in groups of KBP, one group per stage, waited for at the group's
+            // first K-block and released after its last
             // (use = false: a K-block past the tile's end, whose buffer only passes through)
             auto fold = [&](float sa, float s, bool use) -> bool {
+                constexpr int NG = TMEM_BUFS / KBP;
+                const int j = (int)(tb % KBP);
+                const int gi = (int)((tb / KBP) % NG);
                 const int b = (int)(tb % TMEM_BUFS);
-                const uint32_t tph = (tb / TMEM_BUFS) & 1u;
                 const int slot = (int)(tb % SB);
-                bool got = ptx::mbar_wait(tfull(b), tph, abort_flag, err, kErrTimeout, p.limit_ns);
+                bool got = true;
+                if (j == 0)
+                    got = ptx::mbar_wait(tfull(gi), ((tb / KBP) / NG) & 1u, abort_flag, err, kErrTimeout, p.limit_ns);
                 if (PER_ROW_B)
                     got = got && ptx::mbar_wait(sfull(slot), (tb / SB) & 1u, abort_flag, err, kErrTimeout, p.limit_ns);
                 if (!__all_sync(0xFFFFFFFFu, got)) // keep the warp converged for tcgen05.ld
@@ -378,7 +370,8 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                 ptx::tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    ptx::mbar_arrive(tempty(b));
+                    if (j == KBP - 1)
+                        ptx::mbar_arrive(tempty(gi));
                     if (PER_ROW_B)
                         ptx::mbar_arrive(sempty(slot));
                 }
@@ -554,9 +547,14 @@ cudaError_t run(const GemmProblem &g, cudaStream_t st)
     }
     // B rows the map covers: one weight, or every expert's stacked
     const int64_t b_rows = g.group == GroupKind::Rows ? g.N * g.num_experts : g.N;
-    // boxes never taller than the tensor; rows of a stage past the box keep
-    // stale bytes, which only reach accumulator rows/columns that are not stored
-    const int box_a = g.M >= 128 ? 128 : (int)((g.M + 7) / 8 * 8);
+    // single-K-block boxes are never taller than the tensor: rows of a stage
+    // past the box keep stale bytes, which only reach accumulator rows/columns
+    // that are not stored.  A multi-K-block box lays its K-blocks one box
+    // height apart, so its A box is exactly as tall as the K-block stride
+    // (rows past the batch arrive zero-filled).
+    if (KBP > 1 && (b_rows < BN || g.M > A_STRIDE_MAX / 128))
+        return cudaErrorInvalidValue;
+    const int box_a = KBP > 1 ? A_STRIDE_MAX / 128 : (g.M >= 128 ? 128 : (int)((g.M + 7) / 8 * 8));
     const int box_b = b_rows >= BN ? BN : (int)((b_rows + 7) / 8 * 8);
     CUtensorMap ta, tbm;
     if ((e = make_kmajor_map(&ta, g.a, g.K, g.M, g.lda, box_a, KBP)) != cudaSuccess)
@@ -583,12 +581,7 @@ cudaError_t run(const GemmProblem &g, cudaStream_t st)
     kp.sb_e_stride = g.group == GroupKind::Rows ? (g.N / 128) * (g.K / 128) : 0;
     kp.box_a_rows = box_a;
     kp.box_b_rows = box_b;
-    kp.a_stride = A_STRIDE_MAX < 16384 ? box_a * 128 : 16384;
-    // a multi-K-block box packs its K-blocks box-height apart (an N below BN
-    // reads rows past the box as don't-care columns, never stored)
-    kp.b_stride = KBP > 1 ? box_b * 128 : C::kBBytes;
-    if (kp.a_stride > A_STRIDE_MAX)
-        return cudaErrorInvalidValue; // a batch too tall for this instance
+
     kp.out = g.out;
     kp.ldo = g.ldo;
     kp.out_e_stride = g.group == GroupKind::K ? g.M * g.ldo : 0;
@@ -618,6 +611,8 @@ cudaError_t launch_gemm_block128(const GemmProblem &g, GemmShape shape, cudaStre
         return run<256, 8, 4, 2, true>(g, st);
     if (shape == GemmShape::Train)
         return run<256, 8, 4, 2, false>(g, st);
+    if (gemm_decode_swapped_applies(g))
+        return launch_gemm_decode_swapped(g, st);
     // decode: 32 weight rows per tile, four K-blocks per copy, scales eight
     // K-blocks ahead; a batch of up to 32 (64) tokens packs its A K-blocks
     // 4 KB (8 KB) apart

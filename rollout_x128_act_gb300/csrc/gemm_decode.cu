@@ -1,0 +1,441 @@
+// Decode-shaped FP8 GEMM, 128-block recipe, with the operands swapped.
+//
+//   y[t, o] = sum over K-blocks kb of  fl32(Sx[t,kb] * Sw[o/128,kb]) * P_kb[t, o]
+//   P_kb[t, o] = sum_{k in kb} qx[t, k] * qw[o, k]        (E4M3 x E4M3 -> FP32)
+//
+// A rollout step multiplies a handful of tokens (n <= 64) by a whole weight,
+// so the weight stream is the work.  Here the weight is the MMA's A operand
+// (M = 128 weight rows per tile) and the tokens its N operand (NB = 16, 32 or
+// 64 columns, the rows past n zero-filled by TMA): one tcgen05.mma then
+// covers 4 KB of weight, four times what the token-row orientation covers,
+// and every TMEM lane holds a live output feature.  The per-element
+// operation sequence is the training kernel's (ascending K-blocks, one fresh
+// FP32 partial per K-block, acc = fma(P_kb, fl32(Sx * Sw), acc)), so a row of
+// this kernel's output equals the training kernel's row bit for bit.
+//
+//   warp 0      TMA producer: per stage KBP K-blocks of the 128-row weight
+//               tile and of the token rows, one 3-D box each
+//   warp 1      MMA issuer: per K-block 4 x tcgen05.mma (K = 32) into its own
+//               TMEM buffer; one commit per stage releases the smem stage
+//               and hands the stage's buffer group to the epilogue
+//   warp 2      scale producer: per K-block the NB products fl32(Sx * Sw)
+//               into a shared-memory ring
+//   warps 4-7   epilogue: per K-block tcgen05.ld the partial (TMEM lanes =
+//               weight rows, columns = tokens), acc = fma(P, s, acc); after
+//               the last K-block, store y[t, o] for t < n (coalesced along o)
+//
+// One CTA per SM, persistent over 128-row weight tiles.  Every mbarrier wait
+// is bounded; a CTA that gives up raises its abort flag, records the error
+// in the device error word, drains its TMA copies and MMAs (bounded) and
+// frees its TMEM.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "jetq_internal.h"
+#include "ptx.cuh"
+
+namespace jetq {
+
+__device__ unsigned g_gemm_decode_error;
+
+namespace {
+
+constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned long long kWaitLimitNs = 2000000000ull; // 2 s per wait
+
+__host__ __device__ constexpr int gcd_i(int a, int b) { return b ? gcd_i(b, a % b) : a; }
+__host__ __device__ constexpr int lcm_i(int a, int b) { return a / gcd_i(a, b) * b; }
+
+struct DParams {
+    const float *sx;  // token scales [K-blocks x n]
+    const float *sw;  // weight block scales [D/128 x num_kb]
+    int n;            // tokens
+    int tiles;        // D / 128
+    int num_kb;       // K / 128
+    void *out;        // y [n x ldo]
+    int64_t ldo;
+    int out_bf16;
+    unsigned long long limit_ns;
+};
+
+template <int NB, int STAGES, int KBP, int TMEM_BUFS>
+struct DCfg {
+    static constexpr int kWBytes = 128 * 128; // one K-block of the 128-row weight tile
+    static constexpr int kXBytes = NB * 128;  // one K-block of the token rows
+    static constexpr int NG = TMEM_BUFS / KBP; // accumulator groups: one per stage, KBP buffers each
+    static constexpr int kSlots = 16;          // scale-row ring
+    static constexpr int kThreads = 256;
+    static constexpr int kBars = 2 * STAGES + 2 * NG + 2 * kSlots + 1;
+    static constexpr size_t kSmem =
+        1024 + (size_t)STAGES * KBP * (kWBytes + kXBytes) + (size_t)kSlots * NB * 4 + 1024;
+    static_assert(NB % 16 == 0 && NB >= 16 && NB <= 64, "token columns");
+    static_assert(TMEM_BUFS % KBP == 0 && TMEM_BUFS * NB <= 512, "TMEM buffers");
+    static_assert(kBars * 8 + 16 <= 1024, "barrier area");
+    static_assert(kSmem <= 232448, "shared memory");
+};
+
+template <int NB, int STAGES, int KBP, int TMEM_BUFS>
+__global__ void __launch_bounds__(256, 1)
+    k_gemm_decode(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX, const DParams p)
+{
+    using C = DCfg<NB, STAGES, KBP, TMEM_BUFS>;
+    constexpr int NG = C::NG;
+    constexpr int SL = C::kSlots;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *tiles_w = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *tiles_x = tiles_w + (size_t)STAGES * KBP * C::kWBytes;
+    float *srow = reinterpret_cast<float *>(tiles_x + (size_t)STAGES * KBP * C::kXBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(srow + SL * NB);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kBars);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+    const uint32_t bar0 = ptx::smem_addr(bars);
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    auto tfull = [&](int g) { return bar0 + 8u * (2 * STAGES + g); };
+    auto tempty = [&](int g) { return bar0 + 8u * (2 * STAGES + NG + g); };
+    auto sfull = [&](int i) { return bar0 + 8u * (2 * STAGES + 2 * NG + i); };
+    auto sempty = [&](int i) { return bar0 + 8u * (2 * STAGES + 2 * NG + SL + i); };
+    const uint32_t done = bar0 + 8u * (2 * STAGES + 2 * NG + 2 * SL);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    unsigned *err = &g_gemm_decode_error;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            ptx::mbar_init(full(s), 1);
+            ptx::mbar_init(empty(s), 1);
+        }
+        for (int g = 0; g < NG; ++g) {
+            ptx::mbar_init(tfull(g), 1);
+            ptx::mbar_init(tempty(g), 4);
+        }
+        for (int i = 0; i < SL; ++i) {
+            ptx::mbar_init(sfull(i), 32);
+            ptx::mbar_init(sempty(i), 4);
+        }
+        ptx::mbar_init(done, 1);
+        *abort_flag = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        ptx::prefetch_tensormap(&tmW);
+        ptx::prefetch_tensormap(&tmX);
+    }
+    if (warp == 1) {
+        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+
+    const int nkb = p.num_kb;
+    const int spt = (nkb + KBP - 1) / KBP; // stages per tile
+    const int last_nk = nkb - (spt - 1) * KBP;
+    int my_tiles = 0;
+    for (int t = blockIdx.x; t < p.tiles; t += gridDim.x)
+        ++my_tiles;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ---------------------------------------------------- TMA producer
+            // a box past the last K-block is zero-filled and still counts in full
+            constexpr uint32_t tx = (uint32_t)(KBP * (C::kWBytes + C::kXBytes));
+            uint32_t it = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
+                for (int q = 0; q < spt; ++q, ++it) {
+                    const int s = (int)(it % STAGES);
+                    if (!ptx::mbar_wait(empty(s), ((it / STAGES) & 1u) ^ 1u, abort_flag, err, kErrTimeout, p.limit_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(full(s), tx);
+                    ptx::tma_load_3d(ptx::smem_addr(tiles_w + (size_t)s * KBP * C::kWBytes), &tmW, full(s), 0, t * 128,
+                                     q * KBP);
+                    ptx::tma_load_3d(ptx::smem_addr(tiles_x + (size_t)s * KBP * C::kXBytes), &tmX, full(s), 0, 0,
+                                     q * KBP);
+                }
+            }
+            // drain: every copy this thread started must have landed before exit
+            for (int s = 0; s < STAGES; ++s) {
+                if (it > (uint32_t)s) {
+                    const uint32_t last = (uint32_t)s + ((it - 1u - (uint32_t)s) / STAGES) * STAGES;
+                    ptx::mbar_wait(full(s), (last / STAGES) & 1u, abort_flag, err, kErrTimeout, p.limit_ns, false);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ---------------------------------------------------- MMA issuer
+            // operands are base registers plus compile-time offsets (the loop is
+            // unrolled so stage and buffer indices are constants): an operand
+            // computed inside the loop slows each issue by a few hundred cycles
+            constexpr uint32_t idesc = ptx::idesc_e4m3_f32(128, NB);
+            constexpr int U = lcm_i(STAGES, NG);
+            const uint64_t wdesc0 = ptx::desc_kmajor_sw128(ptx::smem_addr(tiles_w));
+            const uint64_t xdesc0 = ptx::desc_kmajor_sw128(ptx::smem_addr(tiles_x));
+            const int total = my_tiles * spt;
+            bool ok = true;
+            for (int q0 = 0; q0 < total && ok; q0 += U) {
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const int q = q0 + u;
+                    if (q < total && ok) {
+                        const int s = u % STAGES;
+                        const int gi = u % NG;
+                        const int nk = q % spt == spt - 1 ? last_nk : KBP;
+                        if (!ptx::mbar_wait(tempty(gi), (((uint32_t)q / NG) & 1u) ^ 1u, abort_flag, err, kErrTimeout,
+                                            p.limit_ns) ||
+                            !ptx::mbar_wait(full(s), ((uint32_t)q / STAGES) & 1u, abort_flag, err, kErrTimeout,
+                                            p.limit_ns)) {
+                            ok = false;
+                        } else {
+                            ptx::tc_fence_after();
+#pragma unroll
+                            for (int j = 0; j < KBP; ++j) {
+                                if (j < nk) {
+                                    // descriptors address 16-byte units
+                                    const uint64_t wd = wdesc0 + (uint64_t)(((s * KBP + j) * C::kWBytes) >> 4);
+                                    const uint64_t xd = xdesc0 + (uint64_t)(((s * KBP + j) * C::kXBytes) >> 4);
+                                    const uint32_t d = tmem_base + (uint32_t)((gi * KBP + j) * NB);
+#pragma unroll
+                                    for (int k = 0; k < 4; ++k) // 4 x K=32 (32 bytes) in the 128-byte swizzle row
+                                        ptx::mma_f8f6f4(d, wd + 2u * k, xd + 2u * k, idesc, k > 0 ? 1u : 0u);
+                                }
+                            }
+                            ptx::mma_commit(empty(s));
+                            ptx::mma_commit(tfull(gi));
+                        }
+                    }
+                }
+            }
+            ptx::mma_commit(done);
+            ptx::mbar_wait(done, 0u, abort_flag, err, kErrTimeout, p.limit_ns, false);
+        }
+        __syncwarp();
+    } else if (warp == 2) {
+        // ---------------------------------------------------- scale producer
+        // slot i holds s[t] = fl32(Sx[t, kb] * Sw[tile, kb]) for t < NB (0 past n);
+        // the loads of the next PFS K-blocks are in flight while a chunk is stored
+        constexpr int PFS = 8;
+        constexpr int TPL = (NB + 31) / 32; // tokens per lane
+        const int total = my_tiles * nkb;   // this CTA's K-blocks, tile after tile
+        auto fetch = [&](int gk, float (&xv)[TPL], float &wv) {
+            const int lt = gk / nkb, kb = gk - lt * nkb;
+            wv = __ldg(p.sw + (int64_t)(blockIdx.x + lt * gridDim.x) * nkb + kb);
+#pragma unroll
+            for (int h = 0; h < TPL; ++h) {
+                const int tt = lane + 32 * h;
+                xv[h] = tt < p.n ? __ldg(p.sx + (int64_t)kb * p.n + tt) : 0.0f;
+            }
+        };
+        float cx[PFS][TPL], cw[PFS];
+#pragma unroll
+        for (int u = 0; u < PFS; ++u)
+            if (u < total)
+                fetch(u, cx[u], cw[u]);
+        bool ok = true;
+        for (int c0 = 0; c0 < total && ok; c0 += PFS) {
+            float nx[PFS][TPL], nw[PFS];
+#pragma unroll
+            for (int u = 0; u < PFS; ++u)
+                if (c0 + PFS + u < total)
+                    fetch(c0 + PFS + u, nx[u], nw[u]);
+#pragma unroll
+            for (int u = 0; u < PFS; ++u) {
+                const uint32_t c = (uint32_t)(c0 + u);
+                if ((int)c < total && ok) {
+                    const int i = (int)(c % SL);
+                    const bool got = ptx::mbar_wait(sempty(i), ((c / SL) & 1u) ^ 1u, abort_flag, err, kErrTimeout,
+                                                    p.limit_ns);
+                    if (!__all_sync(0xFFFFFFFFu, got)) {
+                        ok = false;
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < TPL; ++h) {
+                            const int tt = lane + 32 * h;
+                            if (tt < NB)
+                                srow[i * NB + tt] = tt < p.n ? __fmul_rn(cx[u][h], cw[u]) : 0.0f;
+                        }
+                        ptx::mbar_arrive(sfull(i));
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < PFS; ++u) {
+                cw[u] = nw[u];
+#pragma unroll
+                for (int h = 0; h < TPL; ++h)
+                    cx[u][h] = nx[u][h];
+            }
+        }
+    } else if (warp >= 4) {
+        // ---------------------------------------------------- epilogue
+        const int quarter = warp & 3; // TMEM lanes 32*quarter .. +31 = weight rows of the tile
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        uint32_t c = 0, qg = 0;
+        bool ok = true;
+        for (int t = blockIdx.x; t < p.tiles && ok; t += gridDim.x) {
+            float2 acc[NB / 2];
+#pragma unroll
+            for (int j = 0; j < NB / 2; ++j)
+                acc[j] = make_float2(0.0f, 0.0f);
+            for (int q = 0; q < spt && ok; ++q, ++qg) {
+                const int gi = (int)(qg % NG);
+                const int nk = q == spt - 1 ? last_nk : KBP;
+                bool got = ptx::mbar_wait(tfull(gi), (qg / NG) & 1u, abort_flag, err, kErrTimeout, p.limit_ns);
+                if (!__all_sync(0xFFFFFFFFu, got)) { // keep the warp converged for tcgen05.ld
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+#pragma unroll
+                for (int j = 0; j < KBP; ++j) {
+                    if (j < nk && ok) {
+                        const int i = (int)(c % SL);
+                        got = ptx::mbar_wait(sfull(i), (c / SL) & 1u, abort_flag, err, kErrTimeout, p.limit_ns);
+                        if (!__all_sync(0xFFFFFFFFu, got)) {
+                            ok = false;
+                        } else {
+                            uint32_t P[NB / 16][16];
+                            const uint32_t col = tmem_base + lane_addr + (uint32_t)((gi * KBP + j) * NB);
+#pragma unroll
+                            for (int h = 0; h < NB / 16; ++h)
+                                ptx::tmem_ld_32x32b_x16(col + 16u * h, P[h]);
+                            ptx::tmem_ld_wait();
+                            const float4 *s4 = reinterpret_cast<const float4 *>(srow + i * NB);
+#pragma unroll
+                            for (int h = 0; h < NB / 4; ++h) {
+                                const float4 sv = s4[h];
+                                const uint32_t *ph = &P[h / 4][(h % 4) * 4];
+                                acc[2 * h] = __ffma2_rn(make_float2(__uint_as_float(ph[0]), __uint_as_float(ph[1])),
+                                                        make_float2(sv.x, sv.y), acc[2 * h]);
+                                acc[2 * h + 1] = __ffma2_rn(make_float2(__uint_as_float(ph[2]), __uint_as_float(ph[3])),
+                                                            make_float2(sv.z, sv.w), acc[2 * h + 1]);
+                            }
+                            __syncwarp();
+                            if (lane == 0)
+                                ptx::mbar_arrive(sempty(i));
+                            ++c;
+                        }
+                    }
+                }
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    ptx::mbar_arrive(tempty(gi));
+            }
+            if (!ok)
+                break;
+            const int64_t o = (int64_t)t * 128 + quarter * 32 + lane;
+            if (p.out_bf16) {
+                __nv_bfloat16 *y = reinterpret_cast<__nv_bfloat16 *>(p.out) + o;
+#pragma unroll
+                for (int h = 0; h < NB / 2; ++h) {
+                    if (2 * h < p.n)
+                        y[(int64_t)(2 * h) * p.ldo] = __float2bfloat16_rn(acc[h].x);
+                    if (2 * h + 1 < p.n)
+                        y[(int64_t)(2 * h + 1) * p.ldo] = __float2bfloat16_rn(acc[h].y);
+                }
+            } else {
+                float *y = reinterpret_cast<float *>(p.out) + o;
+#pragma unroll
+                for (int h = 0; h < NB / 2; ++h) {
+                    if (2 * h < p.n)
+                        y[(int64_t)(2 * h) * p.ldo] = acc[h].x;
+                    if (2 * h + 1 < p.n)
+                        y[(int64_t)(2 * h + 1) * p.ldo] = acc[h].y;
+                }
+            }
+        }
+    }
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem_base, 512);
+    }
+}
+
+template <int NB, int STAGES, int KBP, int TMEM_BUFS>
+cudaError_t run_decode(const GemmProblem &g, cudaStream_t st)
+{
+    using C = DCfg<NB, STAGES, KBP, TMEM_BUFS>;
+    auto kern = k_gemm_decode<NB, STAGES, KBP, TMEM_BUFS>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (configured_device != dev) {
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem)) !=
+            cudaSuccess)
+            return e;
+        configured_device = dev;
+    }
+    // weight: 128-row boxes; tokens: NB-row boxes (rows past n arrive zero-filled)
+    CUtensorMap tw, tx;
+    if ((e = make_kmajor_map(&tw, g.b, g.K, g.N, g.ldb, 128, KBP)) != cudaSuccess)
+        return e;
+    if ((e = make_kmajor_map(&tx, g.a, g.K, g.M, g.lda, NB, KBP)) != cudaSuccess)
+        return e;
+    DParams p;
+    p.sx = g.sa;
+    p.sw = g.sb;
+    p.n = (int)g.M;
+    p.tiles = (int)(g.N / 128);
+    p.num_kb = (int)(g.K / 128);
+    p.out = g.out;
+    p.ldo = g.ldo;
+    p.out_bf16 = g.out_dtype == JETQ_OUT_BF16;
+    p.limit_ns = kWaitLimitNs;
+    const int grid = p.tiles < sm_count() ? p.tiles : sm_count();
+    kern<<<grid, C::kThreads, C::kSmem, st>>>(tw, tx, p);
+    return cudaGetLastError();
+}
+
+} // namespace
+
+bool gemm_decode_swapped_applies(const GemmProblem &g)
+{
+    return g.group == GroupKind::None && g.bscale == BScale::Block128 && g.M >= 1 && g.M <= 64 &&
+           g.N % 128 == 0 && g.K % 128 == 0 && g.K > 0 && g.N / 128 >= kDecodeSwappedMinTiles && !g.accumulate;
+}
+
+cudaError_t launch_gemm_decode_swapped(const GemmProblem &g, cudaStream_t st)
+{
+    if (!gemm_decode_swapped_applies(g))
+        return cudaErrorInvalidValue;
+    // few large copies in flight (three stages of 3-4 K-blocks fill shared memory)
+    if (g.M <= 16)
+        return run_decode<16, 3, 4, 12>(g, st);
+    if (g.M <= 32)
+        return run_decode<32, 3, 3, 9>(g, st);
+    return run_decode<64, 3, 3, 6>(g, st);
+}
+
+cudaError_t gemm_decode_read_and_clear_error(cudaStream_t st, unsigned *out)
+{
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_gemm_decode_error, sizeof v, 0, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess)
+        return e;
+    *out |= v;
+    if (v) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_gemm_decode_error, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaStreamSynchronize(st);
+    }
+    return e;
+}
+
+} // namespace jetq

@@ -103,6 +103,15 @@ struct MxGemmProblem {
 cudaError_t launch_gemm_mx(const MxGemmProblem &p, cudaStream_t st);
 cudaError_t gemm_mx_read_and_clear_error(cudaStream_t st, unsigned *out);
 
+// Decode-shaped 128-block FProp/DGrad with the operands swapped (weight rows
+// as the MMA's M, tokens as its N): dense, B-block scales, 1 <= M <= 64
+// tokens, N a multiple of 128 with at least kDecodeSwappedMinTiles 128-row
+// weight tiles, K a multiple of 128.  Bitwise equal to launch_gemm_block128.
+constexpr int64_t kDecodeSwappedMinTiles = 32;
+bool gemm_decode_swapped_applies(const GemmProblem &g);
+cudaError_t launch_gemm_decode_swapped(const GemmProblem &g, cudaStream_t st);
+cudaError_t gemm_decode_read_and_clear_error(cudaStream_t st, unsigned *out);
+
 cudaError_t gemm_read_and_clear_error(cudaStream_t st, unsigned *out);
 
 // TMA descriptor for a K-major byte matrix [rows x k_extent], row stride ld,
