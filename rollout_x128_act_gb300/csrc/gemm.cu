@@ -606,9 +606,10 @@ cudaError_t launch_gemm_block128(const GemmProblem &g, GemmShape shape, cudaStre
 {
     if (g.M == 0)
         return cudaSuccess;
-    // per-row B scales come with WGrad, which always runs the training shape
+    // per-row B scales come with WGrad, which always runs the training shape;
+    // its longer epilogue profits from row scales two K-blocks ahead
     if (g.bscale == BScale::PerRow)
-        return run<256, 8, 4, 2, true>(g, st);
+        return run<256, 8, 4, 2, true, 16384, 1, 2>(g, st);
     if (shape == GemmShape::Train)
         return run<256, 8, 4, 2, false>(g, st);
     if (gemm_decode_swapped_applies(g))
