@@ -67,7 +67,9 @@ typedef enum {
 typedef enum {
     JETQ_PATH_AUTO = 0,   /* DECODE when N <= 256 tokens, else TRAIN */
     JETQ_PATH_TRAIN = 1,  /* wide tiles for large N */
-    JETQ_PATH_DECODE = 2  /* narrow tiles that spread the weight stream over every SM */
+    JETQ_PATH_DECODE = 2  /* few-token kernels that stream the weight: 1-64 tokens against >= 32
+                             weight row blocks run with weight rows as the MMA's M; otherwise
+                             narrow 32-row weight tiles; same per-element arithmetic as TRAIN */
 } jetq_path;
 
 typedef enum {

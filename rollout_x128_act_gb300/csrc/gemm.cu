@@ -12,8 +12,9 @@
 //   warp 0        TMA producer: A and B K-block tiles (128-byte swizzle) into
 //                 a STAGES-deep shared-memory ring
 //   warp 1        MMA issuer: 4 x tcgen05.mma (K = 32 each) per K-block into
-//                 TMEM buffer kb % TMEM_BUFS, then tcgen05.commit to release
-//                 the smem stage and to signal the epilogue
+//                 its TMEM buffer, then tcgen05.commit to release the smem
+//                 stage and to signal the epilogue (one commit per stage of
+//                 KBP K-blocks)
 //   warp 2        (WGrad) bulk copies of the per-column scales into a ring
 //   warp 3        builds the per-expert tile tables of a grouped launch
 //   warps 4..     epilogue: tcgen05.ld the K-block partial, acc = fma(P, s, acc)
@@ -21,12 +22,12 @@
 //                 the last K-block, store the tile
 //
 // One CTA per SM, persistent over output tiles.  The same template serves the
-// training shape (BN = 256, 8 epilogue warps, 2 TMEM buffers) and the decode
-// shape (BN = 32, 4 epilogue warps, 16 TMEM buffers, a narrow weight slice per
-// CTA so the weight stream spreads over every SM).  Both perform the identical
-// per-element operation sequence, so a decode row equals the corresponding
-// training row bit for bit.  Grouped launches (MoE experts) run the same
-// loop over per-expert tiles (sched.cuh).
+// training shape (BN = 256, 8 epilogue warps, 2 TMEM buffers) and a narrow
+// decode shape (BN = 32 weight rows per tile, 4 epilogue warps, four K-blocks
+// per TMA copy) for token batches that gemm_decode.cu does not take.  Both
+// perform the identical per-element operation sequence, so a decode row
+// equals the corresponding training row bit for bit.  Grouped launches (MoE
+// experts) run the same loop over per-expert tiles (sched.cuh).
 //
 // Every mbarrier wait is bounded (wall clock); a CTA that gives up raises a
 // shared abort flag, records the fact in the device error word, drains its
