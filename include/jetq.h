@@ -96,6 +96,21 @@ JETQ_API int jetq_version(void);
  */
 JETQ_API jetq_status jetq_check_device_error(void *stream);
 
+/*
+ * Diagnostic for the bounded waits (the pages have no counterpart: their
+ * kernels are not shown waiting at all).  Launches one CTA whose two waiters
+ * wait on shared-memory mbarriers that nothing ever completes, using the same
+ * wait primitive as the GEMM kernels: waiter 0 gives up after limit_ns of wall
+ * clock, raises the CTA's abort flag and records a timeout in the device error
+ * word; waiter 1 (limit 8 * limit_ns) gives up as soon as it sees the abort
+ * flag.  Each waiter writes the nanoseconds it waited to elapsed_ns[0..1]
+ * (caller-owned device memory, two int64).  The kernel faults nothing and
+ * leaves the context usable; jetq_check_device_error() afterwards returns
+ * JETQ_ERR_TIMEOUT once and clears the word.
+ * Limits: 1 ms <= limit_ns <= 1 s; elapsed_ns 8-byte aligned.
+ */
+JETQ_API jetq_status jetq_selftest_bounded_wait(uint64_t limit_ns, int64_t *elapsed_ns, void *stream);
+
 /* ======================================================================== */
 /* Layouts                                                                  */
 /* ======================================================================== */

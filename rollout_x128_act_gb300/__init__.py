@@ -51,6 +51,7 @@ def lib() -> ctypes.CDLL:
             "jetq_status_string": (ctypes.c_char_p, [I32]),
             "jetq_version": (I32, []),
             "jetq_check_device_error": (I32, [P]),
+            "jetq_selftest_bounded_wait": (I32, [ctypes.c_uint64, P, P]),
             "jetq_colcopy_capacity": (I64, [I64, I32]),
             "jetq_mx_scale_bytes": (I64, [I64, I64]),
             "jetq_quant_act_1x128": (I32, [P, I64, I64, I64, P, P, P, P, I64, P, I32, P]),
@@ -98,6 +99,11 @@ def jetq_version() -> int:
 
 def jetq_check_device_error(stream=None) -> int:
     return int(lib().jetq_check_device_error(_s(stream)))
+
+
+def jetq_selftest_bounded_wait(limit_ns: int, elapsed_ns, stream=None) -> int:
+    """Launch the bounded-wait diagnostic; elapsed_ns: int64 CUDA tensor of 2."""
+    return int(lib().jetq_selftest_bounded_wait(int(limit_ns), _p(elapsed_ns), _s(stream)))
 
 
 def jetq_colcopy_capacity(n: int, nseg: int = 1) -> int:

@@ -123,6 +123,18 @@ jetq_status jetq_check_device_error(void *stream)
     return word ? JETQ_ERR_TIMEOUT : JETQ_OK;
 }
 
+jetq_status jetq_selftest_bounded_wait(uint64_t limit_ns, int64_t *elapsed_ns, void *stream)
+{
+    JQ_REQUIRE(limit_ns >= 1000000ull && limit_ns <= 1000000000ull, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(elapsed_ns != nullptr, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(reinterpret_cast<uintptr_t>(elapsed_ns) % 8 == 0, JETQ_ERR_MISALIGNED);
+    const jetq_status a = check_arch();
+    if (a != JETQ_OK)
+        return a;
+    return from_cuda(launch_selftest_wait(limit_ns, reinterpret_cast<long long *>(elapsed_ns),
+                                          static_cast<cudaStream_t>(stream)));
+}
+
 jetq_status jetq_quant_act_1x128(const uint16_t *x, int64_t n, int64_t c, int64_t ldx, uint8_t *q_row, float *s_row,
                                  uint8_t *q_col, float *s_col, int64_t ldq_col, const int64_t *seg_offsets, int nseg,
                                  void *stream)

@@ -472,6 +472,27 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     }
 }
 
+// Two waiters on mbarriers nothing completes (see jetq_selftest_bounded_wait).
+__global__ void __launch_bounds__(64, 1) k_selftest_wait(unsigned long long limit_ns, long long *elapsed_ns)
+{
+    __shared__ __align__(8) uint64_t bars[2];
+    __shared__ int abort_word;
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_addr(&bars[0]), 1);
+        ptx::mbar_init(ptx::smem_addr(&bars[1]), 1);
+        abort_word = 0;
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 || threadIdx.x == 32) {
+        const int w = threadIdx.x >> 5;
+        const uint64_t t0 = ptx::globaltimer();
+        ptx::mbar_wait(ptx::smem_addr(&bars[w]), 0u, &abort_word, &g_gemm_error, kErrTimeout,
+                       w == 0 ? limit_ns : 8ull * limit_ns, w == 1);
+        elapsed_ns[w] = (long long)(ptx::globaltimer() - t0);
+    }
+}
+
 using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
                                    const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
                                    CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
@@ -623,6 +644,12 @@ cudaError_t launch_gemm_block128(const GemmProblem &g, GemmShape shape, cudaStre
     if (g.M <= 64)
         return run<32, 4, 4, 8, false, 8192, 4, 8>(g, st);
     return run<32, 4, 8, 8, false, 16384, 1, 8>(g, st);
+}
+
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, long long *elapsed_ns, cudaStream_t st)
+{
+    k_selftest_wait<<<1, 64, 0, st>>>(limit_ns, elapsed_ns);
+    return cudaGetLastError();
 }
 
 cudaError_t gemm_read_and_clear_error(cudaStream_t st, unsigned *out)

@@ -103,6 +103,10 @@ struct MxGemmProblem {
 cudaError_t launch_gemm_mx(const MxGemmProblem &p, cudaStream_t st);
 cudaError_t gemm_mx_read_and_clear_error(cudaStream_t st, unsigned *out);
 
+// One CTA whose two waiters time out on mbarriers nothing completes (the
+// bounded-wait diagnostic); records the timeout in the 128-block error word.
+cudaError_t launch_selftest_wait(unsigned long long limit_ns, long long *elapsed_ns, cudaStream_t st);
+
 // Decode-shaped 128-block FProp/DGrad with the operands swapped (weight rows
 // as the MMA's M, tokens as its N): dense, B-block scales, 1 <= M <= 64
 // tokens, N a multiple of 128 with at least kDecodeSwappedMinTiles 128-row

@@ -76,5 +76,10 @@ def test_validation_happens_before_cuda(L):
     # WGrad: K not a multiple of 128, ldk smaller than K
     assert L.jetq_gemm_wgrad(0, fake, fake, fake, fake, 200, 256, 128, 128, fake, 128, 0, None) == 2
     assert L.jetq_gemm_wgrad(0, fake, fake, fake, fake, 256, 128, 128, 128, fake, 128, 0, None) == 2
+    # bounded-wait diagnostic: limit outside [1 ms, 1 s], null or misaligned output
+    assert L.jetq_selftest_bounded_wait(ctypes.c_uint64(999_999), fake, None) == 1
+    assert L.jetq_selftest_bounded_wait(ctypes.c_uint64(2_000_000_000), fake, None) == 1
+    assert L.jetq_selftest_bounded_wait(ctypes.c_uint64(50_000_000), None, None) == 1
+    assert L.jetq_selftest_bounded_wait(ctypes.c_uint64(50_000_000), P(4100), None) == 3
     # MX: columns not a multiple of 128
     assert L.jetq_quant_mx32(fake, 4, 96, 96, fake, fake, None, None, 0, None, 0, None) == 2
