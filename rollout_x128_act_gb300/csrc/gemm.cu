@@ -369,6 +369,11 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                     }
                 }
                 ptx::tc_fence_before();
+                // the column-scale slot was read through the generic proxy and the next
+                // bulk copy into it writes through the async proxy: every reader orders
+                // its reads before that write with a proxy fence ahead of the release
+                if (PER_ROW_B)
+                    ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
                     if (j == KBP - 1)
