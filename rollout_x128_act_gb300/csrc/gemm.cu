@@ -572,6 +572,10 @@ cudaError_t run(const GemmProblem &g, cudaStream_t st)
             return e;
         configured_device = dev;
     }
+    // an epilogue thread stores kCols consecutive columns once the first is in
+    // range, so N must be a multiple of that slice
+    if (g.N % C::kCols != 0)
+        return cudaErrorInvalidValue;
     // B rows the map covers: one weight, or every expert's stacked
     const int64_t b_rows = g.group == GroupKind::Rows ? g.N * g.num_experts : g.N;
     // single-K-block boxes are never taller than the tensor: rows of a stage
@@ -633,10 +637,11 @@ cudaError_t launch_gemm_block128(const GemmProblem &g, GemmShape shape, cudaStre
 {
     if (g.M == 0)
         return cudaSuccess;
-    // per-row B scales come with WGrad, which always runs the training shape;
-    // its longer epilogue profits from row scales two K-blocks ahead
+    // per-row B scales come with WGrad, which always runs the training shape:
+    // 192-column tiles folded by three epilogue warpgroups (64 columns a
+    // thread, no register spills) and row scales two K-blocks ahead
     if (g.bscale == BScale::PerRow)
-        return run<256, 8, 4, 2, true, 16384, 1, 2>(g, st);
+        return run<192, 12, 4, 2, true, 16384, 1, 2>(g, st);
     if (shape == GemmShape::Train)
         return run<256, 8, 4, 2, false>(g, st);
     if (gemm_decode_swapped_applies(g))
