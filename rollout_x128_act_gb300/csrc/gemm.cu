@@ -646,6 +646,10 @@ cudaError_t launch_gemm_block128(const GemmProblem &g, GemmShape shape, cudaStre
         return run<256, 8, 4, 2, false>(g, st);
     if (gemm_decode_swapped_applies(g))
         return launch_gemm_decode_swapped(g, st);
+    // past the swapped kernel's 64 tokens the training tiles stream the weight
+    // faster once they cover 32 CTAs (same per-element arithmetic either way)
+    if (g.group == GroupKind::None && ((g.M + 127) / 128) * ((g.N + 255) / 256) >= 32)
+        return run<256, 8, 4, 2, false>(g, st);
     // decode: 32 weight rows per tile, four K-blocks per copy, scales eight
     // K-blocks ahead; a batch of up to 32 (64) tokens packs its A K-blocks
     // 4 KB (8 KB) apart

@@ -156,7 +156,7 @@ def test_rollout_fprop_equals_training_fprop_bitwise():
     qw, sw, _, _ = jq.quant_weight(to_dev_bf16(w), transposed=False)
     ax = jq.quant_act(tx, col=False)
     y_train = jq.fprop(ax["q_row"], ax["s_row"], qw, sw, path=jq.PATH_TRAIN)
-    for n in (1, 8, 20, 33, 64, 256):
+    for n in (1, 8, 20, 33, 64, 96, 128, 256):
         a = jq.quant_act(tx[:n], col=False)  # rollout quantizes its own batch
         assert torch.equal(a["q_row"], ax["q_row"][:n])
         y_dec = jq.fprop(a["q_row"], a["s_row"], qw, sw, path=jq.PATH_DECODE)
