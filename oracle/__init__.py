@@ -61,11 +61,13 @@ def _load():
         lib.jo_quant_rowgroups.argtypes = [P, I, I, I, I, P, I, P]
         lib.jo_quant_colgroups.argtypes = [P, I, I, I, I, P, ctypes.c_int, P, I, P]
         lib.jo_quant_blocks.argtypes = [P, I, I, I, I, P, P, P, P]
+        lib.jo_quant_blocks_pow2.argtypes = [P, I, I, I, I, P, P, P, P]
         lib.jo_quant_mx_rows.argtypes = [P, I, I, I, I, P, I, P]
         lib.jo_quant_mx_cols.argtypes = [P, I, I, I, I, I, P, ctypes.c_int, P, I, P]
         lib.jo_dequant_rowgroups.argtypes = [P, I, I, I, I, P, P]
         lib.jo_dequant_colgroups.argtypes = [P, I, P, I, I, I, P, ctypes.c_int, P]
         lib.jo_dequant_blocks.argtypes = [P, I, I, I, P, P]
+        lib.jo_dequant_blocks_pow2.argtypes = [P, I, I, I, P, P]
         lib.jo_dequant_mx_rows.argtypes = [P, I, I, I, I, P, P]
         lib.jo_dequant_mx_cols.argtypes = [P, I, P, I, I, I, I, I, P, ctypes.c_int, P]
         for f in ("jo_fprop", "jo_dgrad", "jo_wgrad"):
@@ -169,6 +171,21 @@ def quant_blocks(w, bs: int = 128):
     return q, s, qT, sT
 
 
+def quant_blocks_pow2(w, bs: int = 128):
+    """Power-of-two bs x bs blocks: returns (q [D x C], e8 [D/bs x C/bs], qT [C x D], e8T [C/bs x D/bs]);
+    e8 holds the E8M0 byte e + 127 of each block's scale 2^e."""
+    w = _c(w, np.uint16)
+    D, C = w.shape
+    if D % bs or C % bs:
+        raise ValueError("both dimensions must be multiples of the block size")
+    q = np.empty((D, C), np.uint8)
+    e8 = np.empty((D // bs, C // bs), np.uint8)
+    qT = np.empty((C, D), np.uint8)
+    e8T = np.empty((C // bs, D // bs), np.uint8)
+    _load().jo_quant_blocks_pow2(_p(w), D, C, C, bs, _p(q), _p(e8), _p(qT), _p(e8T))
+    return q, e8, qT, e8T
+
+
 def quant_mx_rows(x, bs: int = 32):
     """MX 1 x bs blocks along each row: returns (q [R x C] u8, e8 [R x C/bs] u8)."""
     x = _c(x, np.uint16)
@@ -224,6 +241,15 @@ def dequant_blocks(q, s, bs: int = 128):
     D, C = q.shape
     out = np.empty((D, C), np.float64)
     _load().jo_dequant_blocks(_p(q), D, C, bs, _p(s), _p(out))
+    return out
+
+
+def dequant_blocks_pow2(q, e8, bs: int = 128):
+    q = _c(q, np.uint8)
+    e8 = _c(e8, np.uint8)
+    D, C = q.shape
+    out = np.empty((D, C), np.float64)
+    _load().jo_dequant_blocks_pow2(_p(q), D, C, bs, _p(e8), _p(out))
     return out
 
 

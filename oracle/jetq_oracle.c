@@ -323,6 +323,46 @@ void jo_quant_mx_rows(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx
 }
 
 /*
+ * Power-of-two bs x bs weight blocks (the blockwise recipe with its FP32
+ * scales constrained to powers of two: [SK] "Deep dive: FP8 quantization with
+ * FP32 and power-of-two block scales"; the only block scaling Blackwell
+ * tensor cores take).  The exponent follows the rule above: per block e is
+ * the smallest integer with amax <= 448 * 2^e, the byte is e + 127 and
+ * q = E4M3(w * 2^-e).
+ *   w : bf16 [rows x cols] stride ldw ; q : [rows x cols] ; e8 : [rows/bs x cols/bs]
+ *   qT, e8T (optional): the transposed codes [cols x rows] and bytes [cols/bs x rows/bs]
+ */
+void jo_quant_blocks_pow2(const uint16_t *w, int64_t rows, int64_t cols, int64_t ldw, int64_t bs,
+                          uint8_t *q, uint8_t *e8, uint8_t *qT, uint8_t *e8T)
+{
+    int64_t bi, bj, i, j;
+    for (bi = 0; bi < rows / bs; ++bi) {
+        for (bj = 0; bj < cols / bs; ++bj) {
+            float amax = 0.0f;
+            int e;
+            for (i = 0; i < bs; ++i)
+                for (j = 0; j < bs; ++j) {
+                    float v = fabsf(bf16_value(w[(bi * bs + i) * ldw + bj * bs + j]));
+                    if (v > amax)
+                        amax = v;
+                }
+            e = jo_e8m0_exponent(amax);
+            e8[bi * (cols / bs) + bj] = (uint8_t)(e + 127);
+            if (e8T)
+                e8T[bj * (rows / bs) + bi] = (uint8_t)(e + 127);
+            for (i = 0; i < bs; ++i)
+                for (j = 0; j < bs; ++j) {
+                    int64_t r = bi * bs + i, c = bj * bs + j;
+                    uint8_t code = mx_value(bf16_value(w[r * ldw + c]), e, amax == 0.0f);
+                    q[r * cols + c] = code;
+                    if (qT)
+                        qT[c * rows + r] = code;
+                }
+        }
+    }
+}
+
+/*
  * Column-wise MX blocks of `bs` consecutive rows inside each segment, stored
  * transposed like jo_quant_colgroups; segments start at multiples of `seg_align`
  * (a multiple of bs) in the column copy.
@@ -408,6 +448,16 @@ void jo_dequant_blocks(const uint8_t *q, int64_t rows, int64_t cols, int64_t bs,
     for (r = 0; r < rows; ++r)
         for (c = 0; c < cols; ++c)
             out[r * cols + c] = jo_e4m3_decode(q[r * cols + c]) * (double)s[(r / bs) * (cols / bs) + c / bs];
+}
+
+/* power-of-two blocks: value = decode(q) * 2^(byte - 127) */
+void jo_dequant_blocks_pow2(const uint8_t *q, int64_t rows, int64_t cols, int64_t bs, const uint8_t *e8, double *out)
+{
+    int64_t r, c;
+    for (r = 0; r < rows; ++r)
+        for (c = 0; c < cols; ++c)
+            out[r * cols + c] =
+                jo_e4m3_decode(q[r * cols + c]) * ldexp(1.0, (int)e8[(r / bs) * (cols / bs) + c / bs] - 127);
 }
 
 void jo_dequant_mx_rows(const uint8_t *q, int64_t rows, int64_t cols, int64_t ldq, int64_t bs,

@@ -252,3 +252,60 @@ def test_mx_cols_is_rows_of_transpose_and_segments():
     deq = oracle.dequant_mx_cols(qc, e8c, 256, offsets=off)
     xf = bf16_f32(x).astype(np.float64)
     assert np.all(np.abs(deq - xf) <= 2.0 ** -4 * np.abs(xf) + 2.0 ** -9 * np.abs(xf).max())
+
+
+# ---------------------------------------------------------------- power-of-two blocks
+# The blockwise recipe with FP32 scales constrained to powers of two (SkyRL,
+# "Deep dive: FP8 quantization with FP32 and power-of-two block scales"): the
+# exponent rule is the MX one, applied to 1 x 128 groups (quant_mx_rows with
+# bs = 128) and to 128 x 128 weight blocks (quant_blocks_pow2).
+
+
+@pytest.mark.parametrize("kind", ["random", "boundary", "zeros", "maxes"])
+def test_pow2_rows_of_128_brute_force(kind):
+    R, C = 3, 256
+    if kind == "random":
+        x = _random_bf16((R, C), 21, 5.0)
+    elif kind == "boundary":
+        x = _boundary_bf16(R, C, 22, gs=128)
+    elif kind == "zeros":
+        x = np.zeros((R, C), np.uint16)
+    else:
+        x = np.full((R, C), 0x7F7F, np.uint16)
+        x[1::2] = 0xFF7F
+    q, e8 = oracle.quant_mx_rows(x, bs=128)
+    assert e8.shape == (R, 2)
+    for r in range(R):
+        for g in range(2):
+            bq, be = brute_mx_group(x[r, g * 128:(g + 1) * 128])
+            assert e8[r, g] == be and np.array_equal(q[r, g * 128:(g + 1) * 128], bq), (r, g)
+
+
+def test_pow2_blocks_brute_force_and_transpose():
+    # two 128 x 128 blocks per side, one all zero, one with an outlier block
+    w = synth.weight(256, 256, seed=23, stream="test")
+    w[128:, :128] = 0
+    w[:128, 128:] = synth.activation(128, 128, seed=23, stream="test")
+    q, e8, qT, e8T = oracle.quant_blocks_pow2(w)
+    assert np.array_equal(qT, q.T) and np.array_equal(e8T, e8.T)
+    for bi in range(2):
+        for bj in range(2):
+            blk = w[bi * 128:(bi + 1) * 128, bj * 128:(bj + 1) * 128]
+            bq, be = brute_mx_group(blk.reshape(-1))
+            assert e8[bi, bj] == be, (bi, bj)
+            assert np.array_equal(q[bi * 128:(bi + 1) * 128, bj * 128:(bj + 1) * 128], bq.reshape(128, 128))
+    assert e8[1, 0] == 127 and not q[128:, :128].any()  # zero block: scale 1, codes 0
+
+
+def test_pow2_blocks_exact_reconstruction_and_exponent_bracket():
+    rng = np.random.default_rng(24)
+    pos = e4m3_positive_values()
+    x = np.empty((256, 128))
+    for bi, k in enumerate((-20, 13)):
+        v = rng.choice(pos[pos <= 448], (128, 128)) * rng.choice([-1.0, 1.0], (128, 128))
+        v[5, 7] = 448.0  # block max exactly 448 * 2^k: exponent k, no round-up
+        x[bi * 128:(bi + 1) * 128] = v * 2.0 ** k
+    xb = _bits(x)
+    q, e8, _, _ = oracle.quant_blocks_pow2(xb)
+    assert list(e8[:, 0]) == [127 - 20, 127 + 13]
+    assert np.array_equal(oracle.dequant_blocks_pow2(q, e8), x)
