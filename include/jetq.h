@@ -60,8 +60,11 @@ typedef enum {
 } jetq_status;
 
 typedef enum {
-    JETQ_RECIPE_BLOCK128 = 0, /* 1x128 activation groups, 128x128 weight blocks, FP32 scales */
-    JETQ_RECIPE_MXFP8 = 1     /* 1x32 blocks, E8M0 power-of-two scales rounded up */
+    JETQ_RECIPE_BLOCK128 = 0,     /* 1x128 activation groups, 128x128 weight blocks, FP32 scales */
+    JETQ_RECIPE_MXFP8 = 1,        /* 1x32 blocks, E8M0 power-of-two scales rounded up */
+    JETQ_RECIPE_BLOCK128_POW2 = 2 /* 1x128 groups, 128x128 blocks, scales constrained to powers of
+                                     two (E8M0 atoms, each 32-element sub-block byte carrying its
+                                     group's exponent); runs the block-scaled MMA like MXFP8 */
 } jetq_recipe;
 
 typedef enum {
@@ -206,6 +209,28 @@ JETQ_API jetq_status jetq_quant_mx32(const uint16_t *x, int64_t rows, int64_t co
                             uint8_t *q_row, uint8_t *e8_row,
                             uint8_t *q_col, uint8_t *e8_col, int64_t ldq_col,
                             const int64_t *seg_offsets, int nseg, void *stream);
+
+/*
+ * 128-block recipe with power-of-two scales (SkyRL "Deep dive: FP8
+ * quantization with FP32 and power-of-two block scales": the blockwise
+ * recipe's FP32 scales constrained to powers of two, the only block scaling
+ * Blackwell tensor cores take).  Per 1x128 row group / 128x1 column group /
+ * 128x128 weight block: e = smallest integer with amax <= 448 * 2^e (the MX
+ * rule), q = E4M3(x * 2^-e).  Scales are written in the MX atom layout for
+ * the same (rows, K) as MXFP8 (jetq_mx_scale_bytes), the byte e + 127 repeated
+ * in the four 32-element sub-blocks of each group, so the GEMMs read them
+ * with JETQ_RECIPE_BLOCK128_POW2 (or MXFP8) unchanged.
+ *
+ * Activations: arguments and layouts as jetq_quant_mx32 (groups of 128).
+ * Weights: q [d x c] (dense), e8 atoms for (d, c); optional qT [c x d] and e8T
+ *          atoms for (c, d) (the DGrad operand), both or neither.
+ */
+JETQ_API jetq_status jetq_quant_act_1x128_pow2(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx,
+                                      uint8_t *q_row, uint8_t *e8_row,
+                                      uint8_t *q_col, uint8_t *e8_col, int64_t ldq_col,
+                                      const int64_t *seg_offsets, int nseg, void *stream);
+JETQ_API jetq_status jetq_quant_w_128x128_pow2(const uint16_t *w, int64_t d, int64_t c, int64_t ldw,
+                                      uint8_t *q, uint8_t *e8, uint8_t *qT, uint8_t *e8T, void *stream);
 
 /* ======================================================================== */
 /* GEMMs                                                                    */

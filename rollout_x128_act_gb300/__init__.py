@@ -22,7 +22,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "_build", "libjetq.so")
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED_SHAPE, ERR_MISALIGNED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(7)
-RECIPE_BLOCK128, RECIPE_MXFP8 = 0, 1
+RECIPE_BLOCK128, RECIPE_MXFP8, RECIPE_BLOCK128_POW2 = 0, 1, 2
 PATH_AUTO, PATH_TRAIN, PATH_DECODE = 0, 1, 2
 GEMM_FPROP, GEMM_DGRAD, GEMM_WGRAD = 0, 1, 2
 OUT_F32, OUT_BF16 = 0, 1
@@ -57,6 +57,8 @@ def lib() -> ctypes.CDLL:
             "jetq_quant_act_1x128": (I32, [P, I64, I64, I64, P, P, P, P, I64, P, I32, P]),
             "jetq_quant_w_128x128": (I32, [P, I64, I64, I64, P, P, P, P, P]),
             "jetq_quant_mx32": (I32, [P, I64, I64, I64, P, P, P, P, I64, P, I32, P]),
+            "jetq_quant_act_1x128_pow2": (I32, [P, I64, I64, I64, P, P, P, P, I64, P, I32, P]),
+            "jetq_quant_w_128x128_pow2": (I32, [P, I64, I64, I64, P, P, P, P, P]),
             "jetq_gemm_fprop": (I32, [I32, P, P, P, P, I64, I64, I64, P, I32, I64, I32, P]),
             "jetq_gemm_dgrad": (I32, [I32, P, P, P, P, I64, I64, I64, P, I32, I64, P]),
             "jetq_gemm_wgrad": (I32, [I32, P, P, P, P, I64, I64, I64, I64, P, I64, I32, P]),
@@ -132,6 +134,18 @@ def jetq_quant_mx32(x, q_row, e8_row, q_col, e8_col, ldq_col, seg_offsets=None, 
                                  ldq_col, _p(seg_offsets), nseg, _s(stream)), "jetq_quant_mx32")
 
 
+def jetq_quant_act_1x128_pow2(x, q_row, e8_row, q_col, e8_col, ldq_col, seg_offsets=None, nseg=0, stream=None):
+    r, c = x.shape
+    _check(lib().jetq_quant_act_1x128_pow2(_p(x), r, c, x.stride(0), _p(q_row), _p(e8_row), _p(q_col), _p(e8_col),
+                                           ldq_col, _p(seg_offsets), nseg, _s(stream)), "jetq_quant_act_1x128_pow2")
+
+
+def jetq_quant_w_128x128_pow2(w, q, e8, qT=None, e8T=None, stream=None):
+    d, c = w.shape
+    _check(lib().jetq_quant_w_128x128_pow2(_p(w), d, c, w.stride(0), _p(q), _p(e8), _p(qT), _p(e8T), _s(stream)),
+           "jetq_quant_w_128x128_pow2")
+
+
 def _out_dtype(t):
     return OUT_BF16 if t.dtype == torch.bfloat16 else OUT_F32
 
@@ -204,6 +218,36 @@ def quant_mx(x, row=True, col=True, seg_offsets=None, stream=None):
         out["e8_col"] = torch.zeros(jetq_mx_scale_bytes(c, cap), dtype=torch.uint8, device=dev)
     jetq_quant_mx32(x, out["q_row"], out["e8_row"], out["q_col"], out["e8_col"], cap, seg_offsets, nseg, stream)
     return out
+
+
+def quant_act_pow2(x, row=True, col=True, seg_offsets=None, stream=None):
+    """Power-of-two 1x128 / 128x1 copies: dict(q_row, e8_row, q_col, e8_col, ldq_col), MX atom layout."""
+    r, c = x.shape
+    dev = x.device
+    nseg = 0 if seg_offsets is None else seg_offsets.numel() - 1
+    cap = jetq_colcopy_capacity(r, max(nseg, 1))
+    out = dict(q_row=None, e8_row=None, q_col=None, e8_col=None, ldq_col=cap)
+    if row:
+        out["q_row"] = torch.empty((r, c), dtype=torch.uint8, device=dev)
+        out["e8_row"] = torch.zeros(jetq_mx_scale_bytes(r, c), dtype=torch.uint8, device=dev)
+    if col:
+        out["q_col"] = torch.empty((c, cap), dtype=torch.uint8, device=dev)
+        out["e8_col"] = torch.zeros(jetq_mx_scale_bytes(c, cap), dtype=torch.uint8, device=dev)
+    jetq_quant_act_1x128_pow2(x, out["q_row"], out["e8_row"], out["q_col"], out["e8_col"], cap, seg_offsets, nseg,
+                              stream)
+    return out
+
+
+def quant_weight_pow2(w, transposed=True, stream=None):
+    """Power-of-two 128x128 blocks: (q [d x c], e8 atoms (d, c), qT [c x d] | None, e8T atoms (c, d) | None)."""
+    d, c = w.shape
+    dev = w.device
+    q = torch.empty((d, c), dtype=torch.uint8, device=dev)
+    e8 = torch.zeros(jetq_mx_scale_bytes(d, c), dtype=torch.uint8, device=dev)
+    qT = torch.empty((c, d), dtype=torch.uint8, device=dev) if transposed else None
+    e8T = torch.zeros(jetq_mx_scale_bytes(c, d), dtype=torch.uint8, device=dev) if transposed else None
+    jetq_quant_w_128x128_pow2(w, q, e8, qT, e8T, stream)
+    return q, e8, qT, e8T
 
 
 def fprop(qx, sx, qw, sw, out_dtype=torch.float32, path=PATH_AUTO, recipe=RECIPE_BLOCK128, stream=None):

@@ -176,9 +176,12 @@ jetq_status jetq_quant_w_128x128(const uint16_t *w, int64_t d, int64_t c, int64_
     return from_cuda(launch_quant_weight(args, static_cast<cudaStream_t>(stream)));
 }
 
-jetq_status jetq_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q_row,
-                            uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, int64_t ldq_col,
-                            const int64_t *seg_offsets, int nseg, void *stream)
+namespace {
+
+// E8M0-scaled row and column copies with groups of `group` (32 or 128) elements
+jetq_status quant_e8m0_groups(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q_row,
+                              uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, int64_t ldq_col,
+                              const int64_t *seg_offsets, int nseg, int group, void *stream)
 {
     JQ_REQUIRE(rows >= 0 && cols > 0, JETQ_ERR_INVALID_ARG);
     JQ_REQUIRE((q_row == nullptr) == (e8_row == nullptr), JETQ_ERR_INVALID_ARG);
@@ -198,14 +201,49 @@ jetq_status jetq_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64
     if (a != JETQ_OK)
         return a;
     MxQuantArgs args{x, rows, cols, ldx, q_row, e8_row, q_col, e8_col, ldq_col, seg_offsets, nseg_eff};
-    return from_cuda(launch_quant_mx(args, static_cast<cudaStream_t>(stream)));
+    return from_cuda(launch_quant_mx(args, group, static_cast<cudaStream_t>(stream)));
+}
+
+} // namespace
+
+jetq_status jetq_quant_mx32(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q_row,
+                            uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, int64_t ldq_col,
+                            const int64_t *seg_offsets, int nseg, void *stream)
+{
+    return quant_e8m0_groups(x, rows, cols, ldx, q_row, e8_row, q_col, e8_col, ldq_col, seg_offsets, nseg, 32,
+                             stream);
+}
+
+jetq_status jetq_quant_act_1x128_pow2(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, uint8_t *q_row,
+                                      uint8_t *e8_row, uint8_t *q_col, uint8_t *e8_col, int64_t ldq_col,
+                                      const int64_t *seg_offsets, int nseg, void *stream)
+{
+    return quant_e8m0_groups(x, rows, cols, ldx, q_row, e8_row, q_col, e8_col, ldq_col, seg_offsets, nseg, 128,
+                             stream);
+}
+
+jetq_status jetq_quant_w_128x128_pow2(const uint16_t *w, int64_t d, int64_t c, int64_t ldw, uint8_t *q, uint8_t *e8,
+                                      uint8_t *qT, uint8_t *e8T, void *stream)
+{
+    JQ_REQUIRE(w != nullptr && q != nullptr && e8 != nullptr && d > 0 && c > 0, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE((qT == nullptr) == (e8T == nullptr), JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(d % 128 == 0 && c % 128 == 0 && ldw >= c, JETQ_ERR_UNSUPPORTED_SHAPE);
+    JQ_REQUIRE(aligned16(w) && ldw % 8 == 0 && aligned16(q) && aligned16(qT) && aligned16(e8) && aligned16(e8T),
+               JETQ_ERR_MISALIGNED);
+    const jetq_status a = check_arch();
+    if (a != JETQ_OK)
+        return a;
+    WeightPow2Args args{w, d, c, ldw, q, e8, qT, e8T};
+    return from_cuda(launch_quant_weight_pow2(args, static_cast<cudaStream_t>(stream)));
 }
 
 jetq_status jetq_gemm_fprop(jetq_recipe recipe, const uint8_t *qx, const void *sx, const uint8_t *qw, const void *sw,
                             int64_t n, int64_t d, int64_t c, void *y, jetq_out_dtype y_dtype, int64_t ldy,
                             jetq_path path, void *stream)
 {
-    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128 || recipe == JETQ_RECIPE_MXFP8, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128 || recipe == JETQ_RECIPE_MXFP8 ||
+                   recipe == JETQ_RECIPE_BLOCK128_POW2,
+               JETQ_ERR_INVALID_ARG);
     JQ_REQUIRE(path == JETQ_PATH_AUTO || path == JETQ_PATH_TRAIN || path == JETQ_PATH_DECODE, JETQ_ERR_INVALID_ARG);
     JQ_REQUIRE(n >= 0 && d > 0 && c > 0, JETQ_ERR_INVALID_ARG);
     JQ_REQUIRE(d % 128 == 0 && c % 128 == 0, JETQ_ERR_UNSUPPORTED_SHAPE);
@@ -218,7 +256,7 @@ jetq_status jetq_gemm_fprop(jetq_recipe recipe, const uint8_t *qx, const void *s
     JQ_REQUIRE(aligned16(qx) && aligned16(qw) && aligned16(sx) && aligned16(sw), JETQ_ERR_MISALIGNED);
     if ((st = check_arch()) != JETQ_OK)
         return st;
-    if (recipe == JETQ_RECIPE_MXFP8) {
+    if (recipe != JETQ_RECIPE_BLOCK128) { // E8M0 scale atoms: the block-scaled MMA
         MxGemmProblem m{qx, static_cast<const uint8_t *>(sx), qw, static_cast<const uint8_t *>(sw), n, d, c, c, c,
                         y, ldy, y_dtype, 0};
         return from_cuda(launch_gemm_mx(m, static_cast<cudaStream_t>(stream)));
@@ -234,7 +272,9 @@ jetq_status jetq_gemm_dgrad(jetq_recipe recipe, const uint8_t *qdy, const void *
                             const void *swt, int64_t n, int64_t d, int64_t c, void *dx, jetq_out_dtype dx_dtype,
                             int64_t lddx, void *stream)
 {
-    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128 || recipe == JETQ_RECIPE_MXFP8, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128 || recipe == JETQ_RECIPE_MXFP8 ||
+                   recipe == JETQ_RECIPE_BLOCK128_POW2,
+               JETQ_ERR_INVALID_ARG);
     JQ_REQUIRE(n >= 0 && d > 0 && c > 0, JETQ_ERR_INVALID_ARG);
     JQ_REQUIRE(d % 128 == 0 && c % 128 == 0, JETQ_ERR_UNSUPPORTED_SHAPE);
     jetq_status st = check_out(dx, dx_dtype, lddx, c);
@@ -246,7 +286,7 @@ jetq_status jetq_gemm_dgrad(jetq_recipe recipe, const uint8_t *qdy, const void *
     JQ_REQUIRE(aligned16(qdy) && aligned16(qwt) && aligned16(sdy) && aligned16(swt), JETQ_ERR_MISALIGNED);
     if ((st = check_arch()) != JETQ_OK)
         return st;
-    if (recipe == JETQ_RECIPE_MXFP8) {
+    if (recipe != JETQ_RECIPE_BLOCK128) { // E8M0 scale atoms: the block-scaled MMA
         MxGemmProblem m{qdy, static_cast<const uint8_t *>(sdy), qwt, static_cast<const uint8_t *>(swt), n, c, d, d, d,
                         dx, lddx, dx_dtype, 0};
         return from_cuda(launch_gemm_mx(m, static_cast<cudaStream_t>(stream)));
@@ -261,7 +301,9 @@ jetq_status jetq_gemm_wgrad(jetq_recipe recipe, const uint8_t *qdyc, const void 
                             const void *sxc, int64_t k, int64_t ldk, int64_t d, int64_t c, float *dw, int64_t lddw,
                             int accumulate, void *stream)
 {
-    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128 || recipe == JETQ_RECIPE_MXFP8, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128 || recipe == JETQ_RECIPE_MXFP8 ||
+                   recipe == JETQ_RECIPE_BLOCK128_POW2,
+               JETQ_ERR_INVALID_ARG);
     JQ_REQUIRE(k >= 0 && d > 0 && c > 0, JETQ_ERR_INVALID_ARG);
     JQ_REQUIRE(d % 128 == 0 && c % 128 == 0 && k % 128 == 0 && ldk >= k, JETQ_ERR_UNSUPPORTED_SHAPE);
     jetq_status st = check_out(dw, JETQ_OUT_F32, lddw, c);
@@ -278,7 +320,7 @@ jetq_status jetq_gemm_wgrad(jetq_recipe recipe, const uint8_t *qdyc, const void 
                JETQ_ERR_MISALIGNED);
     if ((st = check_arch()) != JETQ_OK)
         return st;
-    if (recipe == JETQ_RECIPE_MXFP8) {
+    if (recipe != JETQ_RECIPE_BLOCK128) { // E8M0 scale atoms: the block-scaled MMA
         MxGemmProblem m{qdyc, static_cast<const uint8_t *>(sdyc), qxc, static_cast<const uint8_t *>(sxc), d, c, k, ldk,
                         ldk, dw, lddw, JETQ_OUT_F32, accumulate ? 1 : 0};
         return from_cuda(launch_gemm_mx(m, static_cast<cudaStream_t>(stream)));
@@ -294,7 +336,9 @@ jetq_status jetq_gemm_grouped(jetq_gemm_kind kind, jetq_recipe recipe, const uin
                               int64_t ldo, int accumulate, void *stream)
 {
     JQ_REQUIRE(kind == JETQ_GEMM_FPROP || kind == JETQ_GEMM_DGRAD || kind == JETQ_GEMM_WGRAD, JETQ_ERR_INVALID_ARG);
-    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128 || recipe == JETQ_RECIPE_MXFP8, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128 || recipe == JETQ_RECIPE_MXFP8 ||
+                   recipe == JETQ_RECIPE_BLOCK128_POW2,
+               JETQ_ERR_INVALID_ARG);
     JQ_REQUIRE(m >= 0 && n > 0 && k >= 0 && seg_offsets != nullptr, JETQ_ERR_INVALID_ARG);
     JQ_REQUIRE(num_experts >= 1 && num_experts <= 256, JETQ_ERR_UNSUPPORTED_SHAPE);
     JQ_REQUIRE(n % 128 == 0 && k % 128 == 0 && ldk >= k, JETQ_ERR_UNSUPPORTED_SHAPE);
@@ -321,7 +365,7 @@ jetq_status jetq_gemm_grouped(jetq_gemm_kind kind, jetq_recipe recipe, const uin
     if ((st = check_arch()) != JETQ_OK)
         return st;
     const cudaStream_t cs = static_cast<cudaStream_t>(stream);
-    if (recipe == JETQ_RECIPE_MXFP8) {
+    if (recipe != JETQ_RECIPE_BLOCK128) { // E8M0 scale atoms: the block-scaled MMA
         MxGemmProblem mp{a, static_cast<const uint8_t *>(sa), b, static_cast<const uint8_t *>(sb), m, n, k, ldk, ldk,
                          out, ldo, wgrad ? JETQ_OUT_F32 : out_dtype, accumulate ? 1 : 0};
         mp.group = wgrad ? GroupKind::K : GroupKind::Rows;

@@ -45,7 +45,18 @@ struct MxQuantArgs {
 
 cudaError_t launch_quant_act(const ActQuantArgs &a, cudaStream_t st);
 cudaError_t launch_quant_weight(const WeightQuantArgs &a, cudaStream_t st);
-cudaError_t launch_quant_mx(const MxQuantArgs &a, cudaStream_t st);
+// group: 32 (MXFP8) or 128 (power-of-two 128-block recipe)
+cudaError_t launch_quant_mx(const MxQuantArgs &a, int group, cudaStream_t st);
+
+struct WeightPow2Args {
+    const uint16_t *w;
+    int64_t d, c, ldw;
+    uint8_t *q;
+    uint8_t *e8;  // MX scale atoms of W (rows d, K = c)
+    uint8_t *qT;  // optional
+    uint8_t *e8T; // MX scale atoms of W^T (rows c, K = d), with qT
+};
+cudaError_t launch_quant_weight_pow2(const WeightPow2Args &a, cudaStream_t st);
 
 // --------------------------------------------------------------------- GEMMs
 // One block-scaled GEMM problem: out[M x N] = A[M x K] * B[N x K]^T, both

@@ -544,8 +544,65 @@ __global__ void __launch_bounds__(kThreads, 2) k_quant_weight(WeightQuantArgs a)
     }
 }
 
-// MXFP8 quantizer: 1x32 row blocks and 32x1 column blocks, E8M0 scales.
-template <bool ROW, bool COL>
+// Power-of-two 128x128 weight blocks: one E8M0 exponent per block, written
+// into the MX scale atoms of W (rows D, K = C) and of W^T (rows C, K = D),
+// each 32-element sub-block byte carrying its block's exponent.
+__global__ void __launch_bounds__(kThreads, 2) k_quant_weight_pow2(WeightPow2Args a)
+{
+    __shared__ float red[8];
+    __shared__ __align__(16) uint8_t tileT[128 * 128];
+
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int rg = t >> 4, cc = t & 15;
+    const int64_t d0 = (int64_t)blockIdx.x * 128, c0 = (int64_t)blockIdx.y * 128;
+
+    float v[8][8];
+    load_block(a.w, a.ldw, d0, c0, 128, rg, cc, v);
+
+    float m = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        m = fmaxf(m, absmax8(v[i]));
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, d));
+    if (lane == 0)
+        red[warp] = m;
+    __syncthreads();
+    m = red[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w)
+        m = fmaxf(m, red[w]);
+    const int e = e8m0_exponent(m);
+    const float f = exp2_neg(e);
+    const uint32_t word = (uint32_t)(e + 127) * 0x01010101u;
+    if (t < 128)
+        *reinterpret_cast<uint32_t *>(a.e8 + mx_atom_offset(d0 + t, c0 >> 5, (a.d + 127) / 128)) = word;
+    else if (a.e8T)
+        *reinterpret_cast<uint32_t *>(a.e8T + mx_atom_offset(c0 + (t - 128), d0 >> 5, (a.c + 127) / 128)) = word;
+
+    uint2 rows[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        rows[i] = quant8_mx(v[i], f, m == 0.0f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        *reinterpret_cast<uint2 *>(a.q + (d0 + rg * 8 + i) * a.c + c0 + cc * 8) = rows[i];
+    if (a.qT) {
+        uint2 cols[8];
+        transpose8x8(rows, cols);
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            tileT_put(tileT, cc * 8 + j, rg, cols[j]);
+        __syncthreads();
+        store_tileT(tileT, a.qT, a.d, c0, d0);
+    }
+}
+
+// MX-style quantizer with E8M0 scales: 1xG row blocks and Gx1 column blocks,
+// G = 32 (MXFP8) or 128 (the 128-block recipe with power-of-two scales; each
+// 32-element sub-block byte of the scale atoms then carries its group's exponent).
+template <bool ROW, bool COL, int G>
 __global__ void __launch_bounds__(kThreads, 2) k_quant_mx(MxQuantArgs a)
 {
     __shared__ __align__(16) float red[8][128];
@@ -574,6 +631,10 @@ __global__ void __launch_bounds__(kThreads, 2) k_quant_mx(MxQuantArgs a)
             float m = absmax8(v[i]);
             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
             m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
+            if (G == 128) { // the 16 lanes of a half-warp span the tile's 128 columns
+                m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
+                m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
+            }
             const int e = e8m0_exponent(m);
             const uint2 codes = quant8_mx(v[i], exp2_neg(e), m == 0.0f);
             // the four 32-blocks of this row sit in lanes with cc = 0, 4, 8, 12 of the half-warp
@@ -609,14 +670,18 @@ __global__ void __launch_bounds__(kThreads, 2) k_quant_mx(MxQuantArgs a)
             *reinterpret_cast<float4 *>(&red[warp][cc * 8 + 4]) = make_float4(cm[4], cm[5], cm[6], cm[7]);
         }
         __syncthreads();
-        // 32-row block k = warp / 2 covers warps 2k and 2k+1
-        const int other = warp ^ 1;
-        const float4 p = *reinterpret_cast<const float4 *>(&red[other][cc * 8]);
-        const float4 q = *reinterpret_cast<const float4 *>(&red[other][cc * 8 + 4]);
-        cm[0] = fmaxf(cm[0], p.x); cm[1] = fmaxf(cm[1], p.y);
-        cm[2] = fmaxf(cm[2], p.z); cm[3] = fmaxf(cm[3], p.w);
-        cm[4] = fmaxf(cm[4], q.x); cm[5] = fmaxf(cm[5], q.y);
-        cm[6] = fmaxf(cm[6], q.z); cm[7] = fmaxf(cm[7], q.w);
+        // 32-row block k = warp / 2 covers warps 2k and 2k+1 (G = 128: all eight warps)
+#pragma unroll
+        for (int w = 0; w < 8; ++w) {
+            if (G == 128 ? w == warp : w != (warp ^ 1))
+                continue;
+            const float4 p = *reinterpret_cast<const float4 *>(&red[w][cc * 8]);
+            const float4 q = *reinterpret_cast<const float4 *>(&red[w][cc * 8 + 4]);
+            cm[0] = fmaxf(cm[0], p.x); cm[1] = fmaxf(cm[1], p.y);
+            cm[2] = fmaxf(cm[2], p.z); cm[3] = fmaxf(cm[3], p.w);
+            cm[4] = fmaxf(cm[4], q.x); cm[5] = fmaxf(cm[5], q.y);
+            cm[6] = fmaxf(cm[6], q.z); cm[7] = fmaxf(cm[7], q.w);
+        }
         const int k = warp >> 1;
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
@@ -667,17 +732,35 @@ cudaError_t launch_quant_weight(const WeightQuantArgs &a, cudaStream_t st)
     return cudaGetLastError();
 }
 
-cudaError_t launch_quant_mx(const MxQuantArgs &a, cudaStream_t st)
+cudaError_t launch_quant_mx(const MxQuantArgs &a, int group, cudaStream_t st)
 {
     if (a.rows == 0 || (!a.q_row && !a.q_col))
         return cudaSuccess;
+    if (group != 32 && group != 128)
+        return cudaErrorInvalidValue;
     dim3 grid((unsigned)groups_upper_bound(a.rows, a.seg, a.nseg), (unsigned)(a.cols / 128));
-    if (a.q_row && a.q_col)
-        k_quant_mx<true, true><<<grid, kThreads, 0, st>>>(a);
-    else if (a.q_row)
-        k_quant_mx<true, false><<<grid, kThreads, 0, st>>>(a);
-    else
-        k_quant_mx<false, true><<<grid, kThreads, 0, st>>>(a);
+    if (group == 32) {
+        if (a.q_row && a.q_col)
+            k_quant_mx<true, true, 32><<<grid, kThreads, 0, st>>>(a);
+        else if (a.q_row)
+            k_quant_mx<true, false, 32><<<grid, kThreads, 0, st>>>(a);
+        else
+            k_quant_mx<false, true, 32><<<grid, kThreads, 0, st>>>(a);
+    } else {
+        if (a.q_row && a.q_col)
+            k_quant_mx<true, true, 128><<<grid, kThreads, 0, st>>>(a);
+        else if (a.q_row)
+            k_quant_mx<true, false, 128><<<grid, kThreads, 0, st>>>(a);
+        else
+            k_quant_mx<false, true, 128><<<grid, kThreads, 0, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_weight_pow2(const WeightPow2Args &a, cudaStream_t st)
+{
+    dim3 grid((unsigned)(a.d / 128), (unsigned)(a.c / 128));
+    k_quant_weight_pow2<<<grid, kThreads, 0, st>>>(a);
     return cudaGetLastError();
 }
 
