@@ -363,6 +363,58 @@ def measure_mxfp8(dev):
     return res
 
 
+def measure_pow2(dev):
+    """The dense-8B training step in the 128-block recipe with power-of-two scales
+    (E8M0 atoms, block-scaled MMA): 3 weight + 5 activation/gradient quantizations
+    and the 9 GEMMs, timed as one step, plus the gate-shape GEMMs alone."""
+    import torch
+
+    import rollout_x128_act_gb300 as jq
+
+    act, weight, grad = _dev_inputs(dev, 10)
+    x, h = act(N_TOK, C), act(N_TOK, D)
+    ws = {"gate": weight(D, C), "up": weight(D, C), "down": weight(C, D)}
+    dys = {"gate": grad(N_TOK, D), "up": grad(N_TOK, D), "down": grad(N_TOK, C)}
+    R = jq.RECIPE_BLOCK128_POW2
+    bf = torch.bfloat16
+    y = {"gate": torch.empty((N_TOK, D), dtype=bf, device=dev), "up": torch.empty((N_TOK, D), dtype=bf, device=dev),
+         "down": torch.empty((N_TOK, C), dtype=bf, device=dev)}
+    dx = {"gate": torch.empty((N_TOK, C), dtype=bf, device=dev), "up": torch.empty((N_TOK, C), dtype=bf, device=dev),
+          "down": torch.empty((N_TOK, D), dtype=bf, device=dev)}
+    dw = {g: torch.empty(tuple(ws[g].shape), dtype=torch.float32, device=dev) for g in ws}
+
+    def step():
+        qw = {g: jq.quant_weight_pow2(ws[g]) for g in ws}
+        ax, ah = jq.quant_act_pow2(x), jq.quant_act_pow2(h)
+        a_in = {"gate": ax, "up": ax, "down": ah}
+        for g in ("gate", "up", "down"):
+            a, (q, e, _, _) = a_in[g], qw[g]
+            jq.jetq_gemm_fprop(R, a["q_row"], a["e8_row"], q, e, N_TOK, q.shape[0], q.shape[1], y[g], jq.PATH_TRAIN)
+        ady = {g: jq.quant_act_pow2(dys[g]) for g in dys}
+        for g in ("gate", "up", "down"):
+            a, (_, _, qT, eT) = ady[g], qw[g]
+            jq.jetq_gemm_dgrad(R, a["q_row"], a["e8_row"], qT, eT, N_TOK, qT.shape[1], qT.shape[0], dx[g])
+        for g in ("gate", "up", "down"):
+            a, xa = ady[g], a_in[g]
+            jq.jetq_gemm_wgrad(R, a["q_col"], a["e8_col"], xa["q_col"], xa["e8_col"], N_TOK, a["ldq_col"],
+                               a["q_col"].shape[0], xa["q_col"].shape[0], dw[g])
+
+    ms_step = _time(step, 10)
+    gx, gdy = jq.quant_act_pow2(x), jq.quant_act_pow2(dys["gate"])
+    q, e, qT, eT = jq.quant_weight_pow2(ws["gate"])
+    t = {
+        "fprop": _time(lambda: jq.jetq_gemm_fprop(R, gx["q_row"], gx["e8_row"], q, e, N_TOK, D, C, y["gate"],
+                                                  jq.PATH_TRAIN), 10),
+        "dgrad": _time(lambda: jq.jetq_gemm_dgrad(R, gdy["q_row"], gdy["e8_row"], qT, eT, N_TOK, D, C, dx["gate"]),
+                       10),
+        "wgrad": _time(lambda: jq.jetq_gemm_wgrad(R, gdy["q_col"], gdy["e8_col"], gx["q_col"], gx["e8_col"], N_TOK,
+                                                  gx["ldq_col"], D, C, dw["gate"]), 10),
+    }
+    res = {"step_ms": round(ms_step, 4), "step_tflops": round(9 * GEMM_FLOP / (ms_step * 1e-3) / 1e12, 1)}
+    res.update({k: {"ms": round(v, 4), "tflops": round(GEMM_FLOP / (v * 1e-3) / 1e12, 1)} for k, v in t.items()})
+    return res
+
+
 def measure_moe(dev):
     """MoE grouped GEMMs, 30B-A3B shapes: 128 experts, 16384 tokens top-8 with
     Zipf(1.2) load (131072 routed rows), hidden 2048, expert intermediate 768
@@ -585,6 +637,7 @@ def run_ours(args):
             peaks_now = _peaks()
             line["decode"] = measure_decode(dev, peaks_now)
             line["mxfp8"] = measure_mxfp8(dev)
+            line["block128_pow2"] = measure_pow2(dev)
             line["moe"] = measure_moe(dev)
             if step_error():
                 raise RuntimeError("device error word set during the secondary measurements")
