@@ -62,6 +62,9 @@ def _load():
         lib.jo_quant_colgroups.argtypes = [P, I, I, I, I, P, ctypes.c_int, P, I, P]
         lib.jo_quant_blocks.argtypes = [P, I, I, I, I, P, P, P, P]
         lib.jo_quant_blocks_pow2.argtypes = [P, I, I, I, I, P, P, P, P]
+        lib.jo_requant_colgroups.argtypes = [P, P, I, I, I, P, ctypes.c_int, P, I, P]
+        lib.jo_dequant_rowgroups_bf16.argtypes = [P, I, I, I, P, P]
+        lib.jo_dequant_blocks_bf16.argtypes = [P, I, I, I, P, P]
         lib.jo_quant_mx_rows.argtypes = [P, I, I, I, I, P, I, P]
         lib.jo_quant_mx_cols.argtypes = [P, I, I, I, I, I, P, ctypes.c_int, P, I, P]
         lib.jo_dequant_rowgroups.argtypes = [P, I, I, I, I, P, P]
@@ -169,6 +172,41 @@ def quant_blocks(w, bs: int = 128):
     sT = np.empty((C // bs, D // bs), np.float32)
     _load().jo_quant_blocks(_p(w), D, C, C, bs, _p(q), _p(s), _p(qT), _p(sT))
     return q, s, qT, sT
+
+
+def requant_colgroups(q_row, s_row, offsets=None, gs: int = 128):
+    """Column copy re-quantized from a row copy (q_row [R x C], s_row [C/gs x R]):
+    v = fl32(decode(q) * S_row), then gs x 1 groups as quant_colgroups.
+    Returns (qc [C x P], sc [P/gs x C])."""
+    q_row = _c(q_row, np.uint8)
+    s_row = _c(s_row, np.float32)
+    R, C = q_row.shape
+    off = _offsets(offsets, R)
+    P = colcopy_length(off, R, gs)
+    qc = np.zeros((C, P), np.uint8)
+    sc = np.zeros((P // gs, C), np.float32)
+    _load().jo_requant_colgroups(_p(q_row), _p(s_row), R, C, gs, _p(off), len(off) - 1, _p(qc), P, _p(sc))
+    return qc, sc
+
+
+def dequant_rowgroups_bf16(q, s, gs: int = 128):
+    """BF16 bit patterns of decode(q) * S for a row copy (q [R x C], s [C/gs x R]), rounded once."""
+    q = _c(q, np.uint8)
+    s = _c(s, np.float32)
+    R, C = q.shape
+    out = np.empty((R, C), np.uint16)
+    _load().jo_dequant_rowgroups_bf16(_p(q), R, C, gs, _p(s), _p(out))
+    return out
+
+
+def dequant_blocks_bf16(q, s, bs: int = 128):
+    """BF16 bit patterns of decode(q) * S for bs x bs blocks (s [D/bs x C/bs]), rounded once."""
+    q = _c(q, np.uint8)
+    s = _c(s, np.float32)
+    D, C = q.shape
+    out = np.empty((D, C), np.uint16)
+    _load().jo_dequant_blocks_bf16(_p(q), D, C, bs, _p(s), _p(out))
+    return out
 
 
 def quant_blocks_pow2(w, bs: int = 128):

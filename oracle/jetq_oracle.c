@@ -223,6 +223,95 @@ void jo_quant_colgroups(const uint16_t *x, int64_t rows, int64_t cols, int64_t l
 }
 
 /*
+ * Column copy re-quantized from the FP8 row copy ([JR] requantize_for_dgrad:
+ * the 1x128 copy is taken back through dequantization and quantized again
+ * along the token dimension; [MB] calls this the DeepSeek-V3 style).  Every
+ * value is first rebuilt in binary32,
+ *     v = fl32(decode(q_row[r, k]) * S_row[k/gs, r]),
+ * then quantized exactly as jo_quant_colgroups quantizes BF16 input
+ * (segments start on multiples of gs, gs x 1 groups, padding codes 0).
+ *   q_row : [rows x cols] ; s_row : [cols/gs x rows]
+ */
+static float requant_value(const uint8_t *q_row, const float *s_row, int64_t rows, int64_t cols, int64_t gs,
+                           int64_t r, int64_t c)
+{
+    return (float)jo_e4m3_decode(q_row[r * cols + c]) * s_row[(c / gs) * rows + r];
+}
+
+void jo_requant_colgroups(const uint8_t *q_row, const float *s_row, int64_t rows, int64_t cols, int64_t gs,
+                          const int64_t *off, int nseg, uint8_t *qc, int64_t ldqc, float *sc)
+{
+    int64_t *pad = (int64_t *)malloc(sizeof(int64_t) * (size_t)(nseg + 1));
+    int e;
+    padded_starts(off, nseg, gs, pad);
+    for (e = 0; e < nseg; ++e) {
+        int64_t n_e = off[e + 1] - off[e];
+        int64_t t, c, i;
+        for (t = 0; t * gs < n_e; ++t) {
+            int64_t r0 = off[e] + t * gs;
+            int64_t valid = (n_e - t * gs < gs) ? n_e - t * gs : gs;
+            int64_t col0 = pad[e] + t * gs;
+            for (c = 0; c < cols; ++c) {
+                float amax = 0.0f, s;
+                for (i = 0; i < valid; ++i) {
+                    float v = fabsf(requant_value(q_row, s_row, rows, cols, gs, r0 + i, c));
+                    if (v > amax)
+                        amax = v;
+                }
+                s = scale_of(amax);
+                sc[(col0 / gs) * cols + c] = s;
+                for (i = 0; i < gs; ++i)
+                    qc[c * ldqc + col0 + i] =
+                        (i < valid) ? quant_value(requant_value(q_row, s_row, rows, cols, gs, r0 + i, c), s) : 0x00;
+            }
+        }
+    }
+    free(pad);
+}
+
+/*
+ * BF16 round-to-nearest-even of a binary64 value (used on exact products:
+ * a 4-bit E4M3 significand times a 24-bit scale is exact in binary64, so the
+ * dequantized BF16 value is rounded once).  bf16 keeps 8 significant bits;
+ * below 2^-126 the quantum stays 2^-133 (subnormals).
+ */
+static uint16_t bf16_rne(double v)
+{
+    double a = fabs(v), quantum, m;
+    float f;
+    uint32_t u;
+    int k;
+    if (a == 0.0)
+        return signbit(v) ? 0x8000u : 0u;
+    (void)frexp(a, &k); /* a = f * 2^k, f in [0.5, 1): leading bit 2^(k-1) */
+    quantum = ldexp(1.0, (k - 1 < -126 ? -126 : k - 1) - 7);
+    m = nearbyint(a / quantum); /* a / quantum is exact; default mode rounds half to even */
+    f = (float)(m * quantum);   /* exactly a bf16 value */
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)((u >> 16) | (signbit(v) ? 0x8000u : 0u));
+}
+
+/* Dequantization to BF16 of a row-group copy (gs groups along each row) or of
+ * bs x bs blocks: out = BF16(decode(q) * S), S from the copy's scale layout. */
+void jo_dequant_rowgroups_bf16(const uint8_t *q, int64_t rows, int64_t cols, int64_t gs, const float *s,
+                               uint16_t *out)
+{
+    int64_t r, c;
+    for (r = 0; r < rows; ++r)
+        for (c = 0; c < cols; ++c)
+            out[r * cols + c] = bf16_rne(jo_e4m3_decode(q[r * cols + c]) * (double)s[(c / gs) * rows + r]);
+}
+
+void jo_dequant_blocks_bf16(const uint8_t *q, int64_t rows, int64_t cols, int64_t bs, const float *s, uint16_t *out)
+{
+    int64_t r, c;
+    for (r = 0; r < rows; ++r)
+        for (c = 0; c < cols; ++c)
+            out[r * cols + c] =
+                bf16_rne(jo_e4m3_decode(q[r * cols + c]) * (double)s[(r / bs) * (cols / bs) + c / bs]);
+}
+
+/*
  * Square blocks of bs x bs ([JR] 128x128 per-block weight quantization,
  * S_W(i,j) = max|W_tile(i,j)| / 448, W^ = round(W / S_W)).
  *   w  : bf16 [rows x cols], row stride ldw

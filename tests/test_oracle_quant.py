@@ -309,3 +309,98 @@ def test_pow2_blocks_exact_reconstruction_and_exponent_bracket():
     q, e8, _, _ = oracle.quant_blocks_pow2(xb)
     assert list(e8[:, 0]) == [127 - 20, 127 + 13]
     assert np.array_equal(oracle.dequant_blocks_pow2(q, e8), x)
+
+
+# ---------------------------------------------------------------- re-quantized column copy, BF16 dequantizer
+
+def _decode_f32(codes):
+    """E4M3 code -> value from the format table (brute helper), as float32."""
+    pos = e4m3_positive_values()
+    c = np.asarray(codes, np.uint8)
+    v = pos[np.minimum(c & 0x7F, 0x7E)]
+    return np.where(c & 0x80, -v, v).astype(np.float32)
+
+
+def test_requant_colgroups_brute_force():
+    x = synth.activation(300, 256, seed=41, stream="test")
+    q, s = oracle.quant_rowgroups(x)
+    off = [0, 77, 77, 300]
+    qc, sc = oracle.requant_colgroups(q, s, offsets=off)
+    assert qc.shape == (256, 128 + 256)
+    for (lo, hi, p0) in ((0, 77, 0), (77, 205, 128), (205, 300, 256)):
+        for c in (0, 1, 127, 128, 255):
+            v = _decode_f32(q[lo:hi, c]) * s[c // 128, lo:hi]  # numpy float32 product: IEEE binary32
+            a = np.float32(np.max(np.abs(v)))
+            S = np.float32(a / np.float32(448.0))
+            assert sc[p0 // 128, c] == S
+            assert np.array_equal(qc[c, p0:p0 + (hi - lo)], brute_encode(v / S)), (lo, c)
+            assert not qc[c, p0 + (hi - lo):p0 + 128].any()
+
+
+def test_requant_of_exactly_representable_copy_is_the_direct_column_copy():
+    # every 1x128 group holds E4M3 grid values times 2^k with its maximum at 448 * 2^k,
+    # so the row copy dequantizes back to x exactly and the re-quantized column copy
+    # must equal the column copy taken from x directly
+    rng = np.random.default_rng(42)
+    pos = e4m3_positive_values()
+    R, C = 256, 256
+    x = np.empty((R, C))
+    for r in range(R):
+        for g in range(2):
+            v = rng.choice(pos, 128) * rng.choice([-1.0, 1.0], 128)
+            v[rng.integers(128)] = 448.0
+            x[r, g * 128:(g + 1) * 128] = v * 2.0 ** int(rng.integers(-12, 12))
+    xb = _bits(x)
+    q, s = oracle.quant_rowgroups(xb)
+    assert np.array_equal(oracle.dequant_rowgroups(q, s), x)
+    qc, sc = oracle.requant_colgroups(q, s)
+    qd, sd = oracle.quant_colgroups(xb)
+    assert np.array_equal(qc, qd) and np.array_equal(sc, sd)
+
+
+def _bf16_rne_exact(v):
+    """BF16 RNE by exact rational arithmetic (independent of the C oracle)."""
+    from fractions import Fraction
+    f = Fraction(v)
+    if f == 0:
+        return 0x8000 if np.signbit(v) else 0
+    a = abs(f)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    quantum = Fraction(2) ** (max(e, -126) - 7)
+    m = a / quantum
+    n = m.numerator // m.denominator
+    rem = m - n
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and n % 2 == 1):
+        n += 1
+    val = float(n * quantum)
+    bits = int(np.array([val], np.float32).view(np.uint32)[0]) >> 16
+    return bits | (0x8000 if f < 0 else 0)
+
+
+def test_dequant_bf16_single_rounding():
+    x = synth.activation(64, 256, seed=43, stream="test")
+    q, s = oracle.quant_rowgroups(x)
+    # scales with full 24-bit significands make the products need the single rounding
+    s = (s * np.float32(1.2345678)).astype(np.float32)
+    out = oracle.dequant_rowgroups_bf16(q, s)
+    rng = np.random.default_rng(44)
+    for r, c in zip(rng.integers(0, 64, 400), rng.integers(0, 256, 400)):
+        exact = float(_decode_f32(q[r, c])) * float(s[c // 128, r])
+        assert out[r, c] == _bf16_rne_exact(exact), (r, c)
+    # a product exactly on a bf16 midpoint rounds to even; just above it rounds up
+    qq = np.array([[0x38] * 128], np.uint8)  # decode = 1.0
+    tie = np.float32(1.0 + 2.0 ** -8)  # halfway between bf16 1.0 and 1.0078125
+    above = np.nextafter(tie, np.float32(2))
+    o = oracle.dequant_rowgroups_bf16(qq, np.array([[tie]], np.float32))
+    assert o[0, 0] == 0x3F80
+    o = oracle.dequant_rowgroups_bf16(qq, np.array([[above]], np.float32))
+    assert o[0, 0] == 0x3F81
+    wq, ws, _, _ = oracle.quant_blocks(synth.weight(256, 256, seed=45, stream="test"))
+    ob = oracle.dequant_blocks_bf16(wq, ws)
+    for r, c in zip(rng.integers(0, 256, 200), rng.integers(0, 256, 200)):
+        exact = float(_decode_f32(wq[r, c])) * float(ws[r // 128, c // 128])
+        assert ob[r, c] == _bf16_rne_exact(exact)
