@@ -232,6 +232,39 @@ JETQ_API jetq_status jetq_quant_act_1x128_pow2(const uint16_t *x, int64_t rows, 
 JETQ_API jetq_status jetq_quant_w_128x128_pow2(const uint16_t *w, int64_t d, int64_t c, int64_t ldw,
                                       uint8_t *q, uint8_t *e8, uint8_t *qT, uint8_t *e8T, void *stream);
 
+/*
+ * Column copy re-quantized from the FP8 row copy (JetRL's
+ * requantize_for_dgrad: the 1x128 copy goes back through dequantization and
+ * is quantized again along the token dimension; the Miles post calls this the
+ * DeepSeek-V3 style, as opposed to taking both copies from BF16).  Each value
+ * is rebuilt in binary32, v = fl32(decode(q_row[r,k]) * s_row[k/128, r]),
+ * then quantized as the column copy of jetq_quant_act_1x128 quantizes BF16:
+ * S = fl32(amax/448) per 128x1 group inside each segment, q = E4M3(fl32(v/S)).
+ *
+ *   q_row, s_row   the row copy of an [n x c] tensor (layouts above)
+ *   q_col, s_col   column copy [c x ldq_col] and its scales, exactly the
+ *                  layout jetq_quant_act_1x128 writes (same capacity rule)
+ *   seg_offsets, nseg  as for jetq_quant_act_1x128
+ */
+JETQ_API jetq_status jetq_requant_col_from_row(const uint8_t *q_row, const float *s_row, int64_t n, int64_t c,
+                                      uint8_t *q_col, float *s_col, int64_t ldq_col,
+                                      const int64_t *seg_offsets, int nseg, void *stream);
+
+/*
+ * Dequantization to BF16 (the dequant side of the pages' dequant-requant
+ * boundary and of a dequantized backward pass): out[r, k] = BF16 of the
+ * exact product decode(q[r, k]) * S, rounded once to nearest-even.
+ *   layout ROWGROUPS_1X128: s [cols/128 x rows] (a row copy's scales)
+ *   layout BLOCKS_128X128:  s [rows/128 x cols/128] (a weight's scales)
+ *   q [rows x cols] dense; out BF16 bit patterns [rows x ldo].
+ */
+typedef enum {
+    JETQ_SCALES_ROWGROUPS_1X128 = 0,
+    JETQ_SCALES_BLOCKS_128X128 = 1
+} jetq_scale_layout;
+JETQ_API jetq_status jetq_dequant_bf16(const uint8_t *q, const float *s, int64_t rows, int64_t cols,
+                              jetq_scale_layout layout, uint16_t *out, int64_t ldo, void *stream);
+
 /* ======================================================================== */
 /* GEMMs                                                                    */
 /* ======================================================================== */

@@ -59,6 +59,8 @@ def lib() -> ctypes.CDLL:
             "jetq_quant_mx32": (I32, [P, I64, I64, I64, P, P, P, P, I64, P, I32, P]),
             "jetq_quant_act_1x128_pow2": (I32, [P, I64, I64, I64, P, P, P, P, I64, P, I32, P]),
             "jetq_quant_w_128x128_pow2": (I32, [P, I64, I64, I64, P, P, P, P, P]),
+            "jetq_requant_col_from_row": (I32, [P, P, I64, I64, P, P, I64, P, I32, P]),
+            "jetq_dequant_bf16": (I32, [P, P, I64, I64, I32, P, I64, P]),
             "jetq_gemm_fprop": (I32, [I32, P, P, P, P, I64, I64, I64, P, I32, I64, I32, P]),
             "jetq_gemm_dgrad": (I32, [I32, P, P, P, P, I64, I64, I64, P, I32, I64, P]),
             "jetq_gemm_wgrad": (I32, [I32, P, P, P, P, I64, I64, I64, I64, P, I64, I32, P]),
@@ -144,6 +146,38 @@ def jetq_quant_w_128x128_pow2(w, q, e8, qT=None, e8T=None, stream=None):
     d, c = w.shape
     _check(lib().jetq_quant_w_128x128_pow2(_p(w), d, c, w.stride(0), _p(q), _p(e8), _p(qT), _p(e8T), _s(stream)),
            "jetq_quant_w_128x128_pow2")
+
+
+def jetq_requant_col_from_row(q_row, s_row, q_col, s_col, ldq_col, seg_offsets=None, nseg=0, stream=None):
+    n, c = q_row.shape
+    _check(lib().jetq_requant_col_from_row(_p(q_row), _p(s_row), n, c, _p(q_col), _p(s_col), ldq_col,
+                                           _p(seg_offsets), nseg, _s(stream)), "jetq_requant_col_from_row")
+
+
+SCALES_ROWGROUPS_1X128, SCALES_BLOCKS_128X128 = 0, 1
+
+
+def jetq_dequant_bf16(q, s, layout, out, stream=None):
+    rows, cols = q.shape
+    _check(lib().jetq_dequant_bf16(_p(q), _p(s), rows, cols, layout, _p(out), out.stride(0), _s(stream)),
+           "jetq_dequant_bf16")
+
+
+def requant_col(q_row, s_row, seg_offsets=None, stream=None):
+    """Column copy (q_col [c x cap], s_col [cap/128 x c], ldq_col) re-quantized from a row copy."""
+    n, c = q_row.shape
+    nseg = 0 if seg_offsets is None else seg_offsets.numel() - 1
+    cap = jetq_colcopy_capacity(n, max(nseg, 1))
+    q_col = torch.zeros((c, cap), dtype=torch.uint8, device=q_row.device)
+    s_col = torch.zeros((max(cap, 128) // 128, c), dtype=torch.float32, device=q_row.device)
+    jetq_requant_col_from_row(q_row, s_row, q_col, s_col, cap, seg_offsets, nseg, stream)
+    return dict(q_col=q_col, s_col=s_col, ldq_col=cap)
+
+
+def dequant_bf16(q, s, layout=SCALES_ROWGROUPS_1X128, stream=None):
+    out = torch.empty(q.shape, dtype=torch.bfloat16, device=q.device)
+    jetq_dequant_bf16(q, s, layout, out, stream)
+    return out
 
 
 def _out_dtype(t):

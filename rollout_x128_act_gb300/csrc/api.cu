@@ -237,6 +237,48 @@ jetq_status jetq_quant_w_128x128_pow2(const uint16_t *w, int64_t d, int64_t c, i
     return from_cuda(launch_quant_weight_pow2(args, static_cast<cudaStream_t>(stream)));
 }
 
+jetq_status jetq_requant_col_from_row(const uint8_t *q_row, const float *s_row, int64_t n, int64_t c, uint8_t *q_col,
+                                      float *s_col, int64_t ldq_col, const int64_t *seg_offsets, int nseg,
+                                      void *stream)
+{
+    JQ_REQUIRE(n >= 0 && c > 0, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(seg_offsets == nullptr || nseg >= 1, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(c % 128 == 0, JETQ_ERR_UNSUPPORTED_SHAPE);
+    const int nseg_eff = seg_offsets ? nseg : 1;
+    JQ_REQUIRE(ldq_col % 128 == 0 && ldq_col >= jetq_colcopy_capacity(n, nseg_eff), JETQ_ERR_UNSUPPORTED_SHAPE);
+    if (n == 0)
+        return JETQ_OK;
+    JQ_REQUIRE(q_row && s_row && q_col && s_col, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(aligned16(q_row) && aligned16(q_col) && (reinterpret_cast<uintptr_t>(s_row) & 3u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(s_col) & 3u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(seg_offsets) & 7u) == 0,
+               JETQ_ERR_MISALIGNED);
+    const jetq_status a = check_arch();
+    if (a != JETQ_OK)
+        return a;
+    RequantArgs args{q_row, s_row, n, c, q_col, s_col, ldq_col, seg_offsets, nseg_eff};
+    return from_cuda(launch_requant_col(args, static_cast<cudaStream_t>(stream)));
+}
+
+jetq_status jetq_dequant_bf16(const uint8_t *q, const float *s, int64_t rows, int64_t cols, jetq_scale_layout layout,
+                              uint16_t *out, int64_t ldo, void *stream)
+{
+    JQ_REQUIRE(layout == JETQ_SCALES_ROWGROUPS_1X128 || layout == JETQ_SCALES_BLOCKS_128X128, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(rows >= 0 && cols > 0, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(cols % 128 == 0 && ldo >= cols && (layout == JETQ_SCALES_ROWGROUPS_1X128 || rows % 128 == 0),
+               JETQ_ERR_UNSUPPORTED_SHAPE);
+    if (rows == 0)
+        return JETQ_OK;
+    JQ_REQUIRE(q && s && out, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(aligned16(q) && aligned16(out) && ldo % 8 == 0 && (reinterpret_cast<uintptr_t>(s) & 3u) == 0,
+               JETQ_ERR_MISALIGNED);
+    const jetq_status a = check_arch();
+    if (a != JETQ_OK)
+        return a;
+    DequantArgs args{q, s, rows, cols, layout == JETQ_SCALES_BLOCKS_128X128, out, ldo};
+    return from_cuda(launch_dequant_bf16(args, static_cast<cudaStream_t>(stream)));
+}
+
 jetq_status jetq_gemm_fprop(jetq_recipe recipe, const uint8_t *qx, const void *sx, const uint8_t *qw, const void *sw,
                             int64_t n, int64_t d, int64_t c, void *y, jetq_out_dtype y_dtype, int64_t ldy,
                             jetq_path path, void *stream)

@@ -58,6 +58,31 @@ struct WeightPow2Args {
 };
 cudaError_t launch_quant_weight_pow2(const WeightPow2Args &a, cudaStream_t st);
 
+// Column copy re-quantized from a 1x128 row copy (v = fl32(decode(q) * S_row)).
+struct RequantArgs {
+    const uint8_t *q_row;
+    const float *s_row;
+    int64_t n, c;
+    uint8_t *q_col;
+    float *s_col;
+    int64_t ldq_col;
+    const int64_t *seg;
+    int nseg;
+};
+cudaError_t launch_requant_col(const RequantArgs &a, cudaStream_t st);
+
+// BF16 of decode(q) * S, rounded once; blocks = false: 1x128 row groups
+// (s [cols/128 x rows]), true: 128x128 blocks (s [rows/128 x cols/128]).
+struct DequantArgs {
+    const uint8_t *q;
+    const float *s;
+    int64_t rows, cols;
+    bool blocks;
+    uint16_t *out;
+    int64_t ldo;
+};
+cudaError_t launch_dequant_bf16(const DequantArgs &a, cudaStream_t st);
+
 // --------------------------------------------------------------------- GEMMs
 // One block-scaled GEMM problem: out[M x N] = A[M x K] * B[N x K]^T, both
 // operands K-major FP8 with per-128-K-block scales.

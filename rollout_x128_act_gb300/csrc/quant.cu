@@ -703,6 +703,134 @@ __global__ void __launch_bounds__(kThreads, 2) k_quant_mx(MxQuantArgs a)
     }
 }
 
+// E4M3 codes -> binary32 values (exact: every E4M3 value is an FP16 value)
+__device__ __forceinline__ void decode8(uint2 codes, float (&f)[8])
+{
+    const uint32_t w[2] = {codes.x, codes.y};
+#pragma unroll
+    for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+            const __half2_raw hr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(w[h] >> (16 * k)), __NV_E4M3);
+            const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+            f[4 * h + 2 * k] = v.x;
+            f[4 * h + 2 * k + 1] = v.y;
+        }
+}
+
+// Column copy re-quantized from the row copy: one CTA per 128-token group x
+// 128 channels; v = fl32(decode(q_row) * S_row), 128x1 column groups on v,
+// q = E4M3(fl32(v / S)) by the IEEE division (v is not a BF16 value).
+__global__ void __launch_bounds__(kThreads, 2) k_requant_col(const __grid_constant__ RequantArgs a)
+{
+    __shared__ __align__(16) float red[8][128];
+    __shared__ __align__(16) uint8_t tileT[128 * 128];
+    __shared__ Group grp;
+
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int rg = t >> 4, cc = t & 15;
+    const int64_t c0 = (int64_t)blockIdx.y * 128;
+
+    map_group(blockIdx.x, a.n, a.seg, a.nseg, &grp);
+    __syncthreads();
+    const int cnt = grp.cnt;
+    if (cnt == 0)
+        return;
+    const int64_t t0 = grp.t0, p0 = grp.p0;
+
+    float v[8][8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = rg * 8 + i;
+        if (r < cnt) {
+            const uint2 codes = __ldg(reinterpret_cast<const uint2 *>(a.q_row + (t0 + r) * a.c + c0 + cc * 8));
+            const float s = __ldg(a.s_row + (c0 >> 7) * a.n + t0 + r);
+            float d[8];
+            decode8(codes, d);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[i][j] = __fmul_rn(d[j], s);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+                v[i][j] = 0.0f;
+        }
+    }
+    float cm[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        float m = fabsf(v[0][j]);
+#pragma unroll
+        for (int i = 1; i < 8; ++i)
+            m = fmaxf(m, fabsf(v[i][j]));
+        cm[j] = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
+    }
+    if (lane < 16) {
+        *reinterpret_cast<float4 *>(&red[warp][cc * 8]) = make_float4(cm[0], cm[1], cm[2], cm[3]);
+        *reinterpret_cast<float4 *>(&red[warp][cc * 8 + 4]) = make_float4(cm[4], cm[5], cm[6], cm[7]);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        if (w == warp)
+            continue;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            cm[j] = fmaxf(cm[j], red[w][cc * 8 + j]);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float s = __fdiv_rn(cm[j], kE4M3Max);
+        const bool zero = !(s > 0.0f);
+        float q[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            q[i] = zero ? 0.0f : __fdiv_rn(v[i][j], s);
+        tileT_put(tileT, cc * 8 + j, rg, make_uint2(cvt4(q[0], q[1], q[2], q[3]), cvt4(q[4], q[5], q[6], q[7])));
+        if (rg == 0)
+            a.s_col[(p0 >> 7) * a.c + c0 + cc * 8 + j] = s;
+    }
+    __syncthreads();
+    store_tileT(tileT, a.q_col, a.ldq_col, c0, p0);
+}
+
+// BF16 of decode(q) * S rounded once: the FP32 product is exact or within half
+// an FP32 ulp, so only a product that lands exactly on a BF16 midpoint needs
+// the sign of its (exact, FMA) residual; products below 2^-100, whose residual
+// may not be exact, take the binary64 route.
+__device__ __forceinline__ uint32_t bf16_of_product(float d, float s)
+{
+    const float p = __fmul_rn(d, s);
+    if (p != 0.0f && fabsf(p) < 0x1p-100f)
+        return __bfloat16_as_ushort(__double2bfloat16((double)d * (double)s));
+    const uint32_t b = __float_as_uint(p);
+    const float e = __fmaf_rn(d, s, -p);
+    if ((b & 0xFFFFu) == 0x8000u && e != 0.0f)
+        return (b >> 16) + (((e > 0.0f) == (p > 0.0f)) ? 1u : 0u);
+    return __bfloat16_as_ushort(__float2bfloat16_rn(p));
+}
+
+__global__ void __launch_bounds__(256) k_dequant_bf16(const __grid_constant__ DequantArgs a)
+{
+    const int64_t per_row = a.cols / 16;
+    const int64_t units = a.rows * per_row;
+    for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < units; u += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = u / per_row, c = (u - r * per_row) * 16;
+        const uint4 codes = __ldg(reinterpret_cast<const uint4 *>(a.q + r * a.cols + c));
+        const float s = a.blocks ? __ldg(a.s + (r >> 7) * (a.cols >> 7) + (c >> 7)) : __ldg(a.s + (c >> 7) * a.rows + r);
+        float d[16];
+        decode8(make_uint2(codes.x, codes.y), *reinterpret_cast<float(*)[8]>(&d[0]));
+        decode8(make_uint2(codes.z, codes.w), *reinterpret_cast<float(*)[8]>(&d[8]));
+        uint32_t o[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            o[k] = bf16_of_product(d[2 * k], s) | (bf16_of_product(d[2 * k + 1], s) << 16);
+        uint4 *dst = reinterpret_cast<uint4 *>(a.out + r * a.ldo + c);
+        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    }
+}
+
 int64_t groups_upper_bound(int64_t n, const int64_t *seg, int nseg)
 {
     const int64_t g = (n + 127) / 128;
@@ -754,6 +882,25 @@ cudaError_t launch_quant_mx(const MxQuantArgs &a, int group, cudaStream_t st)
         else
             k_quant_mx<false, true, 128><<<grid, kThreads, 0, st>>>(a);
     }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_requant_col(const RequantArgs &a, cudaStream_t st)
+{
+    if (a.n == 0)
+        return cudaSuccess;
+    dim3 grid((unsigned)groups_upper_bound(a.n, a.seg, a.nseg), (unsigned)(a.c / 128));
+    k_requant_col<<<grid, kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_bf16(const DequantArgs &a, cudaStream_t st)
+{
+    const int64_t units = a.rows * (a.cols / 16);
+    if (units == 0)
+        return cudaSuccess;
+    const int64_t want = (units + 255) / 256, cap = (int64_t)sm_count() * 8;
+    k_dequant_bf16<<<(unsigned)(want < cap ? want : cap), 256, 0, st>>>(a);
     return cudaGetLastError();
 }
 
