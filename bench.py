@@ -415,6 +415,83 @@ def measure_pow2(dev):
     return res
 
 
+def measure_f3_kernels(dev):
+    """Re-quantized column copy and BF16 dequantizer on the 8192 x 12288 activation
+    (HBM-bound; algorithmic bytes: 1 + 4/128 read and 1 + 4/128 written per element for
+    the re-quantizer, 1 + 4/128 read and 2 written for the dequantizer)."""
+    import torch
+
+    import rollout_x128_act_gb300 as jq
+
+    act, _, _ = _dev_inputs(dev, 11)
+    h = act(N_TOK, D)
+    a = jq.quant_act(h, col=False)
+    g = jq.requant_col(a["q_row"], a["s_row"])
+    out = torch.empty((N_TOK, D), dtype=torch.bfloat16, device=dev)
+    ms_r = _time(lambda: jq.jetq_requant_col_from_row(a["q_row"], a["s_row"], g["q_col"], g["s_col"],
+                                                      g["ldq_col"]), 20)
+    ms_d = _time(lambda: jq.jetq_dequant_bf16(a["q_row"], a["s_row"], jq.SCALES_ROWGROUPS_1X128, out), 20)
+    n = N_TOK * D
+    return {"requant_col_gbs": round(n * 2 * (1 + 4 / 128) / (ms_r * 1e-3) / 1e9, 1), "requant_col_us": round(ms_r * 1e3, 1),
+            "dequant_bf16_gbs": round(n * (3 + 4 / 128) / (ms_d * 1e-3) / 1e9, 1), "dequant_bf16_us": round(ms_d * 1e3, 1)}
+
+
+def measure_rollout_step(dev, peaks):
+    """On-policy FP8 weight sync plus one rollout decode step of 128 concurrent
+    sequences through the dense-8B MLP (quantize, gate/up FProp, quantize, down
+    FProp), replayed from a CUDA graph: step latency, weight-stream GB/s, and the
+    payload copy's time and byte identity."""
+    import torch
+
+    import rollout_x128_act_gb300 as jq
+
+    act, weight, _ = _dev_inputs(dev, 12)
+    n = 128
+    trainer = {"gate": jq.quant_weight(weight(D, C), transposed=False)[:2],
+               "up": jq.quant_weight(weight(D, C), transposed=False)[:2],
+               "down": jq.quant_weight(weight(C, D), transposed=False)[:2]}
+    rollout = {k: (torch.empty_like(q), torch.empty_like(s)) for k, (q, s) in trainer.items()}
+
+    def sync():
+        for k in trainer:
+            rollout[k][0].copy_(trainer[k][0], non_blocking=True)
+            rollout[k][1].copy_(trainer[k][1], non_blocking=True)
+
+    ms_sync = _time(sync, 10)
+    payload = sum(q.numel() + s.numel() * 4 for q, s in trainer.values())
+    identical = all(torch.equal(rollout[k][0], trainer[k][0]) and torch.equal(rollout[k][1], trainer[k][1])
+                    for k in trainer)
+    x, h = act(n, C), act(n, D)
+    ax, ah = jq.quant_act(x, col=False), jq.quant_act(h, col=False)
+    y = {"gate": torch.empty((n, D), dtype=torch.bfloat16, device=dev),
+         "up": torch.empty((n, D), dtype=torch.bfloat16, device=dev),
+         "down": torch.empty((n, C), dtype=torch.bfloat16, device=dev)}
+
+    def step():
+        jq.jetq_quant_act_1x128(x, ax["q_row"], ax["s_row"], None, None, 0)
+        for k in ("gate", "up"):
+            q, s = rollout[k]
+            jq.jetq_gemm_fprop(jq.RECIPE_BLOCK128, ax["q_row"], ax["s_row"], q, s, n, D, C, y[k], jq.PATH_DECODE)
+        jq.jetq_quant_act_1x128(h, ah["q_row"], ah["s_row"], None, None, 0)
+        q, s = rollout["down"]
+        jq.jetq_gemm_fprop(jq.RECIPE_BLOCK128, ah["q_row"], ah["s_row"], q, s, n, C, D, y["down"], jq.PATH_DECODE)
+
+    st = torch.cuda.Stream()
+    st.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(st):
+        step()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=st):
+            step()
+    ms_step = _time(graph.replay, 20)
+    return {"concurrent": n, "step_us_graph": round(ms_step * 1e3, 2),
+            "weight_gbs": round(payload / (ms_step * 1e-3) / 1e9, 1),
+            "frac_of_hbm": round(payload / (ms_step * 1e-3) / 1e9 / peaks["hbm"], 3),
+            "sync_payload_bytes": int(payload), "sync_us": round(ms_sync * 1e3, 1),
+            "sync_gbs": round(2 * payload / (ms_sync * 1e-3) / 1e9, 1), "sync_byte_identical": bool(identical)}
+
+
 def measure_moe(dev):
     """MoE grouped GEMMs, 30B-A3B shapes: 128 experts, 16384 tokens top-8 with
     Zipf(1.2) load (131072 routed rows), hidden 2048, expert intermediate 768
@@ -638,6 +715,8 @@ def run_ours(args):
             line["decode"] = measure_decode(dev, peaks_now)
             line["mxfp8"] = measure_mxfp8(dev)
             line["block128_pow2"] = measure_pow2(dev)
+            line["requant_dequant"] = measure_f3_kernels(dev)
+            line["rollout_step"] = measure_rollout_step(dev, peaks_now)
             line["moe"] = measure_moe(dev)
             if step_error():
                 raise RuntimeError("device error word set during the secondary measurements")
