@@ -798,6 +798,8 @@ PROFILE_CASES = {
     "quant_mx": "MXFP8 quantizer, X 8192 x 12288 BF16 (row + column copies)",
     "gemm_mx_fprop": "MXFP8 FProp 4096 x 12288 x 4096 (BF16 out)",
     "grouped_fprop": "grouped FProp, 32 experts x 1536 x 2048, 16384 routed rows (Zipf 1.2), BF16 out",
+    "requant_col": "column copy re-quantized from the row copy of H 8192 x 12288",
+    "dequant_bf16": "BF16 dequantization of the row copy of H 8192 x 12288",
 }
 
 
@@ -853,6 +855,15 @@ def run_case(name: str, launches: int = 5):
         qw, sw = torch.stack([q[0] for q in qs]), torch.stack([q[1] for q in qs])
         out = torch.empty((R, d), dtype=torch.bfloat16, device=dev)
         fn = lambda: jq.grouped(jq.GEMM_FPROP, ax["q_row"], ax["s_row"], qw, sw, seg, n=d, k=c, out=out)  # noqa
+    elif name in ("requant_col", "dequant_bf16"):
+        a = jq.quant_act(bf16(synth.activation(8192, 12288, seed=0, stream="h")), col=False)
+        if name == "requant_col":
+            gcol = jq.requant_col(a["q_row"], a["s_row"])
+            fn = lambda: jq.jetq_requant_col_from_row(a["q_row"], a["s_row"], gcol["q_col"], gcol["s_col"],  # noqa
+                                                      gcol["ldq_col"])
+        else:
+            out = torch.empty((8192, 12288), dtype=torch.bfloat16, device=dev)
+            fn = lambda: jq.jetq_dequant_bf16(a["q_row"], a["s_row"], jq.SCALES_ROWGROUPS_1X128, out)  # noqa
     elif name == "quant_mx":
         x = bf16(synth.activation(8192, 12288, seed=0, stream="h"))
         fn = lambda: jq.quant_mx(x)  # noqa: E731

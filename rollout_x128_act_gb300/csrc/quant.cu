@@ -718,12 +718,32 @@ __device__ __forceinline__ void decode8(uint2 codes, float (&f)[8])
         }
 }
 
+// E4M3(fl32(v / s)) for any binary32 v, s >= 2^-96 (r = RN(1/s)): the
+// residual-corrected quotient is within one binary32 ulp of fl32(v / s), so
+// its E4M3 code is the same unless it lies within two ulps of an E4M3 rounding
+// midpoint (bit 19 of the significand set, bits 18..0 clear) or in the E4M3
+// subnormal range; those take the IEEE division.  Two values at a time.
+__device__ __forceinline__ float2 quotient2_for_e4m3(float2 v, float s, float r)
+{
+    const float2 q0 = __fmul2_rn(v, make_float2(r, r));
+    const float2 e = __ffma2_rn(q0, make_float2(-s, -s), v);
+    float2 q = __ffma2_rn(e, make_float2(r, r), q0);
+    const uint32_t ux = __float_as_uint(q.x) & 0x7FFFFFFFu, uy = __float_as_uint(q.y) & 0x7FFFFFFFu;
+    if (ux < 0x3C800000u || ((ux & 0xFFFFFu) - 0x7FFFEu) <= 4u)
+        q.x = __fdiv_rn(v.x, s);
+    if (uy < 0x3C800000u || ((uy & 0xFFFFFu) - 0x7FFFEu) <= 4u)
+        q.y = __fdiv_rn(v.y, s);
+    return q;
+}
+
 // Column copy re-quantized from the row copy: one CTA per 128-token group x
 // 128 channels; v = fl32(decode(q_row) * S_row), 128x1 column groups on v,
-// q = E4M3(fl32(v / S)) by the IEEE division (v is not a BF16 value).
+// q = E4M3(fl32(v / S)) (quotient2_for_e4m3; v is not a BF16 value, for which
+// the plain corrected quotient is proven exact).
 __global__ void __launch_bounds__(kThreads, 2) k_requant_col(const __grid_constant__ RequantArgs a)
 {
     __shared__ __align__(16) float red[8][128];
+    __shared__ __align__(16) float scS[128], scR[128]; // column scales and their reciprocals
     __shared__ __align__(16) uint8_t tileT[128 * 128];
     __shared__ Group grp;
 
@@ -738,22 +758,27 @@ __global__ void __launch_bounds__(kThreads, 2) k_requant_col(const __grid_consta
         return;
     const int64_t t0 = grp.t0, p0 = grp.p0;
 
-    float v[8][8];
+    // all eight rows' loads first (rows past the group read as codes 0, scale 0)
+    uint2 codes[8];
+    float srow[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int r = rg * 8 + i;
-        if (r < cnt) {
-            const uint2 codes = __ldg(reinterpret_cast<const uint2 *>(a.q_row + (t0 + r) * a.c + c0 + cc * 8));
-            const float s = __ldg(a.s_row + (c0 >> 7) * a.n + t0 + r);
-            float d[8];
-            decode8(codes, d);
+        const bool in = r < cnt;
+        codes[i] = in ? __ldg(reinterpret_cast<const uint2 *>(a.q_row + (t0 + r) * a.c + c0 + cc * 8))
+                      : make_uint2(0u, 0u);
+        srow[i] = in ? __ldg(a.s_row + (c0 >> 7) * a.n + t0 + r) : 0.0f;
+    }
+    float v[8][8];
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                v[i][j] = __fmul_rn(d[j], s);
-        } else {
+    for (int i = 0; i < 8; ++i) {
+        float d[8];
+        decode8(codes[i], d);
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-                v[i][j] = 0.0f;
+        for (int j = 0; j < 8; j += 2) {
+            const float2 p2 = __fmul2_rn(make_float2(d[j], d[j + 1]), make_float2(srow[i], srow[i]));
+            v[i][j] = p2.x;
+            v[i][j + 1] = p2.y;
         }
     }
     float cm[8];
@@ -770,25 +795,41 @@ __global__ void __launch_bounds__(kThreads, 2) k_requant_col(const __grid_consta
         *reinterpret_cast<float4 *>(&red[warp][cc * 8 + 4]) = make_float4(cm[4], cm[5], cm[6], cm[7]);
     }
     __syncthreads();
+    // each column's scale once, by one thread
+    if (t < 128) {
+        float m = red[0][t];
 #pragma unroll
-    for (int w = 0; w < 8; ++w) {
-        if (w == warp)
-            continue;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-            cm[j] = fmaxf(cm[j], red[w][cc * 8 + j]);
+        for (int w = 1; w < 8; ++w)
+            m = fmaxf(m, red[w][t]);
+        const float s = __fdiv_rn(m, kE4M3Max);
+        scS[t] = s;
+        scR[t] = (s >= 0x1p-96f) ? __frcp_rn(s) : 0.0f;
+        a.s_col[(p0 >> 7) * a.c + c0 + t] = s;
     }
+    __syncthreads();
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        const float s = __fdiv_rn(cm[j], kE4M3Max);
+        const float s = scS[cc * 8 + j];
         const bool zero = !(s > 0.0f);
         float q[8];
+        if (zero) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i)
-            q[i] = zero ? 0.0f : __fdiv_rn(v[i][j], s);
+            for (int i = 0; i < 8; ++i)
+                q[i] = 0.0f;
+        } else if (s < 0x1p-96f) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                q[i] = __fdiv_rn(v[i][j], s);
+        } else {
+            const float r = scR[cc * 8 + j];
+#pragma unroll
+            for (int i = 0; i < 8; i += 2) {
+                const float2 qq = quotient2_for_e4m3(make_float2(v[i][j], v[i + 1][j]), s, r);
+                q[i] = qq.x;
+                q[i + 1] = qq.y;
+            }
+        }
         tileT_put(tileT, cc * 8 + j, rg, make_uint2(cvt4(q[0], q[1], q[2], q[3]), cvt4(q[4], q[5], q[6], q[7])));
-        if (rg == 0)
-            a.s_col[(p0 >> 7) * a.c + c0 + cc * 8 + j] = s;
     }
     __syncthreads();
     store_tileT(tileT, a.q_col, a.ldq_col, c0, p0);
@@ -810,25 +851,37 @@ __device__ __forceinline__ uint32_t bf16_of_product(float d, float s)
     return __bfloat16_as_ushort(__float2bfloat16_rn(p));
 }
 
+// One block per (row, 4096-column segment): thread t converts columns
+// 16t .. 16t+15 of the segment (no index division anywhere).
 __global__ void __launch_bounds__(256) k_dequant_bf16(const __grid_constant__ DequantArgs a)
 {
-    const int64_t per_row = a.cols / 16;
-    const int64_t units = a.rows * per_row;
-    for (int64_t u = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; u < units; u += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = u / per_row, c = (u - r * per_row) * 16;
-        const uint4 codes = __ldg(reinterpret_cast<const uint4 *>(a.q + r * a.cols + c));
-        const float s = a.blocks ? __ldg(a.s + (r >> 7) * (a.cols >> 7) + (c >> 7)) : __ldg(a.s + (c >> 7) * a.rows + r);
-        float d[16];
-        decode8(make_uint2(codes.x, codes.y), *reinterpret_cast<float(*)[8]>(&d[0]));
-        decode8(make_uint2(codes.z, codes.w), *reinterpret_cast<float(*)[8]>(&d[8]));
-        uint32_t o[8];
+    const int64_t r = blockIdx.y;
+    const int64_t c = (int64_t)blockIdx.x * 4096 + threadIdx.x * 16;
+    if (c >= a.cols)
+        return;
+    const uint4 codes = __ldg(reinterpret_cast<const uint4 *>(a.q + r * a.cols + c));
+    const float s = a.blocks ? __ldg(a.s + (r >> 7) * (a.cols >> 7) + (c >> 7)) : __ldg(a.s + (c >> 7) * a.rows + r);
+    float d[16];
+    decode8(make_uint2(codes.x, codes.y), *reinterpret_cast<float(*)[8]>(&d[0]));
+    decode8(make_uint2(codes.z, codes.w), *reinterpret_cast<float(*)[8]>(&d[8]));
+    uint32_t o[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-            o[k] = bf16_of_product(d[2 * k], s) | (bf16_of_product(d[2 * k + 1], s) << 16);
-        uint4 *dst = reinterpret_cast<uint4 *>(a.out + r * a.ldo + c);
-        dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-        dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+    for (int j = 0; j < 8; ++j) {
+        // packed product and rounding; a midpoint tie or a tiny product takes the exact route
+        const float2 p2 = __fmul2_rn(make_float2(d[2 * j], d[2 * j + 1]), make_float2(s, s));
+        const uint32_t bx = __float_as_uint(p2.x), by = __float_as_uint(p2.y);
+        const bool odd = (bx & 0xFFFFu) == 0x8000u || (by & 0xFFFFu) == 0x8000u ||
+                         ((bx & 0x7FFFFFFFu) - 1u) < 0x0D7FFFFFu || ((by & 0x7FFFFFFFu) - 1u) < 0x0D7FFFFFu;
+        if (odd) {
+            o[j] = bf16_of_product(d[2 * j], s) | (bf16_of_product(d[2 * j + 1], s) << 16);
+        } else {
+            const __nv_bfloat162 h2 = __floats2bfloat162_rn(p2.x, p2.y);
+            o[j] = *reinterpret_cast<const uint32_t *>(&h2);
+        }
     }
+    uint4 *dst = reinterpret_cast<uint4 *>(a.out + r * a.ldo + c);
+    dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
 int64_t groups_upper_bound(int64_t n, const int64_t *seg, int nseg)
@@ -896,11 +949,12 @@ cudaError_t launch_requant_col(const RequantArgs &a, cudaStream_t st)
 
 cudaError_t launch_dequant_bf16(const DequantArgs &a, cudaStream_t st)
 {
-    const int64_t units = a.rows * (a.cols / 16);
-    if (units == 0)
+    if (a.rows == 0)
         return cudaSuccess;
-    const int64_t want = (units + 255) / 256, cap = (int64_t)sm_count() * 8;
-    k_dequant_bf16<<<(unsigned)(want < cap ? want : cap), 256, 0, st>>>(a);
+    if (a.rows > 2147483647)
+        return cudaErrorInvalidValue;
+    dim3 grid((unsigned)((a.cols + 4095) / 4096), (unsigned)a.rows);
+    k_dequant_bf16<<<grid, 256, 0, st>>>(a);
     return cudaGetLastError();
 }
 

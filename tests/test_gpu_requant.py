@@ -36,6 +36,34 @@ def test_requant_col_bit_exact(kind):
     assert np.array_equal(g["s_col"].cpu().numpy()[:P // 128].view(np.uint32), sc.view(np.uint32))
 
 
+def test_requant_quotients_near_e4m3_midpoints():
+    """Codes of 1.0 make each rebuilt value its row scale, so the values can be placed
+    at S * m nudged by -4..+4 binary32 ulps for E4M3 midpoints m: both sides of the
+    fast quotient's two-ulp guard, and the E4M3 subnormal range."""
+    amax = np.float32(448.0 * 1.2345678)
+    S = np.float32(amax / np.float32(448.0))
+    mids = [1.0625, 1.1875, 1.9375, 0.53125, 3.75, 7.5, 240.0, 416.0, 0.01953125, 0.017578125, 0.0029296875]
+    vals = [amax]
+    for m in mids:
+        base = np.float32(np.float32(m) * S)
+        for k in range(-4, 5):
+            v = base
+            for _ in range(abs(k)):
+                v = np.nextafter(v, np.float32(np.inf) if k > 0 else np.float32(0))
+            vals.append(v)
+    vals = np.array(vals, np.float32)
+    R = 128
+    s_row = np.zeros((1, R), np.float32)
+    s_row[0, :len(vals)] = vals
+    s_row[0, len(vals):] = -vals[1:R - len(vals) + 1]  # negative copies fill the group
+    q_row = np.full((R, 128), 0x38, np.uint8)
+    g = jq.requant_col(torch.as_tensor(q_row, device=DEV), torch.as_tensor(s_row, device=DEV))
+    torch.cuda.synchronize()
+    qc, sc = oracle.requant_colgroups(q_row, s_row)
+    assert sc[0, 0] == S
+    assert np.array_equal(u8(g["q_col"]), qc)
+
+
 def test_requant_col_full_size_sampled():
     R, C = 8192, 12288
     x = synth.activation(R, C, seed=52, stream="h")
