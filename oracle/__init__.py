@@ -62,6 +62,10 @@ def _load():
         lib.jo_quant_colgroups.argtypes = [P, I, I, I, I, P, ctypes.c_int, P, I, P]
         lib.jo_quant_blocks.argtypes = [P, I, I, I, I, P, P, P, P]
         lib.jo_quant_blocks_pow2.argtypes = [P, I, I, I, I, P, P, P, P]
+        lib.jo_expf_fixed.restype = ctypes.c_float
+        lib.jo_expf_fixed.argtypes = [ctypes.c_float]
+        lib.jo_swiglu_bf16.argtypes = [P, P, I, P]
+        lib.jo_rmsnorm_bf16.argtypes = [P, P, I, I, I, ctypes.c_float, P, P]
         lib.jo_requant_colgroups.argtypes = [P, P, I, I, I, P, ctypes.c_int, P, I, P]
         lib.jo_dequant_rowgroups_bf16.argtypes = [P, I, I, I, P, P]
         lib.jo_dequant_blocks_bf16.argtypes = [P, I, I, I, P, P]
@@ -207,6 +211,35 @@ def dequant_blocks_bf16(q, s, bs: int = 128):
     out = np.empty((D, C), np.uint16)
     _load().jo_dequant_blocks_bf16(_p(q), D, C, bs, _p(s), _p(out))
     return out
+
+
+def expf_fixed(x: float) -> float:
+    """The binary32 exp of the fused SwiGLU producer (Cody-Waite + Taylor, fmaf)."""
+    return float(_load().jo_expf_fixed(ctypes.c_float(x)))
+
+
+def swiglu_bf16(gate, up):
+    """BF16 bits of silu(gate) * up, operation by operation in binary32."""
+    gate = _c(gate, np.uint16)
+    up = _c(up, np.uint16)
+    if gate.shape != up.shape:
+        raise ValueError("gate and up must have the same shape")
+    h = np.empty(gate.shape, np.uint16)
+    _load().jo_swiglu_bf16(_p(gate), _p(up), gate.size, _p(h))
+    return h
+
+
+def rmsnorm_bf16(x, w, eps: float = 1e-6):
+    """BF16 bits of RMSNorm(x) * w and the per-row rstd (fixed binary32 summation order)."""
+    x = _c(x, np.uint16)
+    w = _c(w, np.uint16)
+    R, C = x.shape
+    if C % 128 or w.shape != (C,):
+        raise ValueError("columns must be a multiple of 128 and w must have one entry per column")
+    y = np.empty((R, C), np.uint16)
+    rstd = np.empty(R, np.float32)
+    _load().jo_rmsnorm_bf16(_p(x), _p(w), R, C, C, ctypes.c_float(eps), _p(y), _p(rstd))
+    return y, rstd
 
 
 def quant_blocks_pow2(w, bs: int = 128):

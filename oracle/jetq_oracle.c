@@ -311,6 +311,97 @@ void jo_dequant_blocks_bf16(const uint8_t *q, int64_t rows, int64_t cols, int64_
                 bf16_rne(jo_e4m3_decode(q[r * cols + c]) * (double)s[(r / bs) * (cols / bs) + c / bs]);
 }
 
+/* ------------------------------------------------------------------------ */
+/* Producers fused with the 1x128 quantizer ([JR] the activation quantizer  */
+/* sits in the kernel that produces the tensor; the pages name RMSNorm and  */
+/* the SwiGLU product as producers).  The producer output is the BF16 value */
+/* the unfused layer would store, defined operation by operation in          */
+/* binary32 so that the GPU can reproduce it bit for bit; it is then         */
+/* quantized exactly as jo_quant_rowgroups / jo_quant_colgroups quantize     */
+/* BF16 input.                                                               */
+/* ------------------------------------------------------------------------ */
+
+static uint16_t bf16_of_float(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    u += 0x7FFFu + ((u >> 16) & 1u); /* round to nearest even (finite values) */
+    return (uint16_t)(u >> 16);
+}
+
+static float float_of_bits(uint32_t u)
+{
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/*
+ * exp in binary32 by Cody-Waite reduction and a Taylor polynomial (textbook
+ * method, e.g. Muller, "Elementary Functions", ch. 11): n = rint(x log2 e),
+ * r = x - n ln2 with ln2 split in two constants, exp(r) = sum_{k<=7} r^k/k!
+ * in Horner form with fmaf, result p * 2^n (2^n built from its bits).
+ * Inputs above 88 give +inf, below -87 give 0 (flushed).
+ */
+float jo_expf_fixed(float x)
+{
+    const float log2e = 1.44269502f, ln2_hi = 0.693145751953125f, ln2_lo = 1.42860677e-06f;
+    const float c[8] = {1.0f, 1.0f, 0.5f, 0.166666672f, 0.0416666679f, 0.00833333377f, 0.00138888892f,
+                        0.000198412701f};
+    float n, r, p;
+    int k;
+    if (x > 88.0f)
+        return float_of_bits(0x7F800000u);
+    if (x < -87.0f)
+        return 0.0f;
+    n = rintf(x * log2e);
+    r = fmaf(-n, ln2_hi, x);
+    r = fmaf(-n, ln2_lo, r);
+    p = c[7];
+    for (k = 6; k >= 0; --k)
+        p = fmaf(p, r, c[k]);
+    return p * float_of_bits((uint32_t)((int)n + 127) << 23);
+}
+
+/* SwiGLU product: h = BF16(fl32(fl32(g * fl32(1 / fl32(1 + exp(-g)))) * u)) */
+void jo_swiglu_bf16(const uint16_t *gate, const uint16_t *up, int64_t count, uint16_t *h)
+{
+    int64_t i;
+    for (i = 0; i < count; ++i) {
+        float gv = bf16_value(gate[i]), uv = bf16_value(up[i]);
+        float e = jo_expf_fixed(-gv);
+        float sg = 1.0f / (1.0f + e);
+        h[i] = bf16_of_float((gv * sg) * uv);
+    }
+}
+
+/*
+ * RMSNorm: per row, the sum of squares in binary32 in a fixed order (each
+ * 128-column group summed left to right with fmaf, then the group sums added
+ * left to right), rstd = 1 / sqrt(sum / cols + eps) (IEEE division and square
+ * root), y = BF16(fl32(fl32(x * rstd) * w)).  rstd is returned per row.
+ */
+void jo_rmsnorm_bf16(const uint16_t *x, const uint16_t *w, int64_t rows, int64_t cols, int64_t ldx, float eps,
+                     uint16_t *y, float *rstd)
+{
+    int64_t r, c, g;
+    for (r = 0; r < rows; ++r) {
+        float total = 0.0f, rs;
+        for (g = 0; g < cols / 128; ++g) {
+            float part = 0.0f;
+            for (c = g * 128; c < (g + 1) * 128; ++c) {
+                float v = bf16_value(x[r * ldx + c]);
+                part = fmaf(v, v, part);
+            }
+            total = total + part;
+        }
+        rs = 1.0f / sqrtf(total / (float)cols + eps);
+        rstd[r] = rs;
+        for (c = 0; c < cols; ++c)
+            y[r * cols + c] = bf16_of_float((bf16_value(x[r * ldx + c]) * rs) * bf16_value(w[c]));
+    }
+}
+
 /*
  * Square blocks of bs x bs ([JR] 128x128 per-block weight quantization,
  * S_W(i,j) = max|W_tile(i,j)| / 448, W^ = round(W / S_W)).
