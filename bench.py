@@ -436,6 +436,48 @@ def measure_f3_kernels(dev):
             "dequant_bf16_gbs": round(n * (3 + 4 / 128) / (ms_d * 1e-3) / 1e9, 1), "dequant_bf16_us": round(ms_d * 1e3, 1)}
 
 
+def measure_fused_producers(dev):
+    """The 1x128 quantizer fused with its producer, dense-8B MLP shapes, row + column
+    copies.  RMSNorm over X 8192 x 4096 (four input buffers in rotation, 256 MB, so no
+    launch finds its input in L2 from the launch before; the statistics pass and the
+    quantizer each read X, the second read mostly from L2); SwiGLU over gate and up
+    8192 x 12288 (400 MB).  Algorithmic bytes per element: the producer's inputs once
+    (2 for RMSNorm, 4 for SwiGLU) + 2 * (1 + 4/128) written.  The plain quantizer on the
+    same X is timed beside them."""
+    import torch
+
+    import rollout_x128_act_gb300 as jq
+
+    act, _, _ = _dev_inputs(dev, 12)
+    xs = [act(N_TOK, C) for _ in range(4)]
+    w = (1.0 + 0.1 * act(1, C).float().clamp(-3, 3)).to(torch.bfloat16).view(-1)
+    o = jq.quant_act_rmsnorm(xs[0], w)
+    it = [0]
+
+    def rms():
+        it[0] += 1
+        jq.jetq_quant_act_1x128_rmsnorm(xs[it[0] % 4], w, 1e-6, o["rstd"], o["q_row"], o["s_row"], o["q_col"],
+                                        o["s_col"], o["ldq_col"])
+
+    def plain():
+        it[0] += 1
+        jq.jetq_quant_act_1x128(xs[it[0] % 4], o["q_row"], o["s_row"], o["q_col"], o["s_col"], o["ldq_col"])
+
+    ms_rms, ms_plain = _time(rms, 40), _time(plain, 40)
+    del xs
+    gate, up = act(N_TOK, D), act(N_TOK, D)
+    s = jq.quant_act_swiglu(gate, up)
+    ms_sw = _time(lambda: jq.jetq_quant_act_1x128_swiglu(gate, up, s["q_row"], s["s_row"], s["q_col"], s["s_col"],
+                                                         s["ldq_col"]), 20)
+    out_b = 2 * (1 + 4 / 128)
+    nx, nh = N_TOK * C, N_TOK * D
+    return {"rmsnorm_quant_gbs": round(nx * (2 + out_b) / (ms_rms * 1e-3) / 1e9, 1),
+            "rmsnorm_quant_us": round(ms_rms * 1e3, 1),
+            "plain_quant_same_x_us": round(ms_plain * 1e3, 1),
+            "swiglu_quant_gbs": round(nh * (4 + out_b) / (ms_sw * 1e-3) / 1e9, 1),
+            "swiglu_quant_us": round(ms_sw * 1e3, 1)}
+
+
 def measure_rollout_step(dev, peaks):
     """On-policy FP8 weight sync plus one rollout decode step of 128 concurrent
     sequences through the dense-8B MLP (quantize, gate/up FProp, quantize, down
@@ -716,6 +758,7 @@ def run_ours(args):
             line["mxfp8"] = measure_mxfp8(dev)
             line["block128_pow2"] = measure_pow2(dev)
             line["requant_dequant"] = measure_f3_kernels(dev)
+            line["fused_producers"] = measure_fused_producers(dev)
             line["rollout_step"] = measure_rollout_step(dev, peaks_now)
             line["moe"] = measure_moe(dev)
             if step_error():
@@ -800,6 +843,8 @@ PROFILE_CASES = {
     "grouped_fprop": "grouped FProp, 32 experts x 1536 x 2048, 16384 routed rows (Zipf 1.2), BF16 out",
     "requant_col": "column copy re-quantized from the row copy of H 8192 x 12288",
     "dequant_bf16": "BF16 dequantization of the row copy of H 8192 x 12288",
+    "quant_rmsnorm": "RMSNorm statistics + fused RMSNorm quantizer, X 32768 x 4096 BF16 (row + column copies)",
+    "quant_swiglu": "fused SwiGLU quantizer, gate and up 8192 x 12288 BF16 (row + column copies)",
 }
 
 
@@ -864,6 +909,14 @@ def run_case(name: str, launches: int = 5):
         else:
             out = torch.empty((8192, 12288), dtype=torch.bfloat16, device=dev)
             fn = lambda: jq.jetq_dequant_bf16(a["q_row"], a["s_row"], jq.SCALES_ROWGROUPS_1X128, out)  # noqa
+    elif name == "quant_rmsnorm":
+        x = bf16(synth.activation(32768, 4096, seed=0, stream="x"))
+        w = bf16(synth.bf16_bits(1.0 + 0.1 * synth.normal(4096, seed=0, stream=synth.STREAM["x"])))
+        fn = lambda: jq.quant_act_rmsnorm(x, w)  # noqa: E731
+    elif name == "quant_swiglu":
+        gate = bf16(synth.activation(8192, 12288, seed=0, stream="h"))
+        up = bf16(synth.activation(8192, 12288, seed=1, stream="h"))
+        fn = lambda: jq.quant_act_swiglu(gate, up)  # noqa: E731
     elif name == "quant_mx":
         x = bf16(synth.activation(8192, 12288, seed=0, stream="h"))
         fn = lambda: jq.quant_mx(x)  # noqa: E731

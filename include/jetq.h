@@ -180,6 +180,57 @@ JETQ_API jetq_status jetq_quant_act_1x128(const uint16_t *x, int64_t n, int64_t 
                                  const int64_t *seg_offsets, int nseg, void *stream);
 
 /*
+ * Activation quantizer fused with its producer: RMSNorm.
+ * Jet-RL explainer, "The Three GEMM Operations and Their Quantization
+ * Configuration" (the activation quantizer is fused with the preceding
+ * operator, typically RMSNorm) and "Implementation Details: Frameworks,
+ * Kernels, and Weight Synchronization" (fused_rmsnorm_quantize: RMSNorm, then
+ * 1x128 quantization, with no BF16 write in between).
+ *
+ * The quantized tensor is y = BF16(fl32(fl32(x * rstd[r]) * w[col])) with
+ * rstd[r] = 1 / sqrt(fl32(sum_sq(x[r]) / c) + eps), every operation a
+ * correctly rounded binary32 one and the sum of squares taken in a fixed
+ * order: each 128-column group left to right by fma, then the group sums
+ * left to right.  y is quantized exactly as jetq_quant_act_1x128 quantizes
+ * BF16 input; y itself is not stored.
+ *
+ *   x, n, c, ldx   BF16 input [n x c], row stride ldx (multiple of 8); c <= 32768
+ *   w              BF16 weight [c] (16-byte aligned)
+ *   eps            in [0, 1]
+ *   rstd           float [n], device: written with rstd[r] (kept for the
+ *                  backward pass); written even when both copies are skipped
+ *   q_row ... nseg as for jetq_quant_act_1x128
+ * Two launches on `stream`: the per-row statistics, then the quantizer.
+ */
+JETQ_API jetq_status jetq_quant_act_1x128_rmsnorm(const uint16_t *x, int64_t n, int64_t c, int64_t ldx,
+                                 const uint16_t *w, float eps, float *rstd,
+                                 uint8_t *q_row, float *s_row,
+                                 uint8_t *q_col, float *s_col, int64_t ldq_col,
+                                 const int64_t *seg_offsets, int nseg, void *stream);
+
+/*
+ * Activation quantizer fused with its producer: the SwiGLU product feeding
+ * the down projection (Jet-RL explainer, "Summary of What Jet-RL Changes
+ * Versus BF16 Training", MLP block: SiLU of the gate output times the up
+ * output, then 1x128 quantization before the down projection; papercache
+ * summary 4.3: fused activation and RMSNorm kernels beside the quantizers).
+ *
+ * The quantized tensor is h = BF16(fl32(fl32(g * fl32(1 / fl32(1 + e))) * u))
+ * with e = exp(-g) in binary32 by Cody-Waite reduction and a degree-7 Taylor
+ * polynomial evaluated by fma (the same function on every machine; +inf for
+ * -g > 88, 0 for -g < -87).  h is quantized exactly as jetq_quant_act_1x128
+ * quantizes BF16 input and is not stored.
+ *
+ *   gate, up       BF16 [n x c], row strides ldg, ldu (multiples of 8)
+ *   q_row ... nseg as for jetq_quant_act_1x128
+ */
+JETQ_API jetq_status jetq_quant_act_1x128_swiglu(const uint16_t *gate, const uint16_t *up, int64_t n, int64_t c,
+                                 int64_t ldg, int64_t ldu,
+                                 uint8_t *q_row, float *s_row,
+                                 uint8_t *q_col, float *s_col, int64_t ldq_col,
+                                 const int64_t *seg_offsets, int nseg, void *stream);
+
+/*
  * Weight quantizer, 128x128 blocks (Jet-RL explainer, "GEMM Quantization":
  * S_W(i,j) = max|W_tile(i,j)| / 448; the DGrad operand is the same FP8
  * weight, only transposed).  Runs after every optimizer step; its output is

@@ -55,6 +55,9 @@ def lib() -> ctypes.CDLL:
             "jetq_colcopy_capacity": (I64, [I64, I32]),
             "jetq_mx_scale_bytes": (I64, [I64, I64]),
             "jetq_quant_act_1x128": (I32, [P, I64, I64, I64, P, P, P, P, I64, P, I32, P]),
+            "jetq_quant_act_1x128_rmsnorm": (I32, [P, I64, I64, I64, P, ctypes.c_float, P, P, P, P, P, I64, P, I32,
+                                                   P]),
+            "jetq_quant_act_1x128_swiglu": (I32, [P, P, I64, I64, I64, I64, P, P, P, P, I64, P, I32, P]),
             "jetq_quant_w_128x128": (I32, [P, I64, I64, I64, P, P, P, P, P]),
             "jetq_quant_mx32": (I32, [P, I64, I64, I64, P, P, P, P, I64, P, I32, P]),
             "jetq_quant_act_1x128_pow2": (I32, [P, I64, I64, I64, P, P, P, P, I64, P, I32, P]),
@@ -122,6 +125,22 @@ def jetq_quant_act_1x128(x, q_row, s_row, q_col, s_col, ldq_col, seg_offsets=Non
     n, c = x.shape
     _check(lib().jetq_quant_act_1x128(_p(x), n, c, x.stride(0), _p(q_row), _p(s_row), _p(q_col), _p(s_col),
                                       ldq_col, _p(seg_offsets), nseg, _s(stream)), "jetq_quant_act_1x128")
+
+
+def jetq_quant_act_1x128_rmsnorm(x, w, eps, rstd, q_row, s_row, q_col, s_col, ldq_col, seg_offsets=None, nseg=0,
+                                 stream=None):
+    n, c = x.shape
+    _check(lib().jetq_quant_act_1x128_rmsnorm(_p(x), n, c, x.stride(0), _p(w), float(eps), _p(rstd), _p(q_row),
+                                              _p(s_row), _p(q_col), _p(s_col), ldq_col, _p(seg_offsets), nseg,
+                                              _s(stream)), "jetq_quant_act_1x128_rmsnorm")
+
+
+def jetq_quant_act_1x128_swiglu(gate, up, q_row, s_row, q_col, s_col, ldq_col, seg_offsets=None, nseg=0, stream=None):
+    n, c = gate.shape
+    assert up.shape == gate.shape
+    _check(lib().jetq_quant_act_1x128_swiglu(_p(gate), _p(up), n, c, gate.stride(0), up.stride(0), _p(q_row),
+                                             _p(s_row), _p(q_col), _p(s_col), ldq_col, _p(seg_offsets), nseg,
+                                             _s(stream)), "jetq_quant_act_1x128_swiglu")
 
 
 def jetq_quant_w_128x128(w, q, s, qT=None, sT=None, stream=None):
@@ -222,6 +241,38 @@ def quant_act(x, row=True, col=True, seg_offsets=None, stream=None):
         out["q_col"] = torch.empty((c, cap), dtype=torch.uint8, device=dev)
         out["s_col"] = torch.empty((max(cap, 128) // 128, c), dtype=torch.float32, device=dev)
     jetq_quant_act_1x128(x, out["q_row"], out["s_row"], out["q_col"], out["s_col"], cap, seg_offsets, nseg, stream)
+    return out
+
+
+def _act_copies(n, c, dev, row, col, seg_offsets):
+    nseg = 0 if seg_offsets is None else seg_offsets.numel() - 1
+    cap = jetq_colcopy_capacity(n, max(nseg, 1))
+    out = dict(q_row=None, s_row=None, q_col=None, s_col=None, ldq_col=cap)
+    if row:
+        out["q_row"] = torch.empty((n, c), dtype=torch.uint8, device=dev)
+        out["s_row"] = torch.empty((c // 128, n), dtype=torch.float32, device=dev)
+    if col:
+        out["q_col"] = torch.empty((c, cap), dtype=torch.uint8, device=dev)
+        out["s_col"] = torch.empty((max(cap, 128) // 128, c), dtype=torch.float32, device=dev)
+    return out, nseg
+
+
+def quant_act_rmsnorm(x, w, eps=1e-6, row=True, col=True, seg_offsets=None, stream=None):
+    """1x128 copies of RMSNorm(x) * w (BF16, not stored): the quant_act dict plus rstd [n]."""
+    n, c = x.shape
+    out, nseg = _act_copies(n, c, x.device, row, col, seg_offsets)
+    out["rstd"] = torch.empty(n, dtype=torch.float32, device=x.device)
+    jetq_quant_act_1x128_rmsnorm(x, w, eps, out["rstd"], out["q_row"], out["s_row"], out["q_col"], out["s_col"],
+                                 out["ldq_col"], seg_offsets, nseg, stream)
+    return out
+
+
+def quant_act_swiglu(gate, up, row=True, col=True, seg_offsets=None, stream=None):
+    """1x128 copies of silu(gate) * up (BF16, not stored), as the quant_act dict."""
+    n, c = gate.shape
+    out, nseg = _act_copies(n, c, gate.device, row, col, seg_offsets)
+    jetq_quant_act_1x128_swiglu(gate, up, out["q_row"], out["s_row"], out["q_col"], out["s_col"], out["ldq_col"],
+                                seg_offsets, nseg, stream)
     return out
 
 

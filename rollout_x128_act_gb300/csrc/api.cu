@@ -160,6 +160,80 @@ jetq_status jetq_quant_act_1x128(const uint16_t *x, int64_t n, int64_t c, int64_
     return from_cuda(launch_quant_act(args, static_cast<cudaStream_t>(stream)));
 }
 
+namespace {
+
+// validation shared by the activation quantizer and its fused-producer forms
+jetq_status check_act_copies(int64_t n, int64_t c, uint8_t *q_row, float *s_row, uint8_t *q_col, float *s_col,
+                             int64_t ldq_col, const int64_t *seg_offsets, int nseg)
+{
+    JQ_REQUIRE(n >= 0 && c > 0, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE((q_row == nullptr) == (s_row == nullptr), JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE((q_col == nullptr) == (s_col == nullptr), JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(seg_offsets == nullptr || nseg >= 1, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(c % 128 == 0, JETQ_ERR_UNSUPPORTED_SHAPE);
+    if (q_col)
+        JQ_REQUIRE(ldq_col % 128 == 0 && ldq_col >= jetq_colcopy_capacity(n, seg_offsets ? nseg : 1),
+                   JETQ_ERR_UNSUPPORTED_SHAPE);
+    JQ_REQUIRE(aligned16(q_row) && aligned16(s_row) && aligned16(q_col) && aligned16(s_col) &&
+                   (reinterpret_cast<uintptr_t>(seg_offsets) & 7u) == 0,
+               JETQ_ERR_MISALIGNED);
+    return JETQ_OK;
+}
+
+} // namespace
+
+jetq_status jetq_quant_act_1x128_rmsnorm(const uint16_t *x, int64_t n, int64_t c, int64_t ldx, const uint16_t *w,
+                                         float eps, float *rstd, uint8_t *q_row, float *s_row, uint8_t *q_col,
+                                         float *s_col, int64_t ldq_col, const int64_t *seg_offsets, int nseg,
+                                         void *stream)
+{
+    const jetq_status v = check_act_copies(n, c, q_row, s_row, q_col, s_col, ldq_col, seg_offsets, nseg);
+    if (v != JETQ_OK)
+        return v;
+    JQ_REQUIRE(ldx >= c && c <= 32768, JETQ_ERR_UNSUPPORTED_SHAPE);
+    JQ_REQUIRE(eps >= 0.0f && eps <= 1.0f, JETQ_ERR_INVALID_ARG);
+    if (n == 0)
+        return JETQ_OK;
+    JQ_REQUIRE(x != nullptr && w != nullptr && rstd != nullptr, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(aligned16(x) && ldx % 8 == 0 && aligned16(w) && (reinterpret_cast<uintptr_t>(rstd) & 3u) == 0,
+               JETQ_ERR_MISALIGNED);
+    const jetq_status a = check_arch();
+    if (a != JETQ_OK)
+        return a;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_rms_rstd(x, n, c, ldx, eps, rstd, st);
+    if (e != cudaSuccess || (!q_row && !q_col))
+        return from_cuda(e);
+    ActQuantArgs args{x, n, c, ldx, q_row, s_row, q_col, s_col, ldq_col, seg_offsets, seg_offsets ? nseg : 1};
+    args.producer = kProduceRms;
+    args.w = w;
+    args.rstd = rstd;
+    return from_cuda(launch_quant_act(args, st));
+}
+
+jetq_status jetq_quant_act_1x128_swiglu(const uint16_t *gate, const uint16_t *up, int64_t n, int64_t c,
+                                        int64_t ldg, int64_t ldu, uint8_t *q_row, float *s_row, uint8_t *q_col,
+                                        float *s_col, int64_t ldq_col, const int64_t *seg_offsets, int nseg,
+                                        void *stream)
+{
+    const jetq_status v = check_act_copies(n, c, q_row, s_row, q_col, s_col, ldq_col, seg_offsets, nseg);
+    if (v != JETQ_OK)
+        return v;
+    JQ_REQUIRE(ldg >= c && ldu >= c, JETQ_ERR_UNSUPPORTED_SHAPE);
+    if (n == 0 || (!q_row && !q_col))
+        return JETQ_OK;
+    JQ_REQUIRE(gate != nullptr && up != nullptr, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(aligned16(gate) && ldg % 8 == 0 && aligned16(up) && ldu % 8 == 0, JETQ_ERR_MISALIGNED);
+    const jetq_status a = check_arch();
+    if (a != JETQ_OK)
+        return a;
+    ActQuantArgs args{gate, n, c, ldg, q_row, s_row, q_col, s_col, ldq_col, seg_offsets, seg_offsets ? nseg : 1};
+    args.producer = kProduceSwiglu;
+    args.up = up;
+    args.ldup = ldu;
+    return from_cuda(launch_quant_act(args, static_cast<cudaStream_t>(stream)));
+}
+
 jetq_status jetq_quant_w_128x128(const uint16_t *w, int64_t d, int64_t c, int64_t ldw, uint8_t *q, float *s,
                                  uint8_t *qT, float *sT, void *stream)
 {

@@ -10,6 +10,10 @@
 namespace jetq {
 
 // ---------------------------------------------------------------- quantizers
+// Producer fused ahead of the activation quantizer: the quantized tensor is
+// x itself, RMSNorm(x) * w, or silu(x) * up, rounded to BF16.
+enum ActProducer : int { kProducePlain = 0, kProduceRms = 1, kProduceSwiglu = 2 };
+
 struct ActQuantArgs {
     const uint16_t *x;
     int64_t n, c, ldx;
@@ -20,7 +24,18 @@ struct ActQuantArgs {
     int64_t ldq_col;
     const int64_t *seg; // device, nseg + 1 entries, or nullptr
     int nseg;
+    int producer = kProducePlain;
+    const uint16_t *up = nullptr; // SwiGLU: the up projection [n x ldup]
+    int64_t ldup = 0;
+    const uint16_t *w = nullptr;  // RMSNorm: per-column weight [c]
+    const float *rstd = nullptr;  // RMSNorm: per-row 1 / rms, from launch_rms_rstd
 };
+
+// RMSNorm statistics: rstd[r] = 1 / sqrt(sum_sq(x[r]) / c + eps), the sum of
+// squares in binary32 in a fixed order (each 128-column group left to right
+// by fma, then the group sums left to right); c a multiple of 128, <= 32768.
+cudaError_t launch_rms_rstd(const uint16_t *x, int64_t n, int64_t c, int64_t ldx, float eps, float *rstd,
+                            cudaStream_t st);
 
 struct WeightQuantArgs {
     const uint16_t *w;

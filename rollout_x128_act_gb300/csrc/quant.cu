@@ -262,6 +262,127 @@ __device__ __forceinline__ void load_block(const uint16_t *x, int64_t ldx, int64
         unpack8(raw[i], v[i]);
 }
 
+// ------------------------------------------------------------ fused producers
+//
+// The quantized tensor may be produced in the same pass (the activation
+// quantizer sits in the kernel that produces the activation): RMSNorm(x) * w
+// with a per-row rstd from k_rms_rstd, or the SwiGLU product silu(g) * u.
+// Each is the BF16 value the unfused layer would store, computed operation by
+// operation in binary32 with explicitly rounded intrinsics, so it is
+// reproducible on any IEEE machine.
+
+__device__ __forceinline__ float bf16_round(float f)
+{
+    return __bfloat162float(__float2bfloat16_rn(f));
+}
+
+// exp in binary32: Cody-Waite reduction r = x - n ln2 (ln2 in two parts),
+// n = rint(x log2 e), and the degree-7 Taylor polynomial of exp(r) in Horner
+// form (Muller, "Elementary Functions", ch. 11); p * 2^n with 2^n built from
+// its bits.  Above 88: +inf; below -87: 0.
+__device__ __forceinline__ float exp_taylor7(float x)
+{
+    if (x > 88.0f)
+        return __int_as_float(0x7F800000);
+    if (x < -87.0f)
+        return 0.0f;
+    const float n = rintf(__fmul_rn(x, 1.44269502f));
+    float r = __fmaf_rn(-n, 0.693145751953125f, x);
+    r = __fmaf_rn(-n, 1.42860677e-06f, r);
+    float p = 0.000198412701f;
+    p = __fmaf_rn(p, r, 0.00138888892f);
+    p = __fmaf_rn(p, r, 0.00833333377f);
+    p = __fmaf_rn(p, r, 0.0416666679f);
+    p = __fmaf_rn(p, r, 0.166666672f);
+    p = __fmaf_rn(p, r, 0.5f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    return __fmul_rn(p, __int_as_float(((int)n + 127) << 23));
+}
+
+// h = BF16(fl32(fl32(g * fl32(1 / fl32(1 + exp(-g)))) * u))
+__device__ __forceinline__ float swiglu_bf16(float g, float u)
+{
+    const float sg = __frcp_rn(__fadd_rn(1.0f, exp_taylor7(-g)));
+    return bf16_round(__fmul_rn(__fmul_rn(g, sg), u));
+}
+
+// Applies producer P to one 8-column segment v of a row: aux holds the 8 up
+// values (SwiGLU), rs the row's rstd and wc the 8 weights (RMSNorm).
+template <int P>
+__device__ __forceinline__ void apply_producer(float (&v)[8], const uint4 &aux, float rs, const float (&wc)[8])
+{
+    if (P == kProduceRms) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            v[k] = bf16_round(__fmul_rn(__fmul_rn(v[k], rs), wc[k]));
+    } else if (P == kProduceSwiglu) {
+        float u[8];
+        unpack8(aux, u);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            v[k] = swiglu_bf16(v[k], u[k]);
+    }
+}
+
+// the 8 RMSNorm weights of columns col .. col+7 (zeros for other producers)
+template <int P>
+__device__ __forceinline__ void load_weights8(const ActQuantArgs &a, int64_t col, float (&wc)[8])
+{
+    if (P == kProduceRms) {
+        unpack8(__ldg(reinterpret_cast<const uint4 *>(a.w + col)), wc);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            wc[k] = 0.0f;
+    }
+}
+
+// The thread's 8x8 block with the producer applied (rows >= cnt give +0):
+// all loads are issued before any arithmetic.
+template <int P>
+__device__ __forceinline__ void load_block_produced(const ActQuantArgs &a, int64_t row0, int64_t col0, int cnt,
+                                                    int rg, int cc, float (&v)[8][8])
+{
+    if (P == kProducePlain) {
+        load_block(a.x, a.ldx, row0, col0, cnt, rg, cc, v);
+        return;
+    }
+    uint4 raw[8], aux[8];
+    float rs[8], wc[8];
+    load_weights8<P>(a, col0 + cc * 8, wc);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = rg * 8 + i;
+        const bool in = r < cnt;
+        raw[i] = in ? ldg_stream(a.x + (row0 + r) * a.ldx + col0 + cc * 8) : make_uint4(0, 0, 0, 0);
+        aux[i] = (P == kProduceSwiglu && in) ? ldg_stream(a.up + (row0 + r) * a.ldup + col0 + cc * 8)
+                                             : make_uint4(0, 0, 0, 0);
+        rs[i] = (P == kProduceRms && in) ? __ldg(a.rstd + row0 + r) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        unpack8(raw[i], v[i]);
+        apply_producer<P>(v[i], aux[i], rs[i], wc);
+    }
+}
+
+// one produced 8-column segment of row `row` (zeros when !in)
+template <int P>
+__device__ __forceinline__ void load_row8_produced(const ActQuantArgs &a, int64_t row, int64_t col, bool in,
+                                                   float (&v)[8])
+{
+    unpack8(in ? ldg_stream(a.x + row * a.ldx + col) : make_uint4(0, 0, 0, 0), v);
+    if (P != kProducePlain) {
+        float wc[8];
+        load_weights8<P>(a, col, wc);
+        const uint4 aux =
+            (P == kProduceSwiglu && in) ? ldg_stream(a.up + row * a.ldup + col) : make_uint4(0, 0, 0, 0);
+        const float rs = (P == kProduceRms && in) ? __ldg(a.rstd + row) : 0.0f;
+        apply_producer<P>(v, aux, rs, wc);
+    }
+}
+
 __device__ __forceinline__ float absmax8(const float (&v)[8])
 {
     float m = fabsf(v[0]);
@@ -286,6 +407,7 @@ __device__ __forceinline__ void store_tileT(const uint8_t *tileT, uint8_t *qc, i
 
 // The act tile again, element by element, for any scale (zero groups, scales
 // below 2^-96).  Reloads its inputs; scales come from shared memory.
+template <int P>
 __device__ __noinline__ void quant_act_tile_general(const ActQuantArgs &a, int64_t t0, int cnt, int64_t p0,
                                                     int64_t c0, bool row, bool col, const float *scS,
                                                     const float *scR, uint8_t *tileT)
@@ -294,7 +416,7 @@ __device__ __noinline__ void quant_act_tile_general(const ActQuantArgs &a, int64
     for (int i = 0; i < 8; ++i) {
         const int r = rg * 8 + i;
         float v[8];
-        unpack8(r < cnt ? ldg_stream(a.x + (t0 + r) * a.ldx + c0 + cc * 8) : make_uint4(0, 0, 0, 0), v);
+        load_row8_produced<P>(a, t0 + r, c0 + cc * 8, r < cnt, v);
         if (row && r < cnt) {
             float q[8];
 #pragma unroll
@@ -322,7 +444,7 @@ __device__ __noinline__ void quant_act_tile_general(const ActQuantArgs &a, int64
 // Activation / gradient quantizer (1x128 row copy + 128x1 column copy).
 // Each of the 256 scales of a tile (128 rows, 128 columns) is computed once,
 // by one thread, and published through shared memory.
-template <bool ROW, bool COL>
+template <bool ROW, bool COL, int P>
 __global__ void __launch_bounds__(kThreads, 2) k_quant_act(const __grid_constant__ ActQuantArgs a)
 {
     __shared__ __align__(16) float redR[16][132]; // row partial maxima [column chunk][row]
@@ -347,7 +469,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_quant_act(const __grid_constant
     const int64_t t0 = grp.t0, p0 = grp.p0;
 
     float v[8][8];
-    load_block(a.x, a.ldx, t0, c0, cnt, rg, cc, v);
+    load_block_produced<P>(a, t0, c0, cnt, rg, cc, v);
 
     // ---- partial maxima
     if (ROW) {
@@ -405,7 +527,7 @@ __global__ void __launch_bounds__(kThreads, 2) k_quant_act(const __grid_constant
     }
     __syncthreads();
     if (special) { // a zero or tiny scale somewhere in the tile (rare): slow, general path
-        quant_act_tile_general(a, t0, cnt, p0, c0, ROW, COL, &scS[0][0], &scR[0][0], tileT);
+        quant_act_tile_general<P>(a, t0, cnt, p0, c0, ROW, COL, &scS[0][0], &scR[0][0], tileT);
         return;
     }
 
@@ -448,6 +570,45 @@ __global__ void __launch_bounds__(kThreads, 2) k_quant_act(const __grid_constant
         __syncthreads();
         store_tileT(tileT, a.q_col, a.ldq_col, c0, p0);
     }
+}
+
+// RMSNorm statistics, one warp per row.  Lane l sums the 128-column groups
+// l, l + 32, ... (each left to right by fma, 16 loads in flight); the group
+// sums are then added left to right by every lane through shuffles, so the
+// binary32 result follows one fixed order: rstd = 1 / sqrt(total / c + eps).
+__global__ void __launch_bounds__(256) k_rms_rstd(const uint16_t *__restrict__ x, int64_t n, int64_t c,
+                                                  int64_t ldx, float eps, float *__restrict__ rstd)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= n)
+        return;
+    const int groups = (int)(c >> 7);
+    const uint16_t *xr = x + row * ldx;
+    float total = 0.0f;
+    for (int g0 = 0; g0 < groups; g0 += 32) {
+        const int g = g0 + lane;
+        float part = 0.0f;
+        if (g < groups) {
+            uint4 raw[16];
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+                raw[k] = __ldg(reinterpret_cast<const uint4 *>(xr + (int64_t)g * 128 + k * 8));
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                float v[8];
+                unpack8(raw[k], v);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    part = __fmaf_rn(v[j], v[j], part);
+            }
+        }
+        const int live = min(32, groups - g0);
+        for (int j = 0; j < live; ++j)
+            total = __fadd_rn(total, __shfl_sync(0xFFFFFFFFu, part, j));
+    }
+    if (lane == 0)
+        rstd[row] = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(total, (float)c), eps)));
 }
 
 // 8x8 byte transpose: in[i] holds bytes (row i, cols 0..7); out[j] holds
@@ -892,17 +1053,58 @@ int64_t groups_upper_bound(int64_t n, const int64_t *seg, int nseg)
 
 } // namespace
 
+namespace {
+
+template <int P>
+void launch_quant_act_p(const ActQuantArgs &a, dim3 grid, cudaStream_t st)
+{
+    if (a.q_row && a.q_col)
+        k_quant_act<true, true, P><<<grid, kThreads, 0, st>>>(a);
+    else if (a.q_row)
+        k_quant_act<true, false, P><<<grid, kThreads, 0, st>>>(a);
+    else
+        k_quant_act<false, true, P><<<grid, kThreads, 0, st>>>(a);
+}
+
+} // namespace
+
 cudaError_t launch_quant_act(const ActQuantArgs &a, cudaStream_t st)
 {
     if (a.n == 0 || (!a.q_row && !a.q_col))
         return cudaSuccess;
     dim3 grid((unsigned)groups_upper_bound(a.n, a.seg, a.nseg), (unsigned)(a.c / 128));
-    if (a.q_row && a.q_col)
-        k_quant_act<true, true><<<grid, kThreads, 0, st>>>(a);
-    else if (a.q_row)
-        k_quant_act<true, false><<<grid, kThreads, 0, st>>>(a);
-    else
-        k_quant_act<false, true><<<grid, kThreads, 0, st>>>(a);
+    switch (a.producer) {
+    case kProducePlain:
+        launch_quant_act_p<kProducePlain>(a, grid, st);
+        break;
+    case kProduceRms:
+        if (!a.w || !a.rstd)
+            return cudaErrorInvalidValue;
+        launch_quant_act_p<kProduceRms>(a, grid, st);
+        break;
+    case kProduceSwiglu:
+        if (!a.up)
+            return cudaErrorInvalidValue;
+        launch_quant_act_p<kProduceSwiglu>(a, grid, st);
+        break;
+    default:
+        return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_rms_rstd(const uint16_t *x, int64_t n, int64_t c, int64_t ldx, float eps, float *rstd,
+                            cudaStream_t st)
+{
+    if (n == 0)
+        return cudaSuccess;
+    if (c <= 0 || c % 128 != 0 || c > 32768)
+        return cudaErrorInvalidValue;
+    constexpr int kWarps = 8;
+    const int64_t blocks = (n + kWarps - 1) / kWarps;
+    if (blocks > 2147483647)
+        return cudaErrorInvalidValue;
+    k_rms_rstd<<<(unsigned)blocks, kWarps * 32, 0, st>>>(x, n, c, ldx, eps, rstd);
     return cudaGetLastError();
 }
 

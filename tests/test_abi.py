@@ -81,5 +81,20 @@ def test_validation_happens_before_cuda(L):
     assert L.jetq_selftest_bounded_wait(ctypes.c_uint64(2_000_000_000), fake, None) == 1
     assert L.jetq_selftest_bounded_wait(ctypes.c_uint64(50_000_000), None, None) == 1
     assert L.jetq_selftest_bounded_wait(ctypes.c_uint64(50_000_000), P(4100), None) == 3
+    # fused producers: c above 32768 (RMSNorm statistics), eps out of range, missing rstd,
+    # misaligned weight; SwiGLU up stride below c, misaligned up
+    F = ctypes.c_float
+    assert L.jetq_quant_act_1x128_rmsnorm(fake, 4, 32896, 32896, fake, F(1e-6), fake, fake, fake, None, None, 0,
+                                          None, 0, None) == 2
+    assert L.jetq_quant_act_1x128_rmsnorm(fake, 4, 128, 128, fake, F(-1.0), fake, fake, fake, None, None, 0,
+                                          None, 0, None) == 1
+    assert L.jetq_quant_act_1x128_rmsnorm(fake, 4, 128, 128, fake, F(1e-6), None, fake, fake, None, None, 0,
+                                          None, 0, None) == 1
+    assert L.jetq_quant_act_1x128_rmsnorm(fake, 4, 128, 128, P(4098), F(1e-6), fake, fake, fake, None, None, 0,
+                                          None, 0, None) == 3
+    assert L.jetq_quant_act_1x128_swiglu(fake, fake, 4, 256, 256, 128, fake, fake, None, None, 0, None, 0,
+                                         None) == 2
+    assert L.jetq_quant_act_1x128_swiglu(fake, P(4104), 4, 128, 128, 128, fake, fake, None, None, 0, None, 0,
+                                         None) == 3
     # MX: columns not a multiple of 128
     assert L.jetq_quant_mx32(fake, 4, 96, 96, fake, fake, None, None, 0, None, 0, None) == 2
