@@ -118,7 +118,7 @@ jetq_status jetq_check_device_error(void *stream)
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned word = 0;
     if (gemm_read_and_clear_error(st, &word) != cudaSuccess || gemm_mx_read_and_clear_error(st, &word) != cudaSuccess ||
-        gemm_decode_read_and_clear_error(st, &word) != cudaSuccess)
+        gemm_decode_read_and_clear_error(st, &word) != cudaSuccess || quant_read_and_clear_error(st, &word) != cudaSuccess)
         return JETQ_ERR_CUDA;
     return word ? JETQ_ERR_TIMEOUT : JETQ_OK;
 }

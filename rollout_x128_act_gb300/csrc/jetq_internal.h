@@ -169,6 +169,13 @@ cudaError_t gemm_decode_read_and_clear_error(cudaStream_t st, unsigned *out);
 
 cudaError_t gemm_read_and_clear_error(cudaStream_t st, unsigned *out);
 
+// TMA descriptor for a BF16 matrix [rows x cols], row stride ld elements:
+// 128 x 128 boxes (32 KB, rows of 256 bytes, no swizzle), zero fill out of bounds.
+cudaError_t make_bf16_tile_map(CUtensorMap *map, const void *base, int64_t cols, int64_t rows, int64_t ld);
+
+// device error word of the quantizers (bounded waits of the TMA-fed kernels)
+cudaError_t quant_read_and_clear_error(cudaStream_t st, unsigned *out);
+
 // TMA descriptor for a K-major byte matrix [rows x k_extent], row stride ld,
 // boxes of 128 bytes x box_rows (x kb_per_box consecutive K-blocks, as a 3-D
 // map, when kb_per_box > 1), 128-byte swizzle, zero fill out of bounds.

@@ -24,8 +24,12 @@
 #include <cuda_runtime.h>
 
 #include "jetq_internal.h"
+#include "ptx.cuh"
 
 namespace jetq {
+
+__device__ unsigned g_quant_error;
+
 namespace {
 
 constexpr int kThreads = 256;
@@ -47,6 +51,17 @@ __device__ __forceinline__ void unpack8(const uint4 &u, float (&v)[8])
     for (int k = 0; k < 4; ++k) {
         v[2 * k] = __uint_as_float(w[k] << 16);
         v[2 * k + 1] = __uint_as_float(w[k] & 0xFFFF0000u);
+    }
+}
+
+// the same 8 values negated (sign bit flipped: exact)
+__device__ __forceinline__ void unpack8_neg(const uint4 &u, float (&v)[8])
+{
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        v[2 * k] = __uint_as_float((w[k] << 16) ^ 0x80000000u);
+        v[2 * k + 1] = __uint_as_float((w[k] & 0xFFFF0000u) ^ 0x80000000u);
     }
 }
 
@@ -307,50 +322,65 @@ __device__ __forceinline__ float swiglu_bf16(float g, float u)
     return bf16_round(__fmul_rn(__fmul_rn(g, sg), u));
 }
 
-// Applies producer P to one 8-column segment v of a row: aux holds the 8 up
-// values (SwiGLU), rs the row's rstd and wc the 8 weights (RMSNorm).
-template <int P>
-__device__ __forceinline__ void apply_producer(float (&v)[8], const uint4 &aux, float rs, const float (&wc)[8])
+// Producer P on one loaded 8-column segment of a row.  With NEG the result is
+// negated (the fast tile path works on -y, see quant_tile): the negation is
+// folded into the unpacking of x, of the RMSNorm weights or of the SwiGLU up
+// values, so it costs nothing.  aux holds the 8 up values (SwiGLU), rs the
+// row's rstd and w8 the 8 weights, already carrying the NEG sign (RMSNorm).
+template <int P, bool NEG>
+__device__ __forceinline__ void produce8(const uint4 &raw, const uint4 &aux, float rs, const float (&w8)[8],
+                                         float (&v)[8])
 {
-    if (P == kProduceRms) {
+    if (P == kProducePlain) {
+        if (NEG)
+            unpack8_neg(raw, v);
+        else
+            unpack8(raw, v);
+    } else if (P == kProduceRms) {
+        float x[8];
+        unpack8(raw, x);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-            v[k] = bf16_round(__fmul_rn(__fmul_rn(v[k], rs), wc[k]));
-    } else if (P == kProduceSwiglu) {
-        float u[8];
-        unpack8(aux, u);
+            v[k] = bf16_round(__fmul_rn(__fmul_rn(x[k], rs), w8[k]));
+    } else {
+        float gt[8], u[8];
+        unpack8(raw, gt);
+        if (NEG)
+            unpack8_neg(aux, u);
+        else
+            unpack8(aux, u);
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-            v[k] = swiglu_bf16(v[k], u[k]);
+            v[k] = swiglu_bf16(gt[k], u[k]);
     }
 }
 
-// the 8 RMSNorm weights of columns col .. col+7 (zeros for other producers)
-template <int P>
-__device__ __forceinline__ void load_weights8(const ActQuantArgs &a, int64_t col, float (&wc)[8])
+// the 8 RMSNorm weights of columns col .. col+7, negated with NEG (zeros for other producers)
+template <int P, bool NEG>
+__device__ __forceinline__ void load_weights8(const ActQuantArgs &a, int64_t col, float (&w8)[8])
 {
     if (P == kProduceRms) {
-        unpack8(__ldg(reinterpret_cast<const uint4 *>(a.w + col)), wc);
+        const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(a.w + col));
+        if (NEG)
+            unpack8_neg(raw, w8);
+        else
+            unpack8(raw, w8);
     } else {
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-            wc[k] = 0.0f;
+            w8[k] = 0.0f;
     }
 }
 
-// The thread's 8x8 block with the producer applied (rows >= cnt give +0):
+// The thread's 8x8 block of -y from global memory (rows >= cnt give zeros):
 // all loads are issued before any arithmetic.
 template <int P>
-__device__ __forceinline__ void load_block_produced(const ActQuantArgs &a, int64_t row0, int64_t col0, int cnt,
-                                                    int rg, int cc, float (&v)[8][8])
+__device__ __forceinline__ void load_block_neg(const ActQuantArgs &a, int64_t row0, int64_t col0, int cnt, int rg,
+                                               int cc, float (&nv)[8][8])
 {
-    if (P == kProducePlain) {
-        load_block(a.x, a.ldx, row0, col0, cnt, rg, cc, v);
-        return;
-    }
     uint4 raw[8], aux[8];
-    float rs[8], wc[8];
-    load_weights8<P>(a, col0 + cc * 8, wc);
+    float rs[8], w8[8];
+    load_weights8<P, true>(a, col0 + cc * 8, w8);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int r = rg * 8 + i;
@@ -361,26 +391,21 @@ __device__ __forceinline__ void load_block_produced(const ActQuantArgs &a, int64
         rs[i] = (P == kProduceRms && in) ? __ldg(a.rstd + row0 + r) : 0.0f;
     }
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        unpack8(raw[i], v[i]);
-        apply_producer<P>(v[i], aux[i], rs[i], wc);
-    }
+    for (int i = 0; i < 8; ++i)
+        produce8<P, true>(raw[i], aux[i], rs[i], w8, nv[i]);
 }
 
-// one produced 8-column segment of row `row` (zeros when !in)
+// one produced 8-column segment of row `row`, sign as is (zeros when !in)
 template <int P>
 __device__ __forceinline__ void load_row8_produced(const ActQuantArgs &a, int64_t row, int64_t col, bool in,
                                                    float (&v)[8])
 {
-    unpack8(in ? ldg_stream(a.x + row * a.ldx + col) : make_uint4(0, 0, 0, 0), v);
-    if (P != kProducePlain) {
-        float wc[8];
-        load_weights8<P>(a, col, wc);
-        const uint4 aux =
-            (P == kProduceSwiglu && in) ? ldg_stream(a.up + row * a.ldup + col) : make_uint4(0, 0, 0, 0);
-        const float rs = (P == kProduceRms && in) ? __ldg(a.rstd + row) : 0.0f;
-        apply_producer<P>(v, aux, rs, wc);
-    }
+    float w8[8];
+    load_weights8<P, false>(a, col, w8);
+    const uint4 raw = in ? ldg_stream(a.x + row * a.ldx + col) : make_uint4(0, 0, 0, 0);
+    const uint4 aux = (P == kProduceSwiglu && in) ? ldg_stream(a.up + row * a.ldup + col) : make_uint4(0, 0, 0, 0);
+    const float rs = (P == kProduceRms && in) ? __ldg(a.rstd + row) : 0.0f;
+    produce8<P, false>(raw, aux, rs, w8, v);
 }
 
 __device__ __forceinline__ float absmax8(const float (&v)[8])
@@ -441,63 +466,70 @@ __device__ __noinline__ void quant_act_tile_general(const ActQuantArgs &a, int64
     }
 }
 
-// Activation / gradient quantizer (1x128 row copy + 128x1 column copy).
-// Each of the 256 scales of a tile (128 rows, 128 columns) is computed once,
-// by one thread, and published through shared memory.
-template <bool ROW, bool COL, int P>
-__global__ void __launch_bounds__(kThreads, 2) k_quant_act(const __grid_constant__ ActQuantArgs a)
-{
-    __shared__ __align__(16) float redR[16][132]; // row partial maxima [column chunk][row]
-    __shared__ __align__(16) float redC[8][128];  // column partial maxima [warp][column]
-    __shared__ __align__(16) float scS[2][128];   // scales: [0] rows, [1] columns
-    __shared__ __align__(16) float scR[2][128];   // reciprocals
-    __shared__ __align__(16) uint8_t tileT[128 * 128];
-    __shared__ Group grp;
-    __shared__ int special; // some scale needs the general path
+// Shared working set of one 128 x 128 activation tile.
+struct TileSmem {
+    uint8_t tileT[128 * 128]; // transposed column codes (swizzled)
+    float redR[16][132];      // row partial maxima [column chunk][row]
+    float redC[8][128];       // column partial maxima [warp][column]
+    float4 rowSc[128];        // per row: (S, S, -1/S, -1/S), packed operand pairs
+    float colS[128];          // per column: S
+    float colNR[128];         // per column: -1/S
+    float scS[2][128];        // S and 1/S for the general path: [0] rows, [1] columns
+    float scR[2][128];
+};
 
+// Both quotients of a pair, from the negated values nx = -x:
+// q0 = RN(x * r), e' = S*q0 - x (exact by FMA), q1 = RN(q0 - e' * r), which is
+// the residual-corrected quotient of the file header with e' = -e.  Working on
+// -x also gives zero quotients the sign of x: x = -0 yields -0 + -0 = -0.
+__device__ __forceinline__ float2 quotient2_neg(float2 nx, float2 S, float2 NR)
+{
+    const float2 q0 = __fmul2_rn(nx, NR);
+    const float2 e = __ffma2_rn(S, q0, nx);
+    return __ffma2_rn(e, NR, q0);
+}
+
+// The tile computation both activation-quantizer kernels share, from the
+// thread's 8x8 block of negated values (rows >= cnt zero).  Each of the 256
+// scales of the tile is computed once, by one thread, and published through
+// shared memory.  after_sync() runs once every thread holds its block in
+// registers (its input buffer may then be refilled).
+template <bool ROW, bool COL, int P, typename AfterSync>
+__device__ __forceinline__ void quant_tile(const ActQuantArgs &a, TileSmem &ts, float (&nv)[8][8], int64_t t0,
+                                           int cnt, int64_t p0, int64_t c0, AfterSync after_sync)
+{
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int rg = t >> 4, cc = t & 15;
-    const int64_t c0 = (int64_t)blockIdx.y * 128;
-
-    if (t == 0)
-        special = 0;
-    map_group(blockIdx.x, a.n, a.seg, a.nseg, &grp);
-    __syncthreads();
-    const int cnt = grp.cnt;
-    if (cnt == 0)
-        return;
-    const int64_t t0 = grp.t0, p0 = grp.p0;
-
-    float v[8][8];
-    load_block_produced<P>(a, t0, c0, cnt, rg, cc, v);
 
     // ---- partial maxima
     if (ROW) {
         float rm[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i)
-            rm[i] = absmax8(v[i]);
-        *reinterpret_cast<float4 *>(&redR[cc][rg * 8]) = make_float4(rm[0], rm[1], rm[2], rm[3]);
-        *reinterpret_cast<float4 *>(&redR[cc][rg * 8 + 4]) = make_float4(rm[4], rm[5], rm[6], rm[7]);
+            rm[i] = absmax8(nv[i]);
+        *reinterpret_cast<float4 *>(&ts.redR[cc][rg * 8]) = make_float4(rm[0], rm[1], rm[2], rm[3]);
+        *reinterpret_cast<float4 *>(&ts.redR[cc][rg * 8 + 4]) = make_float4(rm[4], rm[5], rm[6], rm[7]);
     }
     if (COL) {
         float cm[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
-            float m = fabsf(v[0][j]);
+            float m = fabsf(nv[0][j]);
 #pragma unroll
             for (int i = 1; i < 8; ++i)
-                m = fmaxf(m, fabsf(v[i][j]));
+                m = fmaxf(m, fabsf(nv[i][j]));
             cm[j] = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
         }
         if (lane < 16) {
-            *reinterpret_cast<float4 *>(&redC[warp][cc * 8]) = make_float4(cm[0], cm[1], cm[2], cm[3]);
-            *reinterpret_cast<float4 *>(&redC[warp][cc * 8 + 4]) = make_float4(cm[4], cm[5], cm[6], cm[7]);
+            *reinterpret_cast<float4 *>(&ts.redC[warp][cc * 8]) = make_float4(cm[0], cm[1], cm[2], cm[3]);
+            *reinterpret_cast<float4 *>(&ts.redC[warp][cc * 8 + 4]) = make_float4(cm[4], cm[5], cm[6], cm[7]);
         }
     }
     __syncthreads();
+    after_sync();
 
     // ---- one scale per thread: threads 0..127 rows, 128..255 columns
+    int special = 0;
     {
         const bool is_row = t < 128;
         const int k = t & 127;
@@ -506,71 +538,223 @@ __global__ void __launch_bounds__(kThreads, 2) k_quant_act(const __grid_constant
             if (is_row) {
 #pragma unroll
                 for (int w = 0; w < 16; ++w)
-                    m = fmaxf(m, redR[w][k]);
+                    m = fmaxf(m, ts.redR[w][k]);
             } else {
 #pragma unroll
                 for (int w = 0; w < 8; ++w)
-                    m = fmaxf(m, redC[w][k]);
+                    m = fmaxf(m, ts.redC[w][k]);
             }
             const Fp32Scale sc = make_scale(m);
-            scS[is_row ? 0 : 1][k] = sc.s;
-            scR[is_row ? 0 : 1][k] = sc.r;
-            if (sc.zero || sc.slow)
-                special = 1;
+            ts.scS[is_row ? 0 : 1][k] = sc.s;
+            ts.scR[is_row ? 0 : 1][k] = sc.r;
+            special = (sc.zero || sc.slow) && (!is_row || k < cnt); // rows past cnt are never stored
             if (is_row) {
+                ts.rowSc[k] = make_float4(sc.s, sc.s, -sc.r, -sc.r);
                 if (k < cnt)
                     a.s_row[(c0 >> 7) * a.n + t0 + k] = sc.s;
             } else {
+                ts.colS[k] = sc.s;
+                ts.colNR[k] = -sc.r;
                 a.s_col[(p0 >> 7) * a.c + c0 + k] = sc.s;
             }
         }
     }
-    __syncthreads();
-    if (special) { // a zero or tiny scale somewhere in the tile (rare): slow, general path
-        quant_act_tile_general<P>(a, t0, cnt, p0, c0, ROW, COL, &scS[0][0], &scR[0][0], tileT);
+    if (__syncthreads_or(special)) { // a zero or tiny scale somewhere in the tile (rare): slow, general path
+        quant_act_tile_general<P>(a, t0, cnt, p0, c0, ROW, COL, &ts.scS[0][0], &ts.scR[0][0], ts.tileT);
         return;
     }
 
-    // ---- row copy: codes straight to global (16 lanes write one 128-byte row)
-    if (ROW) {
+    // ---- row codes straight to global (16 lanes write one 128-byte row); the
+    // column quotients replace the block in place, row by row
+    float cs[8], cnr[8];
+    if (COL) {
+        *reinterpret_cast<float4 *>(cs) = *reinterpret_cast<const float4 *>(&ts.colS[cc * 8]);
+        *reinterpret_cast<float4 *>(cs + 4) = *reinterpret_cast<const float4 *>(&ts.colS[cc * 8 + 4]);
+        *reinterpret_cast<float4 *>(cnr) = *reinterpret_cast<const float4 *>(&ts.colNR[cc * 8]);
+        *reinterpret_cast<float4 *>(cnr + 4) = *reinterpret_cast<const float4 *>(&ts.colNR[cc * 8 + 4]);
+    }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int r = rg * 8 + i;
-            const float s = scS[0][r], rc = scR[0][r];
-            float si[8], ri[8];
+    for (int i = 0; i < 8; ++i) {
+        const int r = rg * 8 + i;
+        if (ROW) {
+            const float4 rs4 = ts.rowSc[r];
+            const float2 S2 = make_float2(rs4.x, rs4.y), NR2 = make_float2(rs4.z, rs4.w);
+            float q[8];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                si[k] = s;
-                ri[k] = rc;
+            for (int k = 0; k < 8; k += 2) {
+                const float2 q2 = quotient2_neg(make_float2(nv[i][k], nv[i][k + 1]), S2, NR2);
+                q[k] = q2.x;
+                q[k + 1] = q2.y;
             }
-            const uint2 codes = quant8_fast(v[i], si, ri);
             if (r < cnt)
-                *reinterpret_cast<uint2 *>(a.q_row + (t0 + r) * a.c + c0 + cc * 8) = codes;
+                *reinterpret_cast<uint2 *>(a.q_row + (t0 + r) * a.c + c0 + cc * 8) =
+                    make_uint2(cvt4(q[0], q[1], q[2], q[3]), cvt4(q[4], q[5], q[6], q[7]));
+        }
+        if (COL) {
+#pragma unroll
+            for (int k = 0; k < 8; k += 2) {
+                const float2 q2 = quotient2_neg(make_float2(nv[i][k], nv[i][k + 1]), make_float2(cs[k], cs[k + 1]),
+                                                make_float2(cnr[k], cnr[k + 1]));
+                nv[i][k] = q2.x;
+                nv[i][k + 1] = q2.y;
+            }
         }
     }
 
-    // ---- column copy: codes transposed through shared memory
+    // ---- column codes transposed through shared memory
     if (COL) {
-        float s8[8], r8[8];
-        *reinterpret_cast<float4 *>(s8) = *reinterpret_cast<const float4 *>(&scS[1][cc * 8]);
-        *reinterpret_cast<float4 *>(s8 + 4) = *reinterpret_cast<const float4 *>(&scS[1][cc * 8 + 4]);
-        *reinterpret_cast<float4 *>(r8) = *reinterpret_cast<const float4 *>(&scR[1][cc * 8]);
-        *reinterpret_cast<float4 *>(r8 + 4) = *reinterpret_cast<const float4 *>(&scR[1][cc * 8 + 4]);
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            float col[8], sj[8], rj[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                col[i] = v[i][j];
-                sj[i] = s8[j];
-                rj[i] = r8[j];
-            }
-            tileT_put(tileT, cc * 8 + j, rg, quant8_fast(col, sj, rj));
-        }
+        for (int j = 0; j < 8; ++j)
+            tileT_put(ts.tileT, cc * 8 + j, rg,
+                      make_uint2(cvt4(nv[0][j], nv[1][j], nv[2][j], nv[3][j]),
+                                 cvt4(nv[4][j], nv[5][j], nv[6][j], nv[7][j])));
         __syncthreads();
-        store_tileT(tileT, a.q_col, a.ldq_col, c0, p0);
+        store_tileT(ts.tileT, a.q_col, a.ldq_col, c0, p0);
     }
 }
+
+// Activation / gradient quantizer (1x128 row copy + 128x1 column copy), one
+// CTA per tile, inputs loaded straight to registers (the SwiGLU producer).
+template <bool ROW, bool COL, int P>
+__global__ void __launch_bounds__(kThreads, 2) k_quant_act(const __grid_constant__ ActQuantArgs a)
+{
+    __shared__ __align__(16) TileSmem ts;
+    __shared__ Group grp;
+
+    const int t = threadIdx.x, rg = t >> 4, cc = t & 15;
+    const int64_t c0 = (int64_t)blockIdx.y * 128;
+    map_group(blockIdx.x, a.n, a.seg, a.nseg, &grp);
+    __syncthreads();
+    const int cnt = grp.cnt;
+    if (cnt == 0)
+        return;
+    float nv[8][8];
+    load_block_neg<P>(a, grp.t0, c0, cnt, rg, cc, nv);
+    quant_tile<ROW, COL, P>(a, ts, nv, grp.t0, cnt, grp.p0, c0, [] {});
+}
+
+// ------------------------------------------------------------ TMA-fed activation quantizer
+//
+// The same tile computation in a persistent loop: each CTA walks tiles
+// blockIdx.x, blockIdx.x + gridDim.x, ...; warp 0 keeps the next tiles' BF16
+// input in flight with TMA (one 32 KB box per tile, a two-stage ring per CTA,
+// two CTAs per SM), so HBM sees requests while the previous tile is reduced,
+// quantized and stored.  A stage is refilled once every thread has moved its
+// 8x8 block into registers (the first barrier of the tile).
+
+constexpr int kPipeStages = 2;
+constexpr uint32_t kPipeTileBytes = 128 * 128 * 2;
+constexpr unsigned long long kQuantWaitLimitNs = 2000000000ull; // 2 s per wait
+constexpr unsigned kQuantErrTimeout = 1u;
+
+struct PipeSmem {
+    uint16_t stage[kPipeStages][128 * 128]; // BF16 input tiles, rows of 256 bytes
+    TileSmem ts;
+    Group grp[kPipeStages]; // the tile each stage holds
+    unsigned long long full[kPipeStages];
+    int issued[kPipeStages];
+    int abort;
+};
+constexpr size_t kPipeSmemBytes = sizeof(PipeSmem) + 1024;
+
+template <bool ROW, bool COL, int P>
+__global__ void __launch_bounds__(kThreads, 2)
+    k_quant_act_tma(const __grid_constant__ ActQuantArgs a, const __grid_constant__ CUtensorMap tmx,
+                    int64_t ngroups, int ncb)
+{
+    static_assert(P != kProduceSwiglu, "the TMA path stages one input tensor");
+    extern __shared__ uint8_t smem_raw[];
+    PipeSmem &sm = *reinterpret_cast<PipeSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int rg = t >> 4, cc = t & 15;
+    const int64_t total = ngroups * ncb;
+    unsigned *err = &g_quant_error;
+
+    // warp 0: map the CTA's k-th tile to its rows and start its load into stage k % kPipeStages
+    auto issue = [&](int64_t k) {
+        const int64_t T = blockIdx.x + k * (int64_t)gridDim.x;
+        if (T >= total || sm.abort)
+            return;
+        const int s = (int)(k % kPipeStages);
+        map_group(T / ncb, a.n, a.seg, a.nseg, &sm.grp[s]);
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t bar = ptx::smem_addr(&sm.full[s]);
+            sm.issued[s] += 1;
+            if (sm.grp[s].cnt > 0) {
+                ptx::mbar_arrive_expect_tx(bar, kPipeTileBytes);
+                ptx::tma_load_2d(ptx::smem_addr(sm.stage[s]), &tmx, bar, (int)((T % ncb) * 128), (int)sm.grp[s].t0);
+            } else {
+                ptx::mbar_arrive(bar);
+            }
+        }
+        __syncwarp();
+    };
+
+    if (t == 0) {
+        for (int s = 0; s < kPipeStages; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&sm.full[s]), 1);
+            sm.issued[s] = 0;
+        }
+        sm.abort = 0;
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0)
+            ptx::prefetch_tensormap(&tmx);
+        for (int s = 0; s < kPipeStages; ++s)
+            issue(s);
+    }
+
+    for (int64_t k = 0;; ++k) {
+        const int64_t T = blockIdx.x + k * (int64_t)gridDim.x;
+        if (T >= total)
+            break;
+        const int s = (int)(k % kPipeStages);
+        ptx::mbar_wait(ptx::smem_addr(&sm.full[s]), (uint32_t)((k / kPipeStages) & 1), &sm.abort, err,
+                       kQuantErrTimeout, kQuantWaitLimitNs);
+        const int cnt = sm.grp[s].cnt;
+        const int64_t t0 = sm.grp[s].t0, p0 = sm.grp[s].p0;
+        const int64_t c0 = (T % ncb) * 128;
+        if (cnt == 0) { // a padded group past the last segment
+            __syncthreads();
+            if (warp == 0)
+                issue(k + kPipeStages);
+            continue;
+        }
+
+        float nv[8][8];
+        {
+            float w8[8];
+            load_weights8<P, true>(a, c0 + cc * 8, w8);
+            const uint16_t *st = sm.stage[s];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = rg * 8 + i;
+                const bool in = r < cnt;
+                const uint4 raw = in ? *reinterpret_cast<const uint4 *>(st + r * 128 + cc * 8) : make_uint4(0, 0, 0, 0);
+                const float rs = (P == kProduceRms && in) ? __ldg(a.rstd + t0 + r) : 0.0f;
+                produce8<P, true>(raw, make_uint4(0, 0, 0, 0), rs, w8, nv[i]);
+            }
+        }
+        ptx::fence_proxy_async_smem(); // the stage's generic reads before the next TMA write into it
+        quant_tile<ROW, COL, P>(a, sm.ts, nv, t0, cnt, p0, c0, [&] {
+            if (warp == 0)
+                issue(k + kPipeStages);
+        });
+    }
+
+    // after a timed-out wait no new loads were started; wait (bounded) for the
+    // ones still in flight before the CTA's shared memory is released
+    if (t == 0 && sm.abort) {
+        for (int s = 0; s < kPipeStages; ++s)
+            if (sm.issued[s] > 0)
+                ptx::mbar_wait(ptx::smem_addr(&sm.full[s]), (uint32_t)((sm.issued[s] - 1) & 1), &sm.abort, err,
+                               kQuantErrTimeout, kQuantWaitLimitNs, false);
+    }
+}
+
 
 // RMSNorm statistics, one warp per row.  Lane l sums the 128-column groups
 // l, l + 32, ... (each left to right by fma, 16 loads in flight); the group
@@ -1055,6 +1239,46 @@ int64_t groups_upper_bound(int64_t n, const int64_t *seg, int nseg)
 
 namespace {
 
+template <bool ROW, bool COL, int P>
+cudaError_t launch_quant_act_tma(const ActQuantArgs &a, const CUtensorMap &map, int64_t ngroups, int ncb,
+                                 cudaStream_t st)
+{
+    auto kern = k_quant_act_tma<ROW, COL, P>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (configured_device != dev) {
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPipeSmemBytes)) !=
+            cudaSuccess)
+            return e;
+        configured_device = dev;
+    }
+    const int64_t tiles = ngroups * ncb;
+    const int64_t cap = 2 * (int64_t)sm_count();
+    kern<<<(unsigned)(tiles < cap ? tiles : cap), kThreads, kPipeSmemBytes, st>>>(a, map, ngroups, ncb);
+    return cudaGetLastError();
+}
+
+template <int P>
+cudaError_t launch_quant_act_tma_p(const ActQuantArgs &a, cudaStream_t st)
+{
+    if (a.n > 2147483647 - 128 || a.c > 2147483647)
+        return cudaErrorInvalidValue; // TMA coordinates are 32-bit
+    CUtensorMap map;
+    cudaError_t e = make_bf16_tile_map(&map, a.x, a.c, a.n, a.ldx);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t ngroups = groups_upper_bound(a.n, a.seg, a.nseg);
+    const int ncb = (int)(a.c / 128);
+    if (a.q_row && a.q_col)
+        return launch_quant_act_tma<true, true, P>(a, map, ngroups, ncb, st);
+    if (a.q_row)
+        return launch_quant_act_tma<true, false, P>(a, map, ngroups, ncb, st);
+    return launch_quant_act_tma<false, true, P>(a, map, ngroups, ncb, st);
+}
+
 template <int P>
 void launch_quant_act_p(const ActQuantArgs &a, dim3 grid, cudaStream_t st)
 {
@@ -1075,13 +1299,11 @@ cudaError_t launch_quant_act(const ActQuantArgs &a, cudaStream_t st)
     dim3 grid((unsigned)groups_upper_bound(a.n, a.seg, a.nseg), (unsigned)(a.c / 128));
     switch (a.producer) {
     case kProducePlain:
-        launch_quant_act_p<kProducePlain>(a, grid, st);
-        break;
+        return launch_quant_act_tma_p<kProducePlain>(a, st);
     case kProduceRms:
         if (!a.w || !a.rstd)
             return cudaErrorInvalidValue;
-        launch_quant_act_p<kProduceRms>(a, grid, st);
-        break;
+        return launch_quant_act_tma_p<kProduceRms>(a, st);
     case kProduceSwiglu:
         if (!a.up)
             return cudaErrorInvalidValue;
@@ -1106,6 +1328,24 @@ cudaError_t launch_rms_rstd(const uint16_t *x, int64_t n, int64_t c, int64_t ldx
         return cudaErrorInvalidValue;
     k_rms_rstd<<<(unsigned)blocks, kWarps * 32, 0, st>>>(x, n, c, ldx, eps, rstd);
     return cudaGetLastError();
+}
+
+cudaError_t quant_read_and_clear_error(cudaStream_t st, unsigned *out)
+{
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_quant_error, sizeof v, 0, cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess)
+        e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess)
+        return e;
+    *out |= v;
+    if (v) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbolAsync(g_quant_error, &zero, sizeof zero, 0, cudaMemcpyHostToDevice, st);
+        if (e == cudaSuccess)
+            e = cudaStreamSynchronize(st);
+    }
+    return e;
 }
 
 cudaError_t launch_quant_weight(const WeightQuantArgs &a, cudaStream_t st)
