@@ -108,7 +108,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS, A_STRIDE_MAX, KBP>;
     constexpr int SB = C::kSbSlots;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *tiles_a = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *tiles_a = ptx::align_smem<1024>(smem_raw);
     uint8_t *tiles_b = tiles_a + C::kARegion;
     float *sb_ring = reinterpret_cast<float *>(tiles_b + (size_t)STAGES * KBP * C::kBBytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sb_ring) + C::kSbBytes);

@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(256, 1)
     constexpr int NG = C::NG;
     constexpr int SL = C::kSlots;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *tiles_w = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *tiles_w = ptx::align_smem<1024>(smem_raw);
     uint8_t *tiles_x = tiles_w + (size_t)STAGES * KBP * C::kWBytes;
     float *srow = reinterpret_cast<float *>(tiles_x + (size_t)STAGES * KBP * C::kXBytes);
     uint64_t *bars = reinterpret_cast<uint64_t *>(srow + SL * NB);

@@ -82,7 +82,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
 {
     using C = MxCfg<BN, EPI_WARPS, STAGES>;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *tiles = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    uint8_t *tiles = ptx::align_smem<1024>(smem_raw);
     uint8_t *sf = tiles + (size_t)STAGES * C::kStage; // STAGES x (SFA atom, SFB atoms)
     uint64_t *bars = reinterpret_cast<uint64_t *>(sf + (size_t)STAGES * C::kSfStage);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kBars);

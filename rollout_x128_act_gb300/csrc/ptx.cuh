@@ -13,6 +13,17 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p)
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// The dynamic shared-memory base rounded up to ALIGN bytes by pointer
+// arithmetic on the shared array itself, so that the compiler still knows the
+// result is a shared address (plain accesses become shared-memory loads and
+// stores, not generic ones).
+template <uint32_t ALIGN>
+__device__ __forceinline__ uint8_t *align_smem(uint8_t *raw)
+{
+    const uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(raw));
+    return raw + ((ALIGN - (a & (ALIGN - 1))) & (ALIGN - 1));
+}
+
 __device__ __forceinline__ uint64_t globaltimer()
 {
     uint64_t t;

@@ -664,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 {
     static_assert(P != kProduceSwiglu, "the TMA path stages one input tensor");
     extern __shared__ uint8_t smem_raw[];
-    PipeSmem &sm = *reinterpret_cast<PipeSmem *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+    PipeSmem &sm = *reinterpret_cast<PipeSmem *>(ptx::align_smem<1024>(smem_raw));
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int rg = t >> 4, cc = t & 15;
     const int64_t total = ngroups * ncb;
