@@ -42,6 +42,7 @@
 #include "ptx.cuh"
 #include "sched.cuh"
 
+
 namespace jetq {
 
 __device__ unsigned g_gemm_error;
@@ -91,8 +92,10 @@ struct Cfg {
     static constexpr int kSbSlots = 4;                 // column-scale ring (WGrad)
     static constexpr int kBars = 2 * STAGES + 2 * TMEM_BUFS + 2 * kSbSlots + 1;
     static constexpr size_t kSbBytes = (size_t)kSbSlots * BN * 4;
-    static constexpr size_t kSmem =
-        1024 + (size_t)kARegion + (size_t)STAGES * KBP * kBBytes + kSbBytes + 1024 + sizeof(GroupTables);
+    // output staging: 32 rows x 64 bytes per epilogue warp, for coalesced stores
+    static constexpr size_t kStageOutBytes = (size_t)EPI_WARPS * 2048;
+    static constexpr size_t kSmem = 1024 + (size_t)kARegion + (size_t)STAGES * KBP * kBBytes + kSbBytes + 1024 +
+                                    sizeof(GroupTables) + 128 + kStageOutBytes;
     static_assert(TMEM_BUFS * BN <= kTmemCols, "TMEM buffers exceed 512 columns");
     static_assert(EPI_WARPS % 4 == 0 && kCols % 32 == 0, "epilogue split");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
@@ -115,6 +118,8 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
     GroupTables *gt = reinterpret_cast<GroupTables *>(reinterpret_cast<uint8_t *>(bars) + 1024);
+    uint8_t *stage_out = reinterpret_cast<uint8_t *>(gt + 1);
+    stage_out += (128u - (ptx::smem_addr(stage_out) & 127u)) & 127u;
 
     const uint32_t bar0 = ptx::smem_addr(bars);
     auto full = [&](int s) { return bar0 + 8u * s; };
@@ -136,11 +141,11 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
         }
         for (int b = 0; b < TMEM_BUFS; ++b) {
             ptx::mbar_init(tfull(b), 1);
-            ptx::mbar_init(tempty(b), EPI_WARPS);
+            ptx::mbar_init(tempty(b), EPI_WARPS * 32); // every epilogue thread arrives
         }
         for (int s = 0; s < SB; ++s) {
             ptx::mbar_init(sfull(s), 1);
-            ptx::mbar_init(sempty(s), EPI_WARPS);
+            ptx::mbar_init(sempty(s), EPI_WARPS * 32);
         }
         ptx::mbar_init(done, 1);
         *abort_flag = 0;
@@ -283,7 +288,6 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
         __syncwarp();
     } else {
         // ------------------------------------------------------ epilogue
-        constexpr int CH = BN >= 64 ? 16 : 32; // TMEM columns per load / wait
         const int ew = warp - 4;
         const int quarter = warp & 3; // TMEM lanes 32*quarter .. +31
         const int col0 = (ew >> 2) * C::kCols;
@@ -338,34 +342,39 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                     return false;
                 ptx::tc_fence_after();
                 const float *sbs = sb_ring + (size_t)slot * BN + col0;
-                // decode slices: a warp whose 32 rows are all past the tile's rows has nothing to keep
-                if (use && (BN > 64 || ti.a_row0 + quarter * 32 < ti.m_end))
+                // 16-column chunks, the next one in flight while the current one is folded (decode
+                // slices: a warp whose 32 rows are all past the tile's rows has nothing to keep)
+                if (use && (BN > 64 || ti.a_row0 + quarter * 32 < ti.m_end)) {
+                    constexpr int NCH = C::kCols / 16;
+                    uint32_t PP[2][16];
+                    const uint32_t tbase = tmem_base + lane_addr + (uint32_t)(b * BN + col0);
+                    ptx::tmem_ld_32x32b_x16(tbase, PP[0]);
+                    ptx::tmem_ld_wait_regs(PP[0]);
 #pragma unroll
-                for (int ch = 0; ch < C::kCols / CH; ++ch) {
-                    uint32_t P[CH];
-                    if constexpr (CH == 32)
-                        ptx::tmem_ld_32x32b_x32(tmem_base + lane_addr + (uint32_t)(b * BN + col0 + ch * CH), P);
-                    else
-                        ptx::tmem_ld_32x32b_x16(tmem_base + lane_addr + (uint32_t)(b * BN + col0 + ch * CH), P);
-                    ptx::tmem_ld_wait();
-                    if constexpr (PER_ROW_B) {
+                    for (int ch = 0; ch < NCH; ++ch) {
+                        if (ch + 1 < NCH)
+                            ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)((ch + 1) * 16), PP[(ch + 1) & 1]);
+                        const uint32_t (&P)[16] = PP[ch & 1];
+                        if constexpr (PER_ROW_B) {
 #pragma unroll
-                        for (int q = 0; q < CH / 4; ++q) {
-                            const float4 sb4 = *reinterpret_cast<const float4 *>(sbs + ch * CH + 4 * q);
-                            const float2 s01 = __fmul2_rn(make_float2(sa, sa), make_float2(sb4.x, sb4.y));
-                            const float2 s23 = __fmul2_rn(make_float2(sa, sa), make_float2(sb4.z, sb4.w));
-                            float2 &a0 = acc[ch * (CH / 2) + 2 * q];
-                            float2 &a1 = acc[ch * (CH / 2) + 2 * q + 1];
-                            a0 = __ffma2_rn(make_float2(__uint_as_float(P[4 * q]), __uint_as_float(P[4 * q + 1])), s01, a0);
-                            a1 = __ffma2_rn(make_float2(__uint_as_float(P[4 * q + 2]), __uint_as_float(P[4 * q + 3])), s23, a1);
+                            for (int q = 0; q < 4; ++q) {
+                                const float4 sb4 = *reinterpret_cast<const float4 *>(sbs + ch * 16 + 4 * q);
+                                const float2 s01 = __fmul2_rn(make_float2(sa, sa), make_float2(sb4.x, sb4.y));
+                                const float2 s23 = __fmul2_rn(make_float2(sa, sa), make_float2(sb4.z, sb4.w));
+                                float2 &a0 = acc[ch * 8 + 2 * q];
+                                float2 &a1 = acc[ch * 8 + 2 * q + 1];
+                                a0 = __ffma2_rn(make_float2(__uint_as_float(P[4 * q]), __uint_as_float(P[4 * q + 1])), s01, a0);
+                                a1 = __ffma2_rn(make_float2(__uint_as_float(P[4 * q + 2]), __uint_as_float(P[4 * q + 3])), s23, a1);
+                            }
+                        } else {
+                            const float2 s2 = make_float2(s, s);
+#pragma unroll
+                            for (int h = 0; h < 8; ++h)
+                                acc[ch * 8 + h] = __ffma2_rn(
+                                    make_float2(__uint_as_float(P[2 * h]), __uint_as_float(P[2 * h + 1])), s2, acc[ch * 8 + h]);
                         }
-                    } else {
-                        const float2 s2 = make_float2(s, s);
-#pragma unroll
-                        for (int j = 0; j < CH / 2; ++j)
-                            acc[ch * (CH / 2) + j] = __ffma2_rn(
-                                make_float2(__uint_as_float(P[2 * j]), __uint_as_float(P[2 * j + 1])), s2,
-                                acc[ch * (CH / 2) + j]);
+                        if (ch + 1 < NCH)
+                            ptx::tmem_ld_wait_regs(PP[(ch + 1) & 1]);
                     }
                 }
                 ptx::tc_fence_before();
@@ -374,13 +383,10 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                 // its reads before that write with a proxy fence ahead of the release
                 if (PER_ROW_B)
                     ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (j == KBP - 1)
-                        ptx::mbar_arrive(tempty(gi));
-                    if (PER_ROW_B)
-                        ptx::mbar_arrive(sempty(slot));
-                }
+                if (j == KBP - 1)
+                    ptx::mbar_arrive(tempty(gi));
+                if (PER_ROW_B)
+                    ptx::mbar_arrive(sempty(slot));
                 ++tb;
                 return true;
             };
@@ -436,7 +442,60 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             }
             if (!ok)
                 break;
-            if (row_ok && col_ok) {
+            if (BN >= 128 && (p.out_bf16 || !p.accumulate)) {
+                // through the warp's staging area: each thread writes 64 bytes of its row, then the
+                // warp stores 8 rows x 64 contiguous bytes per instruction (16-byte chunks swizzled
+                // by row so both the writes and the reads are free of bank conflicts)
+                uint8_t *stg = stage_out + (size_t)ew * 2048;
+                const int64_t mw = (int64_t)ti.a_row0 + quarter * 32; // the warp's first row
+                // one pass: the thread's 16 bytes of chunk c of its row, then the warp's 32 rows out
+                auto pass = [&](auto chunk, auto store) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        *reinterpret_cast<uint4 *>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = chunk(c);
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int pc = lane + 32 * i, r = pc >> 2, c = pc & 3;
+                        const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+                        if (col_ok && mw + r < ti.m_end)
+                            store(mw + r, c, v);
+                    }
+                    __syncwarp();
+                };
+                if (p.out_bf16) {
+#pragma unroll
+                    for (int ps = 0; ps < C::kCols / 32; ++ps) // 32 BF16 columns a pass
+                        pass(
+                            [&](int c) {
+                                uint32_t w[4];
+#pragma unroll
+                                for (int h = 0; h < 4; ++h) {
+                                    const float2 a = acc[ps * 16 + 4 * c + h];
+                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(a.x, a.y);
+                                    w[h] = *reinterpret_cast<const uint32_t *>(&b2);
+                                }
+                                return make_uint4(w[0], w[1], w[2], w[3]);
+                            },
+                            [&](int64_t row, int c, const uint4 &v) {
+                                *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + row * p.ldo + n0 +
+                                                           ps * 32 + c * 8) = v;
+                            });
+                } else {
+#pragma unroll
+                    for (int ps = 0; ps < C::kCols / 16; ++ps) // 16 FP32 columns a pass
+                        pass(
+                            [&](int c) {
+                                const float2 a = acc[ps * 8 + 2 * c], b2 = acc[ps * 8 + 2 * c + 1];
+                                return make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(b2.x),
+                                                  __float_as_uint(b2.y));
+                            },
+                            [&](int64_t row, int c, const uint4 &v) {
+                                *reinterpret_cast<uint4 *>(reinterpret_cast<float *>(p.out) + ti.e * p.out_e_stride +
+                                                           row * p.ldo + n0 + ps * 16 + c * 4) = v;
+                            });
+                }
+            } else if (row_ok && col_ok) {
                 if (p.out_bf16) {
                     __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.out) + m * p.ldo + n0;
 #pragma unroll
