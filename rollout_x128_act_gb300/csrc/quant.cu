@@ -372,29 +372,6 @@ __device__ __forceinline__ void load_weights8(const ActQuantArgs &a, int64_t col
     }
 }
 
-// The thread's 8x8 block of -y from global memory (rows >= cnt give zeros):
-// all loads are issued before any arithmetic.
-template <int P>
-__device__ __forceinline__ void load_block_neg(const ActQuantArgs &a, int64_t row0, int64_t col0, int cnt, int rg,
-                                               int cc, float (&nv)[8][8])
-{
-    uint4 raw[8], aux[8];
-    float rs[8], w8[8];
-    load_weights8<P, true>(a, col0 + cc * 8, w8);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int r = rg * 8 + i;
-        const bool in = r < cnt;
-        raw[i] = in ? ldg_stream(a.x + (row0 + r) * a.ldx + col0 + cc * 8) : make_uint4(0, 0, 0, 0);
-        aux[i] = (P == kProduceSwiglu && in) ? ldg_stream(a.up + (row0 + r) * a.ldup + col0 + cc * 8)
-                                             : make_uint4(0, 0, 0, 0);
-        rs[i] = (P == kProduceRms && in) ? __ldg(a.rstd + row0 + r) : 0.0f;
-    }
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        produce8<P, true>(raw[i], aux[i], rs[i], w8, nv[i]);
-}
-
 // one produced 8-column segment of row `row`, sign as is (zeros when !in)
 template <int P>
 __device__ __forceinline__ void load_row8_produced(const ActQuantArgs &a, int64_t row, int64_t col, bool in,
@@ -613,24 +590,109 @@ __device__ __forceinline__ void quant_tile(const ActQuantArgs &a, TileSmem &ts, 
     }
 }
 
-// Activation / gradient quantizer (1x128 row copy + 128x1 column copy), one
-// CTA per tile, inputs loaded straight to registers (the SwiGLU producer).
-template <bool ROW, bool COL, int P>
-__global__ void __launch_bounds__(kThreads, 2) k_quant_act(const __grid_constant__ ActQuantArgs a)
-{
-    __shared__ __align__(16) TileSmem ts;
-    __shared__ Group grp;
+// ------------------------------------------------------------ SwiGLU-fused quantizer
+//
+// The sigmoid factor fl32(1 / fl32(1 + exp(-g))) depends on the BF16 gate g
+// alone, so each CTA tabulates it once, with the same device function, for the
+// 8192 gates of magnitude 2^-25 .. 2^7 (32 binades, both signs; 32 KB of shared
+// memory), and looks it up per element; other gates (zeros, tiny or large
+// magnitudes) take the direct computation.  The table entries are that
+// computation's results, so the product is unchanged bit for bit.  The kernel
+// is persistent (two CTAs per SM walk the tiles) so the table is built once
+// per CTA.
 
-    const int t = threadIdx.x, rg = t >> 4, cc = t & 15;
-    const int64_t c0 = (int64_t)blockIdx.y * 128;
-    map_group(blockIdx.x, a.n, a.seg, a.nseg, &grp);
-    __syncthreads();
-    const int cnt = grp.cnt;
-    if (cnt == 0)
-        return;
-    float nv[8][8];
-    load_block_neg<P>(a, grp.t0, c0, cnt, rg, cc, nv);
-    quant_tile<ROW, COL, P>(a, ts, nv, grp.t0, cnt, grp.p0, c0, [] {});
+constexpr int kSigTable = 8192;
+constexpr uint32_t kSigE8Lo = 102; // 2^-25
+
+__device__ __forceinline__ float sigmoid_factor(float g)
+{
+    return __frcp_rn(__fadd_rn(1.0f, exp_taylor7(-g)));
+}
+
+// table slot of the BF16 gate with bits b, or -1 outside the tabulated binades:
+// |b| - (102 << 7) is (binade - 102) << 7 | mantissa inside them
+__device__ __forceinline__ int sigmoid_slot(uint32_t b)
+{
+    const uint32_t d = (b & 0x7FFFu) - (kSigE8Lo << 7);
+    return d < 4096u ? (int)(((b >> 3) & 0x1000u) | d) : -1;
+}
+
+// the direct computation, out of line: every element has a call site and
+// almost none take it, so inlining would only crowd the instruction cache
+__device__ __noinline__ float sigmoid_factor_slow(float g)
+{
+    return sigmoid_factor(g);
+}
+
+// -h for 8 columns of one row: gate bits in graw, up values in uraw
+__device__ __forceinline__ void swiglu8_neg(const uint4 &graw, const uint4 &uraw, const float *tab, float (&nv)[8])
+{
+    const uint32_t gw[4] = {graw.x, graw.y, graw.z, graw.w};
+    float gv[8], nu[8], sg[8];
+    unpack8(graw, gv);
+    unpack8_neg(uraw, nu);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const int slot = sigmoid_slot((k & 1) ? (gw[k >> 1] >> 16) : (gw[k >> 1] & 0xFFFFu));
+        sg[k] = slot >= 0 ? tab[slot] : sigmoid_factor_slow(gv[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) {
+        const float2 sl = __fmul2_rn(make_float2(gv[k], gv[k + 1]), make_float2(sg[k], sg[k + 1]));
+        const float2 h = __fmul2_rn(sl, make_float2(nu[k], nu[k + 1]));
+        const __nv_bfloat162 hb = __float22bfloat162_rn(h);
+        nv[k] = __low2float(hb);
+        nv[k + 1] = __high2float(hb);
+    }
+}
+
+struct SwiSmem {
+    TileSmem ts;
+    float tab[kSigTable];
+    Group grp[2];
+};
+
+template <bool ROW, bool COL>
+__global__ void __launch_bounds__(kThreads, 2)
+    k_quant_act_swiglu(const __grid_constant__ ActQuantArgs a, int64_t ngroups, int ncb)
+{
+    extern __shared__ uint8_t smem_raw[];
+    SwiSmem &sm = *reinterpret_cast<SwiSmem *>(ptx::align_smem<16>(smem_raw));
+    const int t = threadIdx.x, warp = t >> 5;
+    const int rg = t >> 4, cc = t & 15;
+    const int64_t total = ngroups * ncb;
+
+    for (int i = t; i < kSigTable; i += kThreads) {
+        const uint32_t b = ((uint32_t)(i >> 12) << 15) | ((kSigE8Lo + (uint32_t)((i >> 7) & 31)) << 7) | (uint32_t)(i & 127);
+        sm.tab[i] = sigmoid_factor(__uint_as_float(b << 16));
+    }
+
+    for (int64_t k = 0;; ++k) {
+        const int64_t T = blockIdx.x + k * (int64_t)gridDim.x;
+        if (T >= total)
+            break;
+        if (warp == 0)
+            map_group(T / ncb, a.n, a.seg, a.nseg, &sm.grp[k & 1]);
+        __syncthreads(); // the group (and, the first time, the table) visible to all
+        const int cnt = sm.grp[k & 1].cnt;
+        if (cnt == 0)
+            continue;
+        const int64_t t0 = sm.grp[k & 1].t0, p0 = sm.grp[k & 1].p0;
+        const int64_t c0 = (T % ncb) * 128;
+        uint4 graw[8], uraw[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int r = rg * 8 + i;
+            const bool in = r < cnt;
+            graw[i] = in ? ldg_stream(a.x + (t0 + r) * a.ldx + c0 + cc * 8) : make_uint4(0, 0, 0, 0);
+            uraw[i] = in ? ldg_stream(a.up + (t0 + r) * a.ldup + c0 + cc * 8) : make_uint4(0, 0, 0, 0);
+        }
+        float nv[8][8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            swiglu8_neg(graw[i], uraw[i], sm.tab, nv[i]);
+        quant_tile<ROW, COL, kProduceSwiglu>(a, sm.ts, nv, t0, cnt, p0, c0, [] {});
+    }
 }
 
 // ------------------------------------------------------------ TMA-fed activation quantizer
@@ -757,42 +819,81 @@ __global__ void __launch_bounds__(kThreads, 2)
 
 
 // RMSNorm statistics, one warp per row.  Lane l sums the 128-column groups
-// l, l + 32, ... (each left to right by fma, 16 loads in flight); the group
-// sums are then added left to right by every lane through shuffles, so the
-// binary32 result follows one fixed order: rstd = 1 / sqrt(total / c + eps).
-__global__ void __launch_bounds__(256) k_rms_rstd(const uint16_t *__restrict__ x, int64_t n, int64_t c,
-                                                  int64_t ldx, float eps, float *__restrict__ rstd)
+// l, l + 32, ... (each left to right by fma); the group sums are then added
+// left to right by every lane through shuffles, so the binary32 result
+// follows one fixed order: rstd = 1 / sqrt(total / c + eps).  A round of 32
+// groups (8 KB) is loaded coalesced (one warp load = 512 contiguous bytes)
+// and regrouped through shared memory, each group padded to 272 bytes so that
+// both the regrouping stores and the per-lane group reads are conflict-free.
+// Warps walk rows grid-stride; the next round's loads are in flight while the
+// current round is summed.
+constexpr int kRmsWarps = 4;
+constexpr int kRmsPitch = 272;
+
+__global__ void __launch_bounds__(kRmsWarps * 32) k_rms_rstd(const uint16_t *__restrict__ x, int64_t n, int64_t c,
+                                                             int64_t ldx, float eps, float *__restrict__ rstd)
 {
-    const int lane = threadIdx.x & 31;
-    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    __shared__ __align__(16) uint8_t stage[kRmsWarps][32 * kRmsPitch];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t stride = (int64_t)gridDim.x * kRmsWarps;
+    int64_t row = (int64_t)blockIdx.x * kRmsWarps + warp;
     if (row >= n)
         return;
+    uint8_t *sw = stage[warp];
     const int groups = (int)(c >> 7);
-    const uint16_t *xr = x + row * ldx;
-    float total = 0.0f;
-    for (int g0 = 0; g0 < groups; g0 += 32) {
-        const int g = g0 + lane;
-        float part = 0.0f;
-        if (g < groups) {
-            uint4 raw[16];
+    // round (row, g0): its live * 16 chunks of 16 bytes; chunk q is slot q % 16 of group q / 16
+    uint4 raw[16];
+    auto load = [&](int64_t r, int g0) {
+        const uint4 *xr = reinterpret_cast<const uint4 *>(x + r * ldx) + (int64_t)g0 * 16;
+        const int chunks = min(32, groups - g0) * 16;
 #pragma unroll
-            for (int k = 0; k < 16; ++k)
-                raw[k] = __ldg(reinterpret_cast<const uint4 *>(xr + (int64_t)g * 128 + k * 8));
+        for (int k = 0; k < 16; ++k) {
+            const int q = k * 32 + lane;
+            raw[k] = q < chunks ? __ldg(xr + q) : make_uint4(0, 0, 0, 0);
+        }
+    };
+    int g0 = 0;
+    float total = 0.0f;
+    load(row, 0);
+    while (row < n) {
+        const int live = min(32, groups - g0);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            const int q = k * 32 + lane;
+            if (q < live * 16)
+                *reinterpret_cast<uint4 *>(sw + (q >> 4) * kRmsPitch + (q & 15) * 16) = raw[k];
+        }
+        __syncwarp();
+        int64_t nrow = row;
+        int ng0 = g0 + 32;
+        if (ng0 >= groups) {
+            nrow = row + stride;
+            ng0 = 0;
+        }
+        if (nrow < n)
+            load(nrow, ng0);
+        float part = 0.0f;
+        if (lane < live) {
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
                 float v[8];
-                unpack8(raw[k], v);
+                unpack8(*reinterpret_cast<const uint4 *>(sw + lane * kRmsPitch + k * 16), v);
 #pragma unroll
                 for (int j = 0; j < 8; ++j)
                     part = __fmaf_rn(v[j], v[j], part);
             }
         }
-        const int live = min(32, groups - g0);
+        __syncwarp(); // every lane has read its group before the next round is staged
         for (int j = 0; j < live; ++j)
             total = __fadd_rn(total, __shfl_sync(0xFFFFFFFFu, part, j));
+        if (ng0 == 0) {
+            if (lane == 0)
+                rstd[row] = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(total, (float)c), eps)));
+            total = 0.0f;
+        }
+        row = nrow;
+        g0 = ng0;
     }
-    if (lane == 0)
-        rstd[row] = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(total, (float)c), eps)));
 }
 
 // 8x8 byte transpose: in[i] holds bytes (row i, cols 0..7); out[j] holds
@@ -1279,15 +1380,36 @@ cudaError_t launch_quant_act_tma_p(const ActQuantArgs &a, cudaStream_t st)
     return launch_quant_act_tma<false, true, P>(a, map, ngroups, ncb, st);
 }
 
-template <int P>
-void launch_quant_act_p(const ActQuantArgs &a, dim3 grid, cudaStream_t st)
+template <bool ROW, bool COL>
+cudaError_t launch_quant_act_swiglu_rc(const ActQuantArgs &a, int64_t ngroups, int ncb, cudaStream_t st)
 {
+    auto kern = k_quant_act_swiglu<ROW, COL>;
+    constexpr size_t smem = sizeof(SwiSmem) + 16;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (configured_device != dev) {
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
+            return e;
+        configured_device = dev;
+    }
+    const int64_t tiles = ngroups * ncb;
+    const int64_t cap = 2 * (int64_t)sm_count();
+    kern<<<(unsigned)(tiles < cap ? tiles : cap), kThreads, smem, st>>>(a, ngroups, ncb);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_act_swiglu(const ActQuantArgs &a, cudaStream_t st)
+{
+    const int64_t ngroups = groups_upper_bound(a.n, a.seg, a.nseg);
+    const int ncb = (int)(a.c / 128);
     if (a.q_row && a.q_col)
-        k_quant_act<true, true, P><<<grid, kThreads, 0, st>>>(a);
-    else if (a.q_row)
-        k_quant_act<true, false, P><<<grid, kThreads, 0, st>>>(a);
-    else
-        k_quant_act<false, true, P><<<grid, kThreads, 0, st>>>(a);
+        return launch_quant_act_swiglu_rc<true, true>(a, ngroups, ncb, st);
+    if (a.q_row)
+        return launch_quant_act_swiglu_rc<true, false>(a, ngroups, ncb, st);
+    return launch_quant_act_swiglu_rc<false, true>(a, ngroups, ncb, st);
 }
 
 } // namespace
@@ -1296,7 +1418,6 @@ cudaError_t launch_quant_act(const ActQuantArgs &a, cudaStream_t st)
 {
     if (a.n == 0 || (!a.q_row && !a.q_col))
         return cudaSuccess;
-    dim3 grid((unsigned)groups_upper_bound(a.n, a.seg, a.nseg), (unsigned)(a.c / 128));
     switch (a.producer) {
     case kProducePlain:
         return launch_quant_act_tma_p<kProducePlain>(a, st);
@@ -1307,12 +1428,10 @@ cudaError_t launch_quant_act(const ActQuantArgs &a, cudaStream_t st)
     case kProduceSwiglu:
         if (!a.up)
             return cudaErrorInvalidValue;
-        launch_quant_act_p<kProduceSwiglu>(a, grid, st);
-        break;
+        return launch_quant_act_swiglu(a, st);
     default:
         return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_rms_rstd(const uint16_t *x, int64_t n, int64_t c, int64_t ldx, float eps, float *rstd,
@@ -1322,11 +1441,17 @@ cudaError_t launch_rms_rstd(const uint16_t *x, int64_t n, int64_t c, int64_t ldx
         return cudaSuccess;
     if (c <= 0 || c % 128 != 0 || c > 32768)
         return cudaErrorInvalidValue;
-    constexpr int kWarps = 8;
-    const int64_t blocks = (n + kWarps - 1) / kWarps;
-    if (blocks > 2147483647)
-        return cudaErrorInvalidValue;
-    k_rms_rstd<<<(unsigned)blocks, kWarps * 32, 0, st>>>(x, n, c, ldx, eps, rstd);
+    // as many CTAs as are resident at once (registers and stages permitting); warps then walk the rows
+    static int per_sm = 0;
+    if (per_sm == 0) {
+        int v = 0;
+        const cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, k_rms_rstd, kRmsWarps * 32, 0);
+        if (e != cudaSuccess)
+            return e;
+        per_sm = v > 0 ? v : 1;
+    }
+    const int64_t blocks = (n + kRmsWarps - 1) / kRmsWarps, cap = (int64_t)per_sm * sm_count();
+    k_rms_rstd<<<(unsigned)(blocks < cap ? blocks : cap), kRmsWarps * 32, 0, st>>>(x, n, c, ldx, eps, rstd);
     return cudaGetLastError();
 }
 

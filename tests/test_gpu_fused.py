@@ -119,6 +119,23 @@ def test_swiglu_saturation_and_tiny_values():
     _check_swiglu(g, u, pad=128)
 
 
+def test_swiglu_every_gate_value():
+    """Every finite BF16 gate, one binade and sign per row (so each 1x128 group
+    resolves its values), against the oracle: covers every sigmoid table slot
+    and the directly computed gates (zeros, subnormals, tiny and large
+    magnitudes) on both sides of the table's edges."""
+    e8 = np.arange(255, dtype=np.uint32)
+    rows = []
+    for s in (0, 1):
+        rows.append((s << 15) | (e8[:, None] << 7) | np.arange(128, dtype=np.uint32)[None, :])
+    g = np.concatenate(rows).astype(np.uint16)  # 510 rows x 128
+    # |up| <= 1 keeps every product finite (|h| <= |g|): the quantizer's domain
+    u = synth.bf16_bits(np.random.default_rng(14).uniform(-1.0, 1.0, g.shape).astype(np.float32))
+    _check_swiglu(g, u)
+    # up = 1: h = BF16(silu(g)) itself is quantized
+    _check_swiglu(g, synth.bf16_bits(np.ones(g.shape, np.float32)))
+
+
 def test_swiglu_segments():
     off, _ = synth.zipf_topk_routing(64, 16, 4, 1.2, seed=1)  # 256 routed rows
     n = int(off[-1])
