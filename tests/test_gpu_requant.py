@@ -23,6 +23,8 @@ def _row_copy(x):
 def test_requant_col_bit_exact(kind):
     R, C = (300, 384) if kind in ("ragged", "segments") else (256, 512)
     x = np.zeros((R, C), np.uint16) if kind == "zeros" else synth.activation(R, C, seed=51, stream="x")
+    if kind == "zeros":
+        x[1::3] = 0x8000  # negative zeros: code 0x80 in both copies
     if kind == "outliers":
         x[::5, ::11] = synth.bf16_bits(np.full(((R + 4) // 5, (C + 10) // 11), -2.5e4, np.float32))
     off = np.array([0, 90, 90, 217, 300], dtype=np.int64) if kind == "segments" else None
@@ -36,13 +38,17 @@ def test_requant_col_bit_exact(kind):
     assert np.array_equal(g["s_col"].cpu().numpy()[:P // 128].view(np.uint32), sc.view(np.uint32))
 
 
-def test_requant_quotients_near_e4m3_midpoints():
+@pytest.mark.parametrize("mids", [
+    [1.0625, 1.1875, 1.9375, 0.53125, 3.75, 7.5, 240.0, 416.0, 0.01953125, 0.017578125, 0.0029296875],
+    [k * 2.0 ** -10 for k in (1, 3, 5, 7, 9, 11, 13, 15)] + [0.0146484375 * 2, 0.5078125],
+], ids=["normal", "subnormal-codes"])
+def test_requant_quotients_near_e4m3_midpoints(mids):
     """Codes of 1.0 make each rebuilt value its row scale, so the values can be placed
     at S * m nudged by -4..+4 binary32 ulps for E4M3 midpoints m: both sides of the
-    fast quotient's two-ulp guard, and the E4M3 subnormal range."""
+    fast quotient's guard, in the normal range and among the subnormal codes (odd
+    multiples of 2^-10)."""
     amax = np.float32(448.0 * 1.2345678)
     S = np.float32(amax / np.float32(448.0))
-    mids = [1.0625, 1.1875, 1.9375, 0.53125, 3.75, 7.5, 240.0, 416.0, 0.01953125, 0.017578125, 0.0029296875]
     vals = [amax]
     for m in mids:
         base = np.float32(np.float32(m) * S)
@@ -53,6 +59,7 @@ def test_requant_quotients_near_e4m3_midpoints():
             vals.append(v)
     vals = np.array(vals, np.float32)
     R = 128
+    assert len(vals) <= R
     s_row = np.zeros((1, R), np.float32)
     s_row[0, :len(vals)] = vals
     s_row[0, len(vals):] = -vals[1:R - len(vals) + 1]  # negative copies fill the group
