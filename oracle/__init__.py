@@ -77,6 +77,14 @@ def _load():
         lib.jo_dequant_blocks_pow2.argtypes = [P, I, I, I, P, P]
         lib.jo_dequant_mx_rows.argtypes = [P, I, I, I, I, P, P]
         lib.jo_dequant_mx_cols.argtypes = [P, I, P, I, I, I, I, I, P, ctypes.c_int, P]
+        lib.jo_e2m1_decode.restype = ctypes.c_double
+        lib.jo_e2m1_decode.argtypes = [ctypes.c_uint8]
+        lib.jo_e2m1_encode.restype = ctypes.c_uint8
+        lib.jo_e2m1_encode.argtypes = [ctypes.c_double]
+        lib.jo_quant_nvfp4.argtypes = [P, I, I, I, P, P, P, P]
+        lib.jo_quant_nvfp4.restype = None
+        lib.jo_dequant_nvfp4_bf16.argtypes = [P, P, P, I, I, ctypes.c_int, P]
+        lib.jo_dequant_nvfp4_bf16.restype = None
         for f in ("jo_fprop", "jo_dgrad", "jo_wgrad"):
             getattr(lib, f).argtypes = [P, P, I, I, I, P, I, P, P]
         for f in ("jo_quant_rowgroups", "jo_quant_colgroups", "jo_quant_blocks", "jo_quant_mx_rows",
@@ -122,6 +130,20 @@ def e4m3_encode(values) -> np.ndarray:
     lib = _load()
     v = np.asarray(values, dtype=np.float64)
     return np.array([lib.jo_e4m3_encode(float(x)) for x in v.ravel()], dtype=np.uint8).reshape(v.shape)
+
+
+def e2m1_decode(codes) -> np.ndarray:
+    """Value of every E2M1 code (4 bits: sign, 2 exponent bits, 1 mantissa bit)."""
+    lib = _load()
+    table = np.array([lib.jo_e2m1_decode(c) for c in range(16)], dtype=np.float64)
+    return table[np.asarray(codes, dtype=np.uint8) & 15]
+
+
+def e2m1_encode(values) -> np.ndarray:
+    """Round each value to the nearest E2M1 code (ties to even, saturating at 6)."""
+    lib = _load()
+    v = np.asarray(values, dtype=np.float64)
+    return np.array([lib.jo_e2m1_encode(float(x)) for x in v.ravel()], dtype=np.uint8).reshape(v.shape)
 
 
 def e8m0_exponent(amax: float) -> int:
@@ -383,3 +405,43 @@ def wgrad(dY, X, at=None):
     C = X.shape[1]
     assert X.shape[0] == N
     return _gemm("jo_wgrad", dY, X, N, D, C, at, (D, C))
+
+
+# --------------------------------------------------------------------------- NVFP4
+
+def quant_nvfp4(x, scope_amax=None):
+    """NVFP4: (q [R x C/2] u8 packed E2M1, sb [R x C/16] u8 E4M3 block scales,
+    sg f32 scope scales: [R] per row when scope_amax is None, else [1] from the
+    given tensor-scope max |x|)."""
+    x = _c(x, np.uint16)
+    R, C = x.shape
+    if C % 16:
+        raise ValueError("columns must be a multiple of 16")
+    q = np.empty((R, C // 2), np.uint8)
+    sb = np.empty((R, C // 16), np.uint8)
+    sg = np.empty(R if scope_amax is None else 1, np.float32)
+    amax = None if scope_amax is None else np.array([scope_amax], np.float32)
+    _load().jo_quant_nvfp4(_p(x), R, C, C, _p(amax), _p(q), _p(sb), _p(sg))
+    return q, sb, sg
+
+
+def dequant_nvfp4_bf16(q, sb, sg):
+    """BF16 bits of e2m1 * decode(e_b) * S_g, rounded once; per-row scales when sg has R entries."""
+    q = _c(q, np.uint8)
+    sb = _c(sb, np.uint8)
+    sg = _c(sg, np.float32)
+    R, C = q.shape[0], q.shape[1] * 2
+    out = np.empty((R, C), np.uint16)
+    _load().jo_dequant_nvfp4_bf16(_p(q), _p(sb), _p(sg), R, C, int(sg.size > 1), _p(out))
+    return out
+
+
+def dequant_nvfp4(q, sb, sg) -> np.ndarray:
+    """Exact binary64 values e2m1 * decode(e_b) * S_g."""
+    q = np.asarray(q, np.uint8)
+    codes = np.empty((q.shape[0], q.shape[1] * 2), np.uint8)
+    codes[:, 0::2] = q & 15
+    codes[:, 1::2] = q >> 4
+    s = np.asarray(sg, np.float64)
+    s = s[:, None] if s.size == q.shape[0] and s.size > 1 else s.reshape(1, 1)
+    return e2m1_decode(codes) * np.repeat(e4m3_decode(sb), 16, axis=1) * s

@@ -739,3 +739,107 @@ void jo_wgrad(const double *dY, const double *X, int64_t N, int64_t D, int64_t C
     for (i = 0; i < count; ++i)
         dot_terms(dY + at[2 * i], D, X + at[2 * i + 1], C, N, &y[i], &bound[i]);
 }
+
+/* ------------------------------------------------------------------------ */
+/* NVFP4 ([MB] NVFP4 section): FP4 E2M1 values with one E4M3 scale per      */
+/* block of 16 consecutive values (rounded to the nearest E4M3 value) and    */
+/* one FP32 scale for a larger scope: one per token (row) for activations,   */
+/* one per tensor (shared by a gate/up pair) for weights.  The pages give    */
+/* no formula; the readings, in the order of the FP8 recipe above:           */
+/*   S_g = fl32(amax_scope / 2688)          (2688 = 448 * 6: the largest     */
+/*                                           E4M3 scale times the largest    */
+/*                                           E2M1 value)                     */
+/*   block b:  e_b = E4M3(fl32(fl32(amax_b / 6) / S_g))                      */
+/*             D_b = fl32(decode(e_b) * S_g)                                 */
+/*             q   = E2M1(fl32(x / D_b)),  D_b = 0: every code 0x0           */
+/* E2M1: sign, 2 exponent bits (bias 1), 1 mantissa bit; magnitudes 0, 0.5,  */
+/* 1, 1.5, 2, 3, 4, 6; nearest value, ties to the even code, saturating at   */
+/* 6, sign of zero kept.  Two codes per byte, element 2j in the low nibble.  */
+/* ------------------------------------------------------------------------ */
+
+double jo_e2m1_decode(uint8_t code)
+{
+    static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+    double m = mag[code & 7];
+    return (code & 8) ? -m : m;
+}
+
+uint8_t jo_e2m1_encode(double v)
+{
+    uint8_t sign = signbit(v) ? 8 : 0;
+    double a = fabs(v), mid;
+    int lo = 0;
+    while (lo < 7 && jo_e2m1_decode((uint8_t)(lo + 1)) <= a) /* largest code with decode <= a */
+        ++lo;
+    if (lo == 7)
+        return (uint8_t)(sign | 7); /* saturate */
+    mid = 0.5 * (jo_e2m1_decode((uint8_t)lo) + jo_e2m1_decode((uint8_t)(lo + 1)));
+    if (a < mid)
+        return (uint8_t)(sign | lo);
+    if (a > mid)
+        return (uint8_t)(sign | (lo + 1));
+    return (uint8_t)(sign | ((lo & 1) ? lo + 1 : lo)); /* tie: even code */
+}
+
+/*
+ *   x   : bf16 [rows x cols], row stride ldx; cols a multiple of 16
+ *   scope_amax : NULL for one scale per row (the row's max |x|), else the
+ *         max |x| of the tensor scope, one scale for every row
+ *   q   : packed codes [rows x cols/2];  sb : E4M3 block scales [rows x cols/16]
+ *   sg  : FP32 scope scales, [rows] (per row) or [1]
+ */
+void jo_quant_nvfp4(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, const float *scope_amax,
+                    uint8_t *q, uint8_t *sb, float *sg)
+{
+    int64_t r, b, j;
+    for (r = 0; r < rows; ++r) {
+        float amax = 0.0f, s;
+        if (scope_amax) {
+            amax = *scope_amax;
+        } else {
+            for (j = 0; j < cols; ++j) {
+                float v = fabsf(bf16_value(x[r * ldx + j]));
+                if (v > amax)
+                    amax = v;
+            }
+        }
+        s = amax / 2688.0f;
+        if (!scope_amax || r == 0)
+            sg[scope_amax ? 0 : r] = s;
+        for (b = 0; b < cols / 16; ++b) {
+            float ab = 0.0f, d;
+            uint8_t e;
+            for (j = 0; j < 16; ++j) {
+                float v = fabsf(bf16_value(x[r * ldx + b * 16 + j]));
+                if (v > ab)
+                    ab = v;
+            }
+            e = s > 0.0f ? jo_e4m3_encode((double)((ab / 6.0f) / s)) : 0x00;
+            sb[r * (cols / 16) + b] = e;
+            d = (float)jo_e4m3_decode(e) * s; /* binary32 product */
+            for (j = 0; j < 16; j += 2) {
+                uint8_t c0 = 0, c1 = 0;
+                if (d != 0.0f) {
+                    c0 = jo_e2m1_encode((double)(bf16_value(x[r * ldx + b * 16 + j]) / d));
+                    c1 = jo_e2m1_encode((double)(bf16_value(x[r * ldx + b * 16 + j + 1]) / d));
+                }
+                q[r * (cols / 2) + b * 8 + j / 2] = (uint8_t)(c0 | (c1 << 4));
+            }
+        }
+    }
+}
+
+/* out = BF16(e2m1 * decode(e_b) * S_g), rounded once: the product of a 2-bit,
+ * a 4-bit and a 24-bit significand is exact in binary64. */
+void jo_dequant_nvfp4_bf16(const uint8_t *q, const uint8_t *sb, const float *sg, int64_t rows, int64_t cols,
+                           int per_row, uint16_t *out)
+{
+    int64_t r, c;
+    for (r = 0; r < rows; ++r)
+        for (c = 0; c < cols; ++c) {
+            uint8_t byte = q[r * (cols / 2) + c / 2];
+            uint8_t code = (c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+            out[r * cols + c] = bf16_rne(jo_e2m1_decode(code) * jo_e4m3_decode(sb[r * (cols / 16) + c / 16]) *
+                                         (double)sg[per_row ? r : 0]);
+        }
+}
