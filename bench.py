@@ -478,6 +478,27 @@ def measure_fused_producers(dev):
             "swiglu_quant_us": round(ms_sw * 1e3, 1)}
 
 
+def measure_nvfp4(dev):
+    """NVFP4 quantizer (per-token scope: two reads of each row) and BF16 dequantizer on
+    the 30B-A3B routed activations, 131072 rows x hidden 2048 (512 MB of BF16).
+    Algorithmic bytes per element: quantizer 2 + 1/2 + 1/16 (+ 4 per row), dequantizer
+    1/2 + 1/16 + 2."""
+    import torch
+
+    import rollout_x128_act_gb300 as jq
+
+    act, _, _ = _dev_inputs(dev, 13)
+    R, Cn = 131072, 2048
+    x = act(R, Cn)
+    o = jq.quant_nvfp4(x)
+    out = torch.empty((R, Cn), dtype=torch.bfloat16, device=dev)
+    ms_q = _time(lambda: jq.jetq_quant_nvfp4(x, o["q"], o["sb"], o["sg"]), 20)
+    ms_d = _time(lambda: jq.jetq_dequant_nvfp4_bf16(o["q"], o["sb"], o["sg"], True, out), 20)
+    n = R * Cn
+    return {"quant_gbs": round((n * (2 + 0.5 + 1 / 16) + 4 * R) / (ms_q * 1e-3) / 1e9, 1), "quant_us": round(ms_q * 1e3, 1),
+            "dequant_gbs": round(n * (0.5 + 1 / 16 + 2) / (ms_d * 1e-3) / 1e9, 1), "dequant_us": round(ms_d * 1e3, 1)}
+
+
 def measure_rollout_step(dev, peaks):
     """On-policy FP8 weight sync plus one rollout decode step of 128 concurrent
     sequences through the dense-8B MLP (quantize, gate/up FProp, quantize, down
@@ -759,6 +780,7 @@ def run_ours(args):
             line["block128_pow2"] = measure_pow2(dev)
             line["requant_dequant"] = measure_f3_kernels(dev)
             line["fused_producers"] = measure_fused_producers(dev)
+            line["nvfp4"] = measure_nvfp4(dev)
             line["rollout_step"] = measure_rollout_step(dev, peaks_now)
             line["moe"] = measure_moe(dev)
             if step_error():
@@ -845,6 +867,7 @@ PROFILE_CASES = {
     "dequant_bf16": "BF16 dequantization of the row copy of H 8192 x 12288",
     "quant_rmsnorm": "RMSNorm statistics + fused RMSNorm quantizer, X 32768 x 4096 BF16 (row + column copies)",
     "quant_swiglu": "fused SwiGLU quantizer, gate and up 8192 x 12288 BF16 (row + column copies)",
+    "quant_nvfp4": "NVFP4 quantizer, per-token scope, 131072 routed rows x 2048 BF16",
 }
 
 
@@ -917,6 +940,9 @@ def run_case(name: str, launches: int = 5):
         gate = bf16(synth.activation(8192, 12288, seed=0, stream="h"))
         up = bf16(synth.activation(8192, 12288, seed=1, stream="h"))
         fn = lambda: jq.quant_act_swiglu(gate, up)  # noqa: E731
+    elif name == "quant_nvfp4":
+        x = bf16(synth.activation(131072, 2048, seed=0, stream="x"))
+        fn = lambda: jq.quant_nvfp4(x)  # noqa: E731
     elif name == "quant_mx":
         x = bf16(synth.activation(8192, 12288, seed=0, stream="h"))
         fn = lambda: jq.quant_mx(x)  # noqa: E731

@@ -231,6 +231,47 @@ JETQ_API jetq_status jetq_quant_act_1x128_swiglu(const uint16_t *gate, const uin
                                  const int64_t *seg_offsets, int nseg, void *stream);
 
 /*
+ * NVFP4 (Miles "Blackwell-native RL recipes" post, NVFP4 section): FP4 E2M1
+ * values, one E4M3 scale per block of 16 consecutive values (rounded to the
+ * nearest E4M3 value), one FP32 scale for a larger scope: per token (row) for
+ * activations, per tensor for weights (a gate/up pair shares one).  The post
+ * gives no formula; the library computes
+ *   S_g = fl32(amax_scope / 2688)                     (2688 = 448 * 6)
+ *   e_b = E4M3(fl32(fl32(amax_b / 6) / S_g)),  D_b = fl32(decode(e_b) * S_g)
+ *   q   = E2M1(fl32(x / D_b))   (nearest, ties to even, saturating at 6;
+ *                                every code 0 where D_b = 0)
+ *
+ *   x, rows, cols, ldx  BF16 [rows x cols], row stride ldx (multiple of 8); cols % 16 == 0
+ *   scope_amax  device float: max |x| of the tensor scope (e.g. from
+ *               jetq_amax_bf16 over gate and up); NULL: one scope per row
+ *   q    packed codes [rows x cols/2], element 2j in the low nibble of byte j (4-byte aligned)
+ *   sb   E4M3 block scales [rows x cols/16], row-major
+ *   sg   FP32 scope scales: [rows] (per row) or [1] (written from row 0's pass)
+ * One warp per row; with a per-row scope it reads the row twice.
+ */
+JETQ_API jetq_status jetq_quant_nvfp4(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx,
+                                 const float *scope_amax, uint8_t *q, uint8_t *sb, float *sg, void *stream);
+
+/*
+ * max |x| over a BF16 tensor, folded into *amax (device float, at least 0 on
+ * entry; a non-negative float compares as its bits): call it on gate and on
+ * up with one *amax for a shared NVFP4 tensor scope.  cols % 8 == 0.
+ */
+JETQ_API jetq_status jetq_amax_bf16(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, float *amax,
+                                 void *stream);
+
+/*
+ * BF16 dequantization of an NVFP4 copy (the post's dequantized-backward mode:
+ * BF16 GEMMs on BF16 values of the exact low-precision operands):
+ * out = BF16(e2m1 * decode(e_b) * S_g), rounded once.
+ *   q, sb, sg   as jetq_quant_nvfp4 writes them; per_row = 1: sg has one scale
+ *               per row, 0: one scale for the tensor
+ *   out         BF16 [rows x cols], row stride ldo (multiple of 8), 16-byte aligned
+ */
+JETQ_API jetq_status jetq_dequant_nvfp4_bf16(const uint8_t *q, const uint8_t *sb, const float *sg, int per_row,
+                                 int64_t rows, int64_t cols, uint16_t *out, int64_t ldo, void *stream);
+
+/*
  * Weight quantizer, 128x128 blocks (Jet-RL explainer, "GEMM Quantization":
  * S_W(i,j) = max|W_tile(i,j)| / 448; the DGrad operand is the same FP8
  * weight, only transposed).  Runs after every optimizer step; its output is

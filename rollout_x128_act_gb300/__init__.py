@@ -59,6 +59,9 @@ def lib() -> ctypes.CDLL:
                                                    P]),
             "jetq_quant_act_1x128_swiglu": (I32, [P, P, I64, I64, I64, I64, P, P, P, P, I64, P, I32, P]),
             "jetq_quant_w_128x128": (I32, [P, I64, I64, I64, P, P, P, P, P]),
+            "jetq_amax_bf16": (I32, [P, I64, I64, I64, P, P]),
+            "jetq_quant_nvfp4": (I32, [P, I64, I64, I64, P, P, P, P, P]),
+            "jetq_dequant_nvfp4_bf16": (I32, [P, P, P, I32, I64, I64, P, I64, P]),
             "jetq_quant_mx32": (I32, [P, I64, I64, I64, P, P, P, P, I64, P, I32, P]),
             "jetq_quant_act_1x128_pow2": (I32, [P, I64, I64, I64, P, P, P, P, I64, P, I32, P]),
             "jetq_quant_w_128x128_pow2": (I32, [P, I64, I64, I64, P, P, P, P, P]),
@@ -141,6 +144,23 @@ def jetq_quant_act_1x128_swiglu(gate, up, q_row, s_row, q_col, s_col, ldq_col, s
     _check(lib().jetq_quant_act_1x128_swiglu(_p(gate), _p(up), n, c, gate.stride(0), up.stride(0), _p(q_row),
                                              _p(s_row), _p(q_col), _p(s_col), ldq_col, _p(seg_offsets), nseg,
                                              _s(stream)), "jetq_quant_act_1x128_swiglu")
+
+
+def jetq_amax_bf16(x, amax, stream=None):
+    r, c = x.shape
+    _check(lib().jetq_amax_bf16(_p(x), r, c, x.stride(0), _p(amax), _s(stream)), "jetq_amax_bf16")
+
+
+def jetq_quant_nvfp4(x, q, sb, sg, scope_amax=None, stream=None):
+    r, c = x.shape
+    _check(lib().jetq_quant_nvfp4(_p(x), r, c, x.stride(0), _p(scope_amax), _p(q), _p(sb), _p(sg), _s(stream)),
+           "jetq_quant_nvfp4")
+
+
+def jetq_dequant_nvfp4_bf16(q, sb, sg, per_row, out, stream=None):
+    r, c = out.shape
+    _check(lib().jetq_dequant_nvfp4_bf16(_p(q), _p(sb), _p(sg), int(per_row), r, c, _p(out), out.stride(0),
+                                         _s(stream)), "jetq_dequant_nvfp4_bf16")
 
 
 def jetq_quant_w_128x128(w, q, s, qT=None, sT=None, stream=None):
@@ -273,6 +293,34 @@ def quant_act_swiglu(gate, up, row=True, col=True, seg_offsets=None, stream=None
     out, nseg = _act_copies(n, c, gate.device, row, col, seg_offsets)
     jetq_quant_act_1x128_swiglu(gate, up, out["q_row"], out["s_row"], out["q_col"], out["s_col"], out["ldq_col"],
                                 seg_offsets, nseg, stream)
+    return out
+
+
+def quant_nvfp4(x, scope_amax=None, stream=None):
+    """NVFP4 copy of BF16 x: dict(q [r x c/2] u8, sb [r x c/16] u8, sg [r] or [1] f32).
+    scope_amax: a device float tensor (tensor scope) or None (one scope per row)."""
+    r, c = x.shape
+    dev = x.device
+    out = dict(q=torch.empty((r, c // 2), dtype=torch.uint8, device=dev),
+               sb=torch.empty((r, c // 16), dtype=torch.uint8, device=dev),
+               sg=torch.empty(r if scope_amax is None else 1, dtype=torch.float32, device=dev))
+    jetq_quant_nvfp4(x, out["q"], out["sb"], out["sg"], scope_amax, stream)
+    return out
+
+
+def amax_bf16(*tensors, stream=None):
+    """max |x| over one or more BF16 tensors, as a device float tensor of one element."""
+    a = torch.zeros(1, dtype=torch.float32, device=tensors[0].device)
+    for t in tensors:
+        jetq_amax_bf16(t, a, stream)
+    return a
+
+
+def dequant_nvfp4_bf16(q, sb, sg, stream=None):
+    """BF16 values of an NVFP4 copy (per-row scope when sg has one entry per row)."""
+    r = q.shape[0]
+    out = torch.empty((r, q.shape[1] * 2), dtype=torch.bfloat16, device=q.device)
+    jetq_dequant_nvfp4_bf16(q, sb, sg, sg.numel() > 1, out, stream)
     return out
 
 

@@ -234,6 +234,54 @@ jetq_status jetq_quant_act_1x128_swiglu(const uint16_t *gate, const uint16_t *up
     return from_cuda(launch_quant_act(args, static_cast<cudaStream_t>(stream)));
 }
 
+jetq_status jetq_amax_bf16(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, float *amax, void *stream)
+{
+    JQ_REQUIRE(rows >= 0 && cols > 0 && amax != nullptr, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(cols % 8 == 0 && ldx >= cols, JETQ_ERR_UNSUPPORTED_SHAPE);
+    if (rows == 0)
+        return JETQ_OK;
+    JQ_REQUIRE(x != nullptr, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(aligned16(x) && ldx % 8 == 0 && (reinterpret_cast<uintptr_t>(amax) & 3u) == 0, JETQ_ERR_MISALIGNED);
+    const jetq_status a = check_arch();
+    if (a != JETQ_OK)
+        return a;
+    return from_cuda(launch_amax_bf16(x, rows, cols, ldx, amax, static_cast<cudaStream_t>(stream)));
+}
+
+jetq_status jetq_quant_nvfp4(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, const float *scope_amax,
+                             uint8_t *q, uint8_t *sb, float *sg, void *stream)
+{
+    JQ_REQUIRE(rows >= 0 && cols > 0, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(cols % 16 == 0 && ldx >= cols, JETQ_ERR_UNSUPPORTED_SHAPE);
+    if (rows == 0)
+        return JETQ_OK;
+    JQ_REQUIRE(x != nullptr && q != nullptr && sb != nullptr && sg != nullptr, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(aligned16(x) && ldx % 8 == 0 && (reinterpret_cast<uintptr_t>(q) & 3u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(sg) & 3u) == 0 && (reinterpret_cast<uintptr_t>(scope_amax) & 3u) == 0,
+               JETQ_ERR_MISALIGNED);
+    const jetq_status a = check_arch();
+    if (a != JETQ_OK)
+        return a;
+    return from_cuda(launch_quant_nvfp4(x, rows, cols, ldx, scope_amax, q, sb, sg, static_cast<cudaStream_t>(stream)));
+}
+
+jetq_status jetq_dequant_nvfp4_bf16(const uint8_t *q, const uint8_t *sb, const float *sg, int per_row, int64_t rows,
+                                    int64_t cols, uint16_t *out, int64_t ldo, void *stream)
+{
+    JQ_REQUIRE(rows >= 0 && cols > 0 && (per_row == 0 || per_row == 1), JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(cols % 16 == 0 && ldo >= cols, JETQ_ERR_UNSUPPORTED_SHAPE);
+    if (rows == 0)
+        return JETQ_OK;
+    JQ_REQUIRE(q != nullptr && sb != nullptr && sg != nullptr && out != nullptr, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE((reinterpret_cast<uintptr_t>(q) & 3u) == 0 && (reinterpret_cast<uintptr_t>(sg) & 3u) == 0 &&
+                   aligned16(out) && ldo % 8 == 0,
+               JETQ_ERR_MISALIGNED);
+    const jetq_status a = check_arch();
+    if (a != JETQ_OK)
+        return a;
+    return from_cuda(launch_dequant_nvfp4(q, sb, sg, per_row, rows, cols, out, ldo, static_cast<cudaStream_t>(stream)));
+}
+
 jetq_status jetq_quant_w_128x128(const uint16_t *w, int64_t d, int64_t c, int64_t ldw, uint8_t *q, float *s,
                                  uint8_t *qT, float *sT, void *stream)
 {

@@ -169,6 +169,14 @@ cudaError_t gemm_decode_read_and_clear_error(cudaStream_t st, unsigned *out);
 
 cudaError_t gemm_read_and_clear_error(cudaStream_t st, unsigned *out);
 
+// NVFP4 (E2M1 values, E4M3 scale per 16, FP32 scope scale per row or tensor)
+cudaError_t launch_amax_bf16(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, float *amax,
+                             cudaStream_t st);
+cudaError_t launch_quant_nvfp4(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, const float *scope_amax,
+                               uint8_t *q, uint8_t *sb, float *sg, cudaStream_t st);
+cudaError_t launch_dequant_nvfp4(const uint8_t *q, const uint8_t *sb, const float *sg, int per_row, int64_t rows,
+                                 int64_t cols, uint16_t *out, int64_t ldo, cudaStream_t st);
+
 // TMA descriptor for a BF16 matrix [rows x cols], row stride ld elements:
 // 128 x 128 boxes (32 KB, rows of 256 bytes, no swizzle), zero fill out of bounds.
 cudaError_t make_bf16_tile_map(CUtensorMap *map, const void *base, int64_t cols, int64_t rows, int64_t ld);

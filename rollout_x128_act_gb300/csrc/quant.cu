@@ -20,6 +20,7 @@
 // pairs (tests/test_division_domain.py).  Groups with S < 2^-96 use the
 // IEEE division itself.
 #include <cuda_bf16.h>
+#include <cuda_fp4.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
@@ -1330,6 +1331,171 @@ __global__ void __launch_bounds__(256) k_dequant_bf16(const __grid_constant__ De
     dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
 }
 
+// ------------------------------------------------------------ NVFP4
+//
+// E2M1 values, one E4M3 scale per block of 16 consecutive values and an FP32
+// scope scale (per row, or one for the tensor): S_g = fl32(amax / 2688),
+// e_b = E4M3(fl32(fl32(amax_b / 6) / S_g)), D_b = fl32(decode(e_b) * S_g),
+// q = E2M1(fl32(x / D_b)), every code 0 where D_b = 0.  One warp per row:
+// lane l holds elements 256k + 8l .. +7 of the row, so a block is a lane pair.
+
+__device__ __forceinline__ float e4m3_value(uint32_t code)
+{
+    const __half_raw h = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)code, __NV_E4M3);
+    return __half2float(*reinterpret_cast<const __half *>(&h));
+}
+
+// 8 consecutive E2M1 codes of the quotients fl32(x / d) (d != 0), element 0 in
+// the low nibble.  With r = RN(1/d): q0 = RN(x * -r), e = x + d*q0 (exact by
+// FMA), q1 = RN(q0 + e * -r) is the residual-corrected quotient, negated (zero
+// quotients then come out with the sign of -x; the sign bits are flipped back
+// on the packed codes).  It is within one binary32 ulp of fl32(x / d), so its
+// E2M1 code is the same unless it lies within two ulps of an E2M1 midpoint
+// (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5: significand bits 20..0 clear); those
+// quotients, and some harmless neighbours, take the IEEE division.
+__device__ __forceinline__ uint32_t e2m1_codes8(const float (&v)[8], float d)
+{
+    const float nr = -__frcp_rn(d);
+    uint32_t w = 0;
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) {
+        const float2 x2 = make_float2(v[k], v[k + 1]);
+        const float2 q0 = __fmul2_rn(x2, make_float2(nr, nr));
+        const float2 e = __ffma2_rn(make_float2(d, d), q0, x2);
+        float2 q = __ffma2_rn(e, make_float2(nr, nr), q0);
+        if (((__float_as_uint(q.x) + 2u) & 0x1FFFFFu) <= 4u)
+            q.x = -__fdiv_rn(v[k], d);
+        if (((__float_as_uint(q.y) + 2u) & 0x1FFFFFu) <= 4u)
+            q.y = -__fdiv_rn(v[k + 1], d);
+        const __nv_fp4x2_storage_t b = __nv_cvt_float2_to_fp4x2(q, __NV_E2M1, cudaRoundNearest);
+        w |= (uint32_t)b << (4 * k);
+    }
+    return w ^ 0x88888888u; // the codes of fl32(x / d)
+}
+
+// max |x| over the tensor, folded into *amax (a non-negative float compared as its bits)
+__global__ void __launch_bounds__(256) k_amax_bf16(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
+                                                   int64_t ldx, float *amax)
+{
+    const int64_t per_row = cols / 8;
+    float m = 0.0f;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < rows * per_row;
+         i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = i / per_row, c = (i - r * per_row) * 8;
+        float v[8];
+        unpack8(ldg_stream(x + r * ldx + c), v);
+        m = fmaxf(m, absmax8(v));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if ((threadIdx.x & 31) == 0 && m > 0.0f)
+        atomicMax(reinterpret_cast<unsigned *>(amax), __float_as_uint(m));
+}
+
+// quantizes the lane's chunk (8 values at column c) with scope scale s; the block
+// maximum is a lane-pair shuffle, so every lane of the warp calls it in step
+__device__ __forceinline__ void nvfp4_chunk(const float (&v)[8], bool in, float s, int64_t row, int64_t c,
+                                            int64_t cols, int lane, uint8_t *q, uint8_t *sb)
+{
+    const float own = absmax8(v);
+    const float ab = fmaxf(own, __shfl_xor_sync(0xFFFFFFFFu, own, 1));
+    uint32_t e = 0;
+    if (s > 0.0f)
+        e = __nv_cvt_float2_to_fp8x2(make_float2(__fdiv_rn(__fdiv_rn(ab, 6.0f), s), 0.0f), __NV_SATFINITE, __NV_E4M3) &
+            0xFFu;
+    const float d = __fmul_rn(e4m3_value(e), s);
+    const uint32_t codes = d != 0.0f ? e2m1_codes8(v, d) : 0u;
+    if (in) {
+        *reinterpret_cast<uint32_t *>(q + row * (cols / 2) + c / 2) = codes;
+        if ((lane & 1) == 0)
+            sb[row * (cols / 16) + c / 16] = (uint8_t)e;
+    }
+}
+
+// One warp per row, two passes over it in 256-column steps (its maximum, then
+// the quantization; the second read mostly hits L1).  A lane past the row's end
+// holds zeros and stores nothing (cols % 16 == 0 keeps both lanes of a block
+// pair on the same side).  Holding a row in registers between the passes cut
+// the warps per SM and measured slower.
+template <bool PER_ROW>
+__global__ void __launch_bounds__(256) k_quant_nvfp4(const uint16_t *__restrict__ x, int64_t rows, int64_t cols,
+                                                     int64_t ldx, const float *scope_amax, uint8_t *__restrict__ q,
+                                                     uint8_t *__restrict__ sb, float *__restrict__ sg)
+{
+    const int lane = threadIdx.x & 31;
+    const int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (row >= rows)
+        return;
+    const uint16_t *xr = x + row * ldx;
+    float amax;
+    if (PER_ROW) {
+        float m = 0.0f;
+        for (int64_t c = (int64_t)lane * 8; c < cols; c += 256) {
+            float v[8];
+            unpack8(__ldg(reinterpret_cast<const uint4 *>(xr + c)), v);
+            m = fmaxf(m, absmax8(v));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1)
+            m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        amax = m;
+    } else {
+        amax = __ldg(scope_amax);
+    }
+    const float s = __fdiv_rn(amax, 2688.0f);
+    if (lane == 0 && (PER_ROW || row == 0))
+        sg[PER_ROW ? row : 0] = s;
+    for (int64_t c0 = 0; c0 < cols; c0 += 256) {
+        const int64_t c = c0 + lane * 8;
+        const bool in = c < cols;
+        float v[8];
+        unpack8(in ? __ldg(reinterpret_cast<const uint4 *>(xr + c)) : make_uint4(0, 0, 0, 0), v);
+        nvfp4_chunk(v, in, s, row, c, cols, lane, q, sb);
+    }
+}
+
+// BF16 of e2m1 * decode(e_b) * S_g, rounded once (bf16_of_product on the exact
+// binary32 product e2m1 * decode(e_b)).  Grid (column segments of 2048, groups
+// of kDqRows rows): thread t converts elements 8t .. 8t+7 of its segment in
+// each row of the group, the group's loads issued together.
+constexpr int kDqRows = 8;
+
+__global__ void __launch_bounds__(256) k_dequant_nvfp4(const uint8_t *__restrict__ q, const uint8_t *__restrict__ sb,
+                                                       const float *__restrict__ sg, int per_row, int64_t rows,
+                                                       int64_t cols, uint16_t *__restrict__ out, int64_t ldo)
+{
+    const int64_t r0 = (int64_t)blockIdx.y * kDqRows;
+    const int64_t c = (int64_t)blockIdx.x * 2048 + threadIdx.x * 8;
+    if (c >= cols)
+        return;
+    uint32_t w[kDqRows];
+    float bs[kDqRows], s[kDqRows];
+#pragma unroll
+    for (int i = 0; i < kDqRows; ++i) {
+        const int64_t r = r0 + i;
+        const bool in = r < rows;
+        w[i] = in ? __ldg(reinterpret_cast<const uint32_t *>(q + r * (cols / 2) + c / 2)) : 0u;
+        bs[i] = in ? e4m3_value(__ldg(sb + r * (cols / 16) + c / 16)) : 0.0f;
+        s[i] = in ? __ldg(sg + (per_row ? r : 0)) : 0.0f;
+    }
+#pragma unroll
+    for (int i = 0; i < kDqRows; ++i) {
+        if (r0 + i >= rows)
+            break;
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            const __half2_raw hr =
+                __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((w[i] >> (4 * k)) & 0xFFu), __NV_E2M1);
+            const float2 e2 = __half22float2(*reinterpret_cast<const __half2 *>(&hr));
+            o[k / 2] = bf16_of_product(__fmul_rn(e2.x, bs[i]), s[i]) |
+                       (bf16_of_product(__fmul_rn(e2.y, bs[i]), s[i]) << 16);
+        }
+        *reinterpret_cast<uint4 *>(out + (r0 + i) * ldo + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 int64_t groups_upper_bound(int64_t n, const int64_t *seg, int nseg)
 {
     const int64_t g = (n + 127) / 128;
@@ -1511,6 +1677,48 @@ cudaError_t launch_requant_col(const RequantArgs &a, cudaStream_t st)
         return cudaSuccess;
     dim3 grid((unsigned)groups_upper_bound(a.n, a.seg, a.nseg), (unsigned)(a.c / 128));
     k_requant_col<<<grid, kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_amax_bf16(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, float *amax,
+                             cudaStream_t st)
+{
+    if (rows == 0)
+        return cudaSuccess;
+    const int64_t threads = rows * (cols / 8), cap = 4 * (int64_t)sm_count();
+    const int64_t blocks = (threads + 255) / 256;
+    k_amax_bf16<<<(unsigned)(blocks < cap ? blocks : cap), 256, 0, st>>>(x, rows, cols, ldx, amax);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quant_nvfp4(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, const float *scope_amax,
+                               uint8_t *q, uint8_t *sb, float *sg, cudaStream_t st)
+{
+    if (rows == 0)
+        return cudaSuccess;
+    const int64_t blocks = (rows + 7) / 8;
+    if (blocks > 2147483647)
+        return cudaErrorInvalidValue;
+    if (scope_amax)
+        k_quant_nvfp4<false><<<(unsigned)blocks, 256, 0, st>>>(x, rows, cols, ldx, scope_amax, q, sb, sg);
+    else
+        k_quant_nvfp4<true><<<(unsigned)blocks, 256, 0, st>>>(x, rows, cols, ldx, nullptr, q, sb, sg);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_dequant_nvfp4(const uint8_t *q, const uint8_t *sb, const float *sg, int per_row, int64_t rows,
+                                 int64_t cols, uint16_t *out, int64_t ldo, cudaStream_t st)
+{
+    if (rows == 0)
+        return cudaSuccess;
+    // row groups on grid.y (at most 65535 per launch), column segments of 2048 on grid.x
+    constexpr int64_t kRowsPerLaunch = (int64_t)65535 * kDqRows;
+    for (int64_t r0 = 0; r0 < rows; r0 += kRowsPerLaunch) {
+        const int64_t nr = rows - r0 < kRowsPerLaunch ? rows - r0 : kRowsPerLaunch;
+        dim3 grid((unsigned)((cols + 2047) / 2048), (unsigned)((nr + kDqRows - 1) / kDqRows));
+        k_dequant_nvfp4<<<grid, 256, 0, st>>>(q + r0 * (cols / 2), sb + r0 * (cols / 16), per_row ? sg + r0 : sg,
+                                              per_row, nr, cols, out + r0 * ldo, ldo);
+    }
     return cudaGetLastError();
 }
 

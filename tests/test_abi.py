@@ -96,5 +96,10 @@ def test_validation_happens_before_cuda(L):
                                          None) == 2
     assert L.jetq_quant_act_1x128_swiglu(fake, P(4104), 4, 128, 128, 128, fake, fake, None, None, 0, None, 0,
                                          None) == 3
+    # NVFP4: columns not a multiple of 16, misaligned packed codes, bad scope flag
+    assert L.jetq_quant_nvfp4(fake, 4, 40, 40, None, fake, fake, fake, None) == 2
+    assert L.jetq_quant_nvfp4(fake, 4, 32, 32, None, P(4098), fake, fake, None) == 3
+    assert L.jetq_dequant_nvfp4_bf16(fake, fake, fake, 2, 4, 32, fake, 32, None) == 1
+    assert L.jetq_amax_bf16(fake, 4, 12, 12, fake, None) == 2
     # MX: columns not a multiple of 128
     assert L.jetq_quant_mx32(fake, 4, 96, 96, fake, fake, None, None, 0, None, 0, None) == 2
