@@ -15,7 +15,9 @@ value  = GEMM FLOPs of the step / wall time of the whole step (quantizers
          included), TFLOP/s, inputs resident; every step touches ~1.07 GB of
          inputs, several times the 129 MB L2.
 e2e    = the same through host buffers: each step copies its BF16 inputs from
-         pinned host memory and reads the three FP32 weight gradients back.
+         pinned host memory and reads the three FP32 weight gradients back
+         (copy streams overlap one step's copies with the neighbouring steps'
+         compute; every copy is inside the timed region).
 roofline = the dominant kernel (the FProp/DGrad GEMM kernel) against the FP8
          dense peak (measured BF16 cuBLAS peak x 2, the nominal FP8/BF16 ratio).
 
@@ -189,19 +191,23 @@ class Step:
             self.t[k].view(torch.int16).copy_(src.view(torch.int16) if isinstance(v, torch.Tensor) else src,
                                               non_blocking=non_blocking)
 
-    def run(self, stream=None, time_gemms=False):
+    def run(self, stream=None, time_gemms=False, inputs=None, dw=None):
+        """The step on `inputs` (device BF16 tensors, default self.t), weight gradients into
+        `dw` (default self.dw)."""
         import torch
 
         jq = self.jq
+        t_in = self.t if inputs is None else inputs
+        dw_out = self.dw if dw is None else dw
         launches = 0
         for name in ("w_gate", "w_up", "w_down"):
             q, s, qT, sT = self.w[name]
-            jq.jetq_quant_w_128x128(self.t[name], q, s, qT, sT, stream)
+            jq.jetq_quant_w_128x128(t_in[name], q, s, qT, sT, stream)
             launches += 1
 
         def qa(name):
             a = self.act[name]
-            jq.jetq_quant_act_1x128(self.t[name], a["q_row"], a["s_row"], a["q_col"], a["s_col"], a["cap"],
+            jq.jetq_quant_act_1x128(t_in[name], a["q_row"], a["s_row"], a["q_col"], a["s_col"], a["cap"],
                                     None, 0, stream)
 
         def timed(fn):
@@ -240,7 +246,7 @@ class Step:
             d, c = a["q_col"].shape[0], xa["q_col"].shape[0]
             timed(lambda a=a, xa=xa, g=g, d=d, c=c: jq.jetq_gemm_wgrad(
                 jq.RECIPE_BLOCK128, a["q_col"], a["s_col"], xa["q_col"], xa["s_col"], N_TOK, a["cap"], d, c,
-                self.dw[g], False, stream))
+                dw_out[g], False, stream))
             launches += 1
         return launches
 
@@ -678,29 +684,62 @@ def run_ours(args):
     gemm_ms = [a.elapsed_time(b) for a, b in step.gemm_events]
     step.gemm_events.clear()
 
-    # ---- e2e: pinned host inputs in, weight gradients out, every step
+    # ---- e2e: pinned host inputs in, weight gradients out, every step.  Two device
+    # buffer sets: step i+1's inputs are copied in (and step i-1's gradients out) on
+    # copy streams while step i computes; events order every buffer's reuse, and the
+    # timed region spans every step's copies.
     pinned = {k: torch.from_numpy(np.ascontiguousarray(v).view(np.int16)).pin_memory() for k, v in inputs.items()}
-    dw_host = {g: torch.empty(t.shape, dtype=t.dtype).pin_memory() for g, t in step.dw.items()}
     h2d = sum(v.numel() * 2 for v in pinned.values())
     d2h = sum(t.numel() * 4 for t in step.dw.values())
-    for _ in range(max(1, args.warmup // 2)):
-        step.load(pinned, non_blocking=True)
-        step.run()
-        for g, t in step.dw.items():
-            dw_host[g].copy_(t, non_blocking=True)
+    t_sets = [step.t, {k: torch.empty_like(v) for k, v in step.t.items()}]
+    dw_sets = [step.dw, {g: torch.empty_like(t) for g, t in step.dw.items()}]
+    dw_host = [{g: torch.empty(t.shape, dtype=t.dtype).pin_memory() for g, t in step.dw.items()} for _ in range(2)]
+    h2d_s, d2h_s = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def e2e_steps(n):
+        comp_done, d2h_done = [None, None], [None, None]
+        start = torch.cuda.Event()
+        start.record(stream)
+        h2d_s.wait_event(start)
+        for i in range(n):
+            b = i % 2
+            if comp_done[b] is not None:
+                h2d_s.wait_event(comp_done[b])  # the step that last read set b has finished
+            with torch.cuda.stream(h2d_s):
+                for k, v in pinned.items():
+                    t_sets[b][k].view(torch.int16).copy_(v, non_blocking=True)
+            loaded = torch.cuda.Event()
+            loaded.record(h2d_s)
+            stream.wait_event(loaded)
+            if d2h_done[b] is not None:
+                stream.wait_event(d2h_done[b])  # set b's previous gradients have left
+            step.run(inputs=t_sets[b], dw=dw_sets[b])
+            done = torch.cuda.Event()
+            done.record(stream)
+            comp_done[b] = done
+            d2h_s.wait_event(done)
+            with torch.cuda.stream(d2h_s):
+                for g, t in dw_sets[b].items():
+                    dw_host[b][g].copy_(t, non_blocking=True)
+            out = torch.cuda.Event()
+            out.record(d2h_s)
+            d2h_done[b] = out
+        for ev in d2h_done:
+            if ev is not None:
+                stream.wait_event(ev)
+
+    e2e_steps(max(2, args.warmup // 2))
     torch.cuda.synchronize()
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _ in range(args.steps):
-        step.load(pinned, non_blocking=True)
-        step.run()
-        for g, t in step.dw.items():
-            dw_host[g].copy_(t, non_blocking=True)
+    e2e_steps(args.steps)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
     ms_e2e = e0.elapsed_time(e1)
+    if step.jq.jetq_check_device_error() != 0:
+        raise RuntimeError("device error word set during the e2e steps")
 
     # ---- reduce over ranks (max time)
     t = torch.tensor([ms_total, ms_e2e], dtype=torch.float64, device=dev)
@@ -772,7 +811,7 @@ def run_ours(args):
     }
     if rank == 0:
         if not args.no_extras:
-            del step, pinned, dw_host
+            del step, pinned, dw_host, t_sets, dw_sets
             torch.cuda.empty_cache()
             peaks_now = _peaks()
             line["decode"] = measure_decode(dev, peaks_now)
