@@ -139,6 +139,17 @@ def _rank_env():
     return rank, world, local
 
 
+def _max_over_ranks(values, dev, world):
+    """Each value's maximum over the ranks of the process group (the slowest replica
+    sets the job's time); the values themselves when running alone."""
+    import torch
+
+    t = torch.tensor(values, dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in t]
+
+
 def _inputs_host(seed: int):
     """The step's BF16 inputs as numpy uint16 arrays (synthetic, seeded)."""
     import synth
@@ -742,10 +753,7 @@ def run_ours(args):
         raise RuntimeError("device error word set during the e2e steps")
 
     # ---- reduce over ranks (max time)
-    t = torch.tensor([ms_total, ms_e2e], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    ms_total, ms_e2e = float(t[0]), float(t[1])
+    ms_total, ms_e2e = _max_over_ranks([ms_total, ms_e2e], dev, world)
     flops = GEMM_FLOP * GEMMS_PER_STEP * args.steps * world
     value = flops / (ms_total * 1e-3) / 1e12
     e2e = flops / (ms_e2e * 1e-3) / 1e12
