@@ -39,6 +39,40 @@ def test_library_exports_every_declared_symbol(L):
         assert hasattr(L, name), name
 
 
+def _declarations():
+    text = open(HEADER).read()
+    out = {}
+    for name, params in re.findall(r"JETQ_API\s+[\w\s\*]+?\b(jetq_\w+)\s*\(([^;]*?)\)\s*;", text, re.S):
+        p = " ".join(params.split())
+        out[name] = [] if p in ("", "void") else [x.strip() for x in p.split(",")]
+    return out
+
+
+def _ctype_of(param):
+    """The ctypes type the binding must pass for one C parameter declaration."""
+    if "*" in param:
+        return ctypes.c_void_p
+    base = param.rsplit(" ", 1)[0].replace("const ", "").strip()
+    if base in re.findall(r"}\s*(jetq_\w+)\s*;", open(HEADER).read()):  # the header's enums
+        return ctypes.c_int
+    return {"int64_t": ctypes.c_int64, "int": ctypes.c_int, "float": ctypes.c_float, "uint64_t": ctypes.c_uint64}[base]
+
+
+def test_binding_matches_every_declaration(L):
+    """The ctypes binding passes exactly the parameters the header declares, with
+    matching widths (a pointer, a 64-bit or 32-bit integer, a float)."""
+    decl = _declarations()
+    assert decl, "no declarations parsed"
+    for name, params in decl.items():
+        fn = getattr(L, name)
+        assert fn.argtypes is not None, name
+        assert len(fn.argtypes) == len(params), (name, len(fn.argtypes), len(params))
+        for got, param in zip(fn.argtypes, params):
+            want = _ctype_of(param)
+            assert ctypes.sizeof(got) == ctypes.sizeof(want), (name, param, got, want)
+            assert (got is ctypes.c_float) == (want is ctypes.c_float), (name, param)
+
+
 def test_status_strings_and_sizes(L):
     import rollout_x128_act_gb300 as jq
 
