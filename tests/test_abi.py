@@ -130,6 +130,20 @@ def test_validation_happens_before_cuda(L):
                                          None) == 2
     assert L.jetq_quant_act_1x128_swiglu(fake, P(4104), 4, 128, 128, 128, fake, fake, None, None, 0, None, 0,
                                          None) == 3
+    # re-quantizer: channels not a multiple of 128; column copy too short
+    assert L.jetq_requant_col_from_row(fake, fake, 4, 100, fake, fake, 128, None, 0, None) == 2
+    assert L.jetq_requant_col_from_row(fake, fake, 300, 128, fake, fake, 256, None, 0, None) == 2
+    # dequantizer: unknown scale layout; 128x128 blocks need rows % 128 == 0
+    assert L.jetq_dequant_bf16(fake, fake, 4, 128, 5, fake, 128, None) == 1
+    assert L.jetq_dequant_bf16(fake, fake, 100, 128, 1, fake, 128, None) == 2
+    # power-of-two weight blocks: a transposed copy without its scales
+    assert L.jetq_quant_w_128x128_pow2(fake, 128, 128, 128, fake, fake, fake, None, None) == 1
+    # grouped GEMM: unknown kind; more than 256 experts
+    #   (kind, recipe, a, sa, b, sb, m, n, k, ldk, seg_offsets, num_experts, out, out_dtype, ldo, accumulate, stream)
+    assert L.jetq_gemm_grouped(7, 0, fake, fake, fake, fake, 128, 128, 128, 128, fake, 4, fake, 0, 128, 0,
+                               None) == 1
+    assert L.jetq_gemm_grouped(0, 0, fake, fake, fake, fake, 128, 128, 128, 128, fake, 300, fake, 0, 128, 0,
+                               None) == 2
     # NVFP4: columns not a multiple of 16, misaligned packed codes, bad scope flag
     assert L.jetq_quant_nvfp4(fake, 4, 40, 40, None, fake, fake, fake, None) == 2
     assert L.jetq_quant_nvfp4(fake, 4, 32, 32, None, P(4098), fake, fake, None) == 3
