@@ -822,12 +822,12 @@ __global__ void __launch_bounds__(kThreads, 2)
 // RMSNorm statistics, one warp per row.  Lane l sums the 128-column groups
 // l, l + 32, ... (each left to right by fma); the group sums are then added
 // left to right by every lane through shuffles, so the binary32 result
-// follows one fixed order: rstd = 1 / sqrt(total / c + eps).  A round of 32
+// follows one fixed order: rstd = 1 / sqrt(total / c + eps).  A batch of 32
 // groups (8 KB) is loaded coalesced (one warp load = 512 contiguous bytes)
 // and regrouped through shared memory, each group padded to 272 bytes so that
 // both the regrouping stores and the per-lane group reads are conflict-free.
-// Warps walk rows grid-stride; the next round's loads are in flight while the
-// current round is summed.
+// Warps walk rows grid-stride; the next batch's loads are in flight while the
+// current batch is summed.
 constexpr int kRmsWarps = 4;
 constexpr int kRmsPitch = 272;
 
@@ -842,7 +842,7 @@ __global__ void __launch_bounds__(kRmsWarps * 32) k_rms_rstd(const uint16_t *__r
         return;
     uint8_t *sw = stage[warp];
     const int groups = (int)(c >> 7);
-    // round (row, g0): its live * 16 chunks of 16 bytes; chunk q is slot q % 16 of group q / 16
+    // batch (row, g0): its live * 16 chunks of 16 bytes; chunk q is slot q % 16 of group q / 16
     uint4 raw[16];
     auto load = [&](int64_t r, int g0) {
         const uint4 *xr = reinterpret_cast<const uint4 *>(x + r * ldx) + (int64_t)g0 * 16;
@@ -884,7 +884,7 @@ __global__ void __launch_bounds__(kRmsWarps * 32) k_rms_rstd(const uint16_t *__r
                     part = __fmaf_rn(v[j], v[j], part);
             }
         }
-        __syncwarp(); // every lane has read its group before the next round is staged
+        __syncwarp(); // every lane has read its group before the next batch is staged
         for (int j = 0; j < live; ++j)
             total = __fadd_rn(total, __shfl_sync(0xFFFFFFFFu, part, j));
         if (ng0 == 0) {
