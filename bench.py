@@ -19,7 +19,10 @@ e2e    = the same through host buffers: each step copies its BF16 inputs from
          (copy streams overlap one step's copies with the neighbouring steps'
          compute; every copy is inside the timed region).
 roofline = the dominant kernel (the FProp/DGrad GEMM kernel) against the FP8
-         dense peak (measured BF16 cuBLAS peak x 2, the nominal FP8/BF16 ratio).
+         dense peak: the measured burst BF16 cuBLAS peak x 2 (the nominal
+         FP8/BF16 ratio), because the timed region lasts well under a second
+         at full clock; the sustained figure (measured at a lower clock under
+         the power cap) is reported beside it.
 
 --impl reference times the CPU oracle (oracle/) on a bounded sample of the same
 workload on the host cores.  Multi-GPU (torchrun): independent replicas, one
@@ -759,6 +762,8 @@ def run_ours(args):
     e2e = flops / (ms_e2e * 1e-3) / 1e12
 
     peaks = _peaks()
+    # the timed region is a fraction of a second at full clock: the burst peak applies
+    fp8_peak = 2.0 * peaks["bf16"]
     fp8_peak_sust = 2.0 * peaks["bf16_sust"]
     # per GEMM kind: [fprop x3, dgrad x3, wgrad x3] per step
     per = {"fprop": [], "dgrad": [], "wgrad": []}
@@ -792,19 +797,21 @@ def run_ours(args):
             "kernel": "k_gemm_b128<256,8,4,2,block-scaled B> (FProp/DGrad, training shape)",
             "bound": "tensor",
             "achieved": round(achieved, 1),
-            "peak": round(fp8_peak_sust, 1),
+            "peak": round(fp8_peak, 1),
             "unit": "TFLOP/s",
-            "frac": round(achieved / fp8_peak_sust, 4),
+            "frac": round(achieved / fp8_peak, 4),
             "traffic": traffic,
-            "peak_note": f"FP8 dense = 2 x {peaks['src']} sustained BF16 cuBLAS ({peaks['bf16_sust']} TFLOP/s), "
-                         "the nominal FP8/BF16 ratio",
+            "peak_note": f"FP8 dense = 2 x {peaks['src']} burst BF16 cuBLAS ({peaks['bf16']} TFLOP/s), the nominal "
+                         f"FP8/BF16 ratio; the timed region lasts {ms_total:.0f} ms at the sampled clock "
+                         f"(frac of measured)",
+            "frac_of_sustained": round(achieved / fp8_peak_sust, 4),
         },
         "gemm": {
             "fprop_dgrad_ms": round(avg_blk, 4), "wgrad_ms": round(avg_wg, 4),
             "fprop_dgrad_tflops": round(achieved, 1),
             "wgrad_tflops": round(GEMM_FLOP / (avg_wg * 1e-3) / 1e12, 1),
             "gemm_only_tflops": round(GEMM_FLOP * GEMMS_PER_STEP / (gemm_only_ms * 1e-3) / 1e12, 1),
-            "frac_of_fp8_peak_burst": round(achieved / (2.0 * peaks["bf16"]), 4),
+            "wgrad_frac_of_fp8_peak": round(GEMM_FLOP / (avg_wg * 1e-3) / 1e12 / fp8_peak, 4),
         },
         "quantizers": {
             "bytes_per_step": quant_bytes_per_step(),

@@ -120,8 +120,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void *src, uint32_
                  : "memory");
 }
 
-// Tiled 2-D load delivered to the same shared-memory offset, and completed on
-// the same mbarrier offset, in every CTA of the cluster named in cta_mask.
 // 3-D tiled load: coordinates (x, y, z) in the map's element units
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y, int z)
 {
@@ -129,16 +127,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap *map
                  " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
                  "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
                  : "memory");
-}
-
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y,
-                                                      uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-        : "memory");
 }
 
 __device__ __forceinline__ uint32_t cluster_ctarank()
@@ -260,15 +248,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar)
 {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
-}
-
-// As mma_commit, arriving on the mbarrier at the same offset in every CTA of cta_mask.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
-        "h"(cta_mask)
-        : "memory");
 }
 
 // 32 lanes x 32 consecutive 32-bit columns: thread i of the warp gets lane
