@@ -36,6 +36,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cstring>
 #include <mutex>
 
 #include "jetq_internal.h"
@@ -50,6 +51,7 @@ __device__ unsigned g_gemm_error;
 namespace {
 
 constexpr unsigned kErrTimeout = 1u;
+constexpr unsigned kErrLayout = 2u;
 constexpr unsigned long long kWaitLimitNs = 2000000000ull; // 2 s per wait
 
 struct KParams {
@@ -66,13 +68,36 @@ struct KParams {
     int64_t out_e_stride;   // elements between experts' outputs (grouped K)
     int out_bf16;
     int accumulate;
+    int tma_out;            // BF16 tiles leave through the output tensor map
     unsigned long long limit_ns;
 };
 
 __host__ __device__ constexpr int gcd_int(int a, int b) { return b ? gcd_int(b, a % b) : a; }
 __host__ __device__ constexpr int lcm_int(int a, int b) { return a / gcd_int(a, b) * b; }
 
-template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, int A_STRIDE_MAX = 16384, int KBP = 1>
+// Epilogue of the narrow decode tiles: 16-column TMEM loads, the next one in
+// flight while the current one is folded; 2 KB per-warp store staging.
+struct EpiNarrow {
+    static constexpr bool kWide = false;
+    static constexpr int LDX = 16, REG_WG0 = 0, REG_EPI = 0, DEPTH = 1;
+    static constexpr int TMA_OUT = 0;
+};
+
+// Epilogue of the training tiles: the producer/MMA warpgroup hands registers
+// to the epilogue warpgroups (REG_WG0 / REG_EPI per thread); TMEM is read in
+// groups of DEPTH loads of LDX columns per wait; the K-blocks' scales arrive
+// in a shared-memory ring filled ahead by warp 2 (per-thread asynchronous
+// copies), so no global load sits on the fold's path; tiles leave through
+// TMA stores of 32-row x 64-byte boxes from a per-warp staging area.
+template <int LDX_, int DEPTH_, int REG_WG0_, int REG_EPI_>
+struct EpiWide {
+    static constexpr bool kWide = true;
+    static constexpr int LDX = LDX_, DEPTH = DEPTH_, REG_WG0 = REG_WG0_, REG_EPI = REG_EPI_;
+    static constexpr int TMA_OUT = 1;
+};
+
+template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, int A_STRIDE_MAX = 16384, int KBP = 1,
+          bool PER_ROW_B = false, class E = EpiNarrow>
 struct Cfg {
     static constexpr int kABytes = 128 * 128;
     static constexpr int kBBytes = BN * 128;
@@ -89,37 +114,64 @@ struct Cfg {
     static constexpr int kThreads = 128 + 32 * EPI_WARPS;
     static constexpr int kCols = BN / (EPI_WARPS / 4); // accumulator columns per epilogue thread
     static constexpr int kTmemCols = 512;
-    static constexpr int kSbSlots = 4;                 // column-scale ring (WGrad)
+    // scale ring: narrow tiles, WGrad column scales only (bulk copies); training
+    // tiles, each slot the K-block's 128 row scales then its column scales
+    // (per-row B) or weight-block scales (4 floats)
+    static constexpr int kSbSlots = E::kWide ? 8 : 4;
+    static constexpr int kSlotFloats = E::kWide ? 128 + (PER_ROW_B ? BN : 4) : BN;
     static constexpr int kBars = 2 * STAGES + 2 * TMEM_BUFS + 2 * kSbSlots + 1;
-    static constexpr size_t kSbBytes = (size_t)kSbSlots * BN * 4;
-    // output staging: 32 rows x 64 bytes per epilogue warp, for coalesced stores
-    static constexpr size_t kStageOutBytes = (size_t)EPI_WARPS * 2048;
-    static constexpr size_t kSmem = 1024 + (size_t)kARegion + (size_t)STAGES * KBP * kBBytes + kSbBytes + 1024 +
-                                    sizeof(GroupTables) + 128 + kStageOutBytes;
+    static constexpr size_t kSbBytes =
+        (E::kWide || PER_ROW_B) ? ((size_t)kSbSlots * kSlotFloats * 4 + 1023) / 1024 * 1024 : 0;
+    // output staging per epilogue warp: 32 rows x 64 bytes (the stores' unit)
+    static constexpr size_t kStgWarp = 2048;
+    static constexpr size_t kStageOutBytes = (size_t)EPI_WARPS * kStgWarp;
+    // layout: barriers (512 B) and group tables first, then 1024-aligned tiles,
+    // the column-scale ring and the output staging.  With TMA stores the size
+    // assumes the dynamic shared memory starts on a 1024-byte boundary (the
+    // kernel checks that the layout fits before it touches anything).
+    static constexpr size_t kFront = 512 + sizeof(GroupTables);
+    static constexpr size_t kFrontAligned = (kFront + 1023) / 1024 * 1024;
+    static constexpr size_t kSmem = kFrontAligned + (size_t)kARegion + (size_t)STAGES * KBP * kBBytes + kSbBytes +
+                                    kStageOutBytes + (E::TMA_OUT ? 0 : 1024);
+    static_assert(!E::kWide || (KBP == 1 && kCols % 64 == 0 && kCols % (E::LDX * E::DEPTH) == 0 &&
+                                (kSlotFloats * 4) % 16 == 0),
+                  "wide epilogue");
+    static_assert(!E::kWide || E::REG_WG0 == 0 ||
+                      E::REG_WG0 * 128 + E::REG_EPI * 32 * EPI_WARPS <= 65536, "register split exceeds the SM");
     static_assert(TMEM_BUFS * BN <= kTmemCols, "TMEM buffers exceed 512 columns");
     static_assert(EPI_WARPS % 4 == 0 && kCols % 32 == 0, "epilogue split");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "MMA N for M = 128");
-    static_assert(kBars * 8 + 16 <= 1024, "barrier area");
+    static_assert(kBars * 8 + 16 <= 512, "barrier area");
+    static_assert(kSbBytes % 1024 == 0, "staging alignment");
+    static_assert(E::kWide || !PER_ROW_B, "per-row B scales are folded by the training-tile epilogue");
     static_assert(A_STRIDE_MAX % 1024 == 0 && A_STRIDE_MAX <= kABytes, "A stages on 1024-byte swizzle atoms");
     static_assert(kSmem <= 232448, "shared memory");
 };
 
-template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B, int A_STRIDE_MAX, int KBP, int PF>
+template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B, int A_STRIDE_MAX, int KBP, int PF,
+          class E>
 __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
-    k_gemm_b128(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p)
+    k_gemm_b128(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                const __grid_constant__ CUtensorMap tmO, const KParams p)
 {
-    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS, A_STRIDE_MAX, KBP>;
+    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS, A_STRIDE_MAX, KBP, PER_ROW_B, E>;
     constexpr int SB = C::kSbSlots;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *tiles_a = ptx::align_smem<1024>(smem_raw);
-    uint8_t *tiles_b = tiles_a + C::kARegion;
-    float *sb_ring = reinterpret_cast<float *>(tiles_b + (size_t)STAGES * KBP * C::kBBytes);
-    uint64_t *bars = reinterpret_cast<uint64_t *>(reinterpret_cast<uint8_t *>(sb_ring) + C::kSbBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem_raw);
     uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + C::kBars);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-    GroupTables *gt = reinterpret_cast<GroupTables *>(reinterpret_cast<uint8_t *>(bars) + 1024);
-    uint8_t *stage_out = reinterpret_cast<uint8_t *>(gt + 1);
-    stage_out += (128u - (ptx::smem_addr(stage_out) & 127u)) & 127u;
+    GroupTables *gt = reinterpret_cast<GroupTables *>(smem_raw + 512);
+    uint8_t *tiles_a = ptx::align_smem<1024>(smem_raw + C::kFront);
+    uint8_t *tiles_b = tiles_a + C::kARegion;
+    float *sb_ring = reinterpret_cast<float *>(tiles_b + (size_t)STAGES * KBP * C::kBBytes);
+    uint8_t *stage_out = reinterpret_cast<uint8_t *>(sb_ring) + C::kSbBytes;
+    // the layout must fit the allocation (it does unless the dynamic shared
+    // memory starts far off a 1024-byte boundary): otherwise report and stop
+    if (ptx::smem_addr(stage_out + C::kStageOutBytes) - ptx::smem_addr(smem_raw) > (uint32_t)C::kSmem) {
+        if (threadIdx.x == 0)
+            atomicOr(&g_gemm_error, kErrLayout);
+        return;
+    }
 
     const uint32_t bar0 = ptx::smem_addr(bars);
     auto full = [&](int s) { return bar0 + 8u * s; };
@@ -144,7 +196,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             ptx::mbar_init(tempty(b), EPI_WARPS * 32); // every epilogue thread arrives
         }
         for (int s = 0; s < SB; ++s) {
-            ptx::mbar_init(sfull(s), 1);
+            ptx::mbar_init(sfull(s), E::kWide ? 32 : 1); // training tiles: one cp.async arrival per lane
             ptx::mbar_init(sempty(s), EPI_WARPS * 32);
         }
         ptx::mbar_init(done, 1);
@@ -166,6 +218,12 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int num_tiles = total_tiles(sc, gt);
+    if constexpr (E::REG_WG0 > 0) {
+        if (warp < 4)
+            ptx::setmaxnreg_dec<E::REG_WG0>();
+        else
+            ptx::setmaxnreg_inc<E::REG_EPI>();
+    }
 
     if (warp < 4) {
         if (warp == 0 && lane == 0) {
@@ -258,54 +316,234 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             }
             ptx::mma_commit(done);
             ptx::mbar_wait(done, 0u, abort_flag, err, kErrTimeout, p.limit_ns, false);
-        } else if (PER_ROW_B && warp == 2 && lane == 0) {
-            // -------------------------------------------------- column-scale producer
-            // one bulk copy per K-block: Sb[kb, n0 .. n0 + BN) into a ring slot
+        } else if (E::kWide && warp == 2) {
+            // -------------------------------------------------- scale producer (training tiles)
+            // Per K-block: the tile's 128 row scales and its column scales (per-row B:
+            // BN of them) or weight-block scales, copied by the 32 lanes with cp.async
+            // into a ring slot; each lane's copies complete as one arrival on sfull.
             uint32_t it = 0;
             bool ok = true;
             for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
                 const TileInfo ti = get_tile(sc, gt, t);
-                const uint32_t bytes = (uint32_t)((sc.N - ti.n0 < BN ? sc.N - ti.n0 : BN) * 4);
                 for (int kb = 0; kb < ti.num_kb; ++kb, ++it) {
-                    const int s = (int)(it % SB);
-                    const uint32_t ph = (it / SB) & 1u;
-                    if (!ptx::mbar_wait(sempty(s), ph ^ 1u, abort_flag, err, kErrTimeout, p.limit_ns)) {
+                    const int slot = (int)(it % SB);
+                    if (!ptx::mbar_wait(sempty(slot), ((it / SB) & 1u) ^ 1u, abort_flag, err, kErrTimeout,
+                                        p.limit_ns)) {
                         ok = false;
                         break;
                     }
-                    ptx::mbar_arrive_expect_tx(sfull(s), bytes);
-                    ptx::bulk_load(ptx::smem_addr(sb_ring + (size_t)s * BN),
-                                   p.sb + (int64_t)(ti.kb0 + kb) * sc.N + ti.n0, bytes, sfull(s));
+                    const int kbg = ti.kb0 + kb;
+                    float *ring = sb_ring + (size_t)slot * C::kSlotFloats;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int64_t m = (int64_t)ti.a_row0 + lane + 32 * i;
+                        const bool in = m < sc.M;
+                        ptx::cp_async_4(ptx::smem_addr(ring + lane + 32 * i),
+                                        p.sa + (in ? (int64_t)kbg * p.sa_ld + m : 0), in ? 4u : 0u);
+                    }
+                    if constexpr (PER_ROW_B) {
+                        for (int c4 = lane; c4 < BN / 4; c4 += 32) {
+                            const int n = ti.n0 + 4 * c4;
+                            const bool in = n < sc.N; // N is a multiple of 64
+                            ptx::cp_async_16(ptx::smem_addr(ring + 128 + 4 * c4),
+                                             p.sb + (in ? (int64_t)kbg * sc.N + n : 0), in ? 16u : 0u);
+                        }
+                    } else {
+                        if (lane < BN / 128) {
+                            const int n = ti.n0 + 128 * lane;
+                            const bool in = n < sc.N;
+                            ptx::cp_async_4(ptx::smem_addr(ring + 128 + lane),
+                                            p.sb + (in ? ti.e * p.sb_e_stride + (int64_t)(n >> 7) * p.kb_total + kbg
+                                                       : 0),
+                                            in ? 4u : 0u);
+                        }
+                    }
+                    ptx::cp_async_mbar_arrive(sfull(slot));
                 }
             }
-            for (int s = 0; s < SB; ++s) {
-                if (it > (uint32_t)s) {
-                    const uint32_t last = (uint32_t)s + ((it - 1u - (uint32_t)s) / SB) * SB;
-                    ptx::mbar_wait(sfull(s), (last / SB) & 1u, abort_flag, err, kErrTimeout, p.limit_ns, false);
-                }
-            }
+            ptx::cp_async_wait_all();
         }
         __syncwarp();
-    } else {
-        // ------------------------------------------------------ epilogue
+    } else if constexpr (E::kWide) {
+        // ------------------------------------------------------ epilogue (training tiles)
+        constexpr int LDX = E::LDX;
+        constexpr int GC = LDX * E::DEPTH;   // columns per TMEM wait
+        constexpr int NGR = C::kCols / GC;
         const int ew = warp - 4;
         const int quarter = warp & 3; // TMEM lanes 32*quarter .. +31
         const int col0 = (ew >> 2) * C::kCols;
         const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
+        uint8_t *stg = stage_out + (size_t)ew * C::kStgWarp;
 
-        // scales of the next K-block (possibly of the next tile), loaded one K-block ahead
-        float sa_n = 0.0f, sb_n = 0.0f;
-        auto load_first = [&](const TileInfo &ti) {
-            const int64_t m = (int64_t)ti.a_row0 + quarter * 32 + lane;
+        uint32_t tb = 0; // K-blocks folded so far (TMEM buffer tb % TMEM_BUFS, scale slot tb % SB)
+        bool ok = true;
+        bool stored = false; // a TMA store of this warp may still be reading the staging area
+        for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
+            const TileInfo ti = get_tile(sc, gt, t);
+            const int64_t mw = (int64_t)ti.a_row0 + quarter * 32; // the warp's first row
             const int n0 = ti.n0 + col0;
-            sa_n = (m < sc.M && ti.num_kb > 0) ? __ldg(p.sa + (int64_t)ti.kb0 * p.sa_ld + m) : 0.0f;
-            if (!PER_ROW_B)
-                sb_n = (n0 < sc.N && ti.num_kb > 0)
-                           ? __ldg(p.sb + ti.e * p.sb_e_stride + (int64_t)(n0 >> 7) * p.kb_total + ti.kb0)
-                           : 0.0f;
-        };
-        if (PF == 1 && (int)blockIdx.x < num_tiles)
-            load_first(get_tile(sc, gt, blockIdx.x));
+            const bool col_ok = n0 < sc.N; // a slice past N (N % BN != 0) computes nothing it stores
+            float2 acc[C::kCols / 2];
+#pragma unroll
+            for (int j = 0; j < C::kCols / 2; ++j)
+                acc[j] = make_float2(0.0f, 0.0f);
+
+            for (int kb = 0; kb < ti.num_kb; ++kb) {
+                const int b = (int)(tb % TMEM_BUFS);
+                const int slot = (int)(tb % SB);
+                bool got = ptx::mbar_wait(sfull(slot), (tb / SB) & 1u, abort_flag, err, kErrTimeout, p.limit_ns);
+                got = got && ptx::mbar_wait(tfull(b), (tb / TMEM_BUFS) & 1u, abort_flag, err, kErrTimeout, p.limit_ns);
+                if (!__all_sync(0xFFFFFFFFu, got)) { // keep the warp converged for tcgen05.ld
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const float *ring = sb_ring + (size_t)slot * C::kSlotFloats;
+                const float sa = ring[quarter * 32 + lane];
+                const float *sbs = ring + 128 + col0;              // per-row B: this slice's column scales
+                const float s = PER_ROW_B ? 0.0f : __fmul_rn(sa, ring[128 + (col0 >> 7)]);
+                const uint32_t tbase = tmem_base + lane_addr + (uint32_t)(b * BN + col0);
+                uint32_t Q[GC];
+#pragma unroll
+                for (int gr = 0; gr < NGR; ++gr) {
+#pragma unroll
+                    for (int d = 0; d < E::DEPTH; ++d)
+                        ptx::tmem_ld_x(tbase + (uint32_t)(gr * GC + d * LDX),
+                                       *reinterpret_cast<uint32_t(*)[LDX]>(&Q[d * LDX]));
+                    ptx::tmem_ld_wait_tie(Q);
+                    if (gr == NGR - 1) {
+                        // every load of buffer b has completed: hand it back to the MMA
+                        ptx::tc_fence_before();
+                        ptx::mbar_arrive(tempty(b));
+                    }
+                    if constexpr (PER_ROW_B) {
+#pragma unroll
+                        for (int q = 0; q < GC / 4; ++q) {
+                            const float4 sb4 = *reinterpret_cast<const float4 *>(sbs + gr * GC + 4 * q);
+                            const float2 s01 = __fmul2_rn(make_float2(sa, sa), make_float2(sb4.x, sb4.y));
+                            const float2 s23 = __fmul2_rn(make_float2(sa, sa), make_float2(sb4.z, sb4.w));
+                            float2 &a0 = acc[gr * (GC / 2) + 2 * q];
+                            float2 &a1 = acc[gr * (GC / 2) + 2 * q + 1];
+                            a0 = __ffma2_rn(make_float2(__uint_as_float(Q[4 * q]), __uint_as_float(Q[4 * q + 1])), s01,
+                                            a0);
+                            a1 = __ffma2_rn(make_float2(__uint_as_float(Q[4 * q + 2]), __uint_as_float(Q[4 * q + 3])),
+                                            s23, a1);
+                        }
+                    } else {
+                        const float2 s2 = make_float2(s, s);
+#pragma unroll
+                        for (int h = 0; h < GC / 2; ++h)
+                            acc[gr * (GC / 2) + h] = __ffma2_rn(
+                                make_float2(__uint_as_float(Q[2 * h]), __uint_as_float(Q[2 * h + 1])), s2,
+                                acc[gr * (GC / 2) + h]);
+                    }
+                }
+                ptx::mbar_arrive(sempty(slot)); // the slot's scales have been read
+                ++tb;
+            }
+            if (!ok)
+                break;
+
+            // ---- store the tile: passes of 64 bytes per row (32 BF16 or 16 FP32 columns),
+            // each written into the warp's staging area with its 16-byte chunks swizzled by
+            // row (the 64-byte swizzle of the output tensor map: conflict-free), then stored
+            // by one TMA box of 32 rows, or (rows past a problem's end, accumulation) read
+            // back as 8 rows x 64 contiguous bytes per store instruction
+            const bool tma = p.tma_out && !p.accumulate && col_ok &&
+                             (mw + 32 <= ti.m_end || (ti.m_end == sc.M && sc.mode != kGroupedK));
+            const int64_t out_row0 = (sc.mode == kGroupedK ? (int64_t)ti.e * sc.M : 0) + mw;
+            auto pass = [&](int px, auto chunk, auto store) {
+                if (stored) {
+                    // the previous box must have been read before the area is rewritten
+                    if (lane == 0)
+                        ptx::bulk_wait_group_read0();
+                    __syncwarp();
+                    stored = false;
+                }
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+                    *reinterpret_cast<uint4 *>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = chunk(c);
+                if (tma) {
+                    ptx::fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) {
+                        ptx::tma_store_2d(&tmO, ptx::smem_addr(stg), px, (int)out_row0);
+                        ptx::bulk_commit_group();
+                    }
+                    stored = true;
+                } else {
+                    __syncwarp();
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int pc = lane + 32 * i, r = pc >> 2, c = pc & 3;
+                        const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+                        if (col_ok && mw + r < ti.m_end)
+                            store(mw + r, c, v);
+                    }
+                    __syncwarp();
+                }
+            };
+            if (p.out_bf16) {
+#pragma unroll
+                for (int ps = 0; ps < C::kCols / 32; ++ps) // 32 BF16 columns a pass
+                    pass(
+                        n0 + ps * 32,
+                        [&](int c) {
+                            uint32_t w[4];
+#pragma unroll
+                            for (int h = 0; h < 4; ++h) {
+                                const float2 a = acc[ps * 16 + 4 * c + h];
+                                const __nv_bfloat162 b2 = __floats2bfloat162_rn(a.x, a.y);
+                                w[h] = *reinterpret_cast<const uint32_t *>(&b2);
+                            }
+                            return make_uint4(w[0], w[1], w[2], w[3]);
+                        },
+                        [&](int64_t row, int c, const uint4 &v) {
+                            *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + row * p.ldo + n0 +
+                                                       ps * 32 + c * 8) = v;
+                        });
+            } else if (!p.accumulate) {
+#pragma unroll
+                for (int ps = 0; ps < C::kCols / 16; ++ps) // 16 FP32 columns a pass
+                    pass(
+                        n0 + ps * 16,
+                        [&](int c) {
+                            const float2 a = acc[ps * 8 + 2 * c], b2 = acc[ps * 8 + 2 * c + 1];
+                            return make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(b2.x),
+                                              __float_as_uint(b2.y));
+                        },
+                        [&](int64_t row, int c, const uint4 &v) {
+                            *reinterpret_cast<uint4 *>(reinterpret_cast<float *>(p.out) + ti.e * p.out_e_stride +
+                                                       row * p.ldo + n0 + ps * 16 + c * 4) = v;
+                        });
+            } else {
+                const int64_t m = mw + lane;
+                if (m < ti.m_end && col_ok) {
+                    float *o = reinterpret_cast<float *>(p.out) + ti.e * p.out_e_stride + m * p.ldo + n0;
+#pragma unroll
+                    for (int j4 = 0; j4 < C::kCols / 4; ++j4) {
+                        float4 v = make_float4(acc[2 * j4].x, acc[2 * j4].y, acc[2 * j4 + 1].x, acc[2 * j4 + 1].y);
+                        const float4 old = *reinterpret_cast<const float4 *>(o + 4 * j4);
+                        v.x = __fadd_rn(old.x, v.x);
+                        v.y = __fadd_rn(old.y, v.y);
+                        v.z = __fadd_rn(old.z, v.z);
+                        v.w = __fadd_rn(old.w, v.w);
+                        *reinterpret_cast<float4 *>(o + 4 * j4) = v;
+                    }
+                }
+            }
+        }
+        // every TMA store of this warp must complete before the CTA exits
+        if (lane == 0)
+            ptx::bulk_wait_group0();
+        __syncwarp();
+    } else {
+        // ------------------------------------------------------ epilogue (narrow decode tiles)
+        static_assert(!PER_ROW_B && BN < 128 && PF > 1, "narrow epilogue: decode tiles only");
+        const int ew = warp - 4;
+        const int quarter = warp & 3; // TMEM lanes 32*quarter .. +31
+        const int col0 = (ew >> 2) * C::kCols;
+        const uint32_t lane_addr = (uint32_t)(quarter * 32) << 16;
 
         uint32_t tb = 0;
         bool ok = true;
@@ -323,28 +561,24 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             for (int j = 0; j < C::kCols / 2; ++j)
                 acc[j] = make_float2(0.0f, 0.0f);
 
-            // fold one K-block's accumulator buffer into acc with scale s (row scale sa for PER_ROW_B);
-            // buffers come in groups of KBP, one group per stage, waited for at the group's
-            // first K-block and released after its last
-            // (use = false: a K-block past the tile's end, whose buffer only passes through)
-            auto fold = [&](float sa, float s, bool use) -> bool {
+            // fold one K-block's accumulator buffer into acc with scale s; buffers come in
+            // groups of KBP, one group per stage, waited for at the group's first K-block and
+            // released after its last (use = false: a K-block past the tile's end, whose
+            // buffer only passes through)
+            auto fold = [&](float s, bool use) -> bool {
                 constexpr int NG = TMEM_BUFS / KBP;
                 const int j = (int)(tb % KBP);
                 const int gi = (int)((tb / KBP) % NG);
                 const int b = (int)(tb % TMEM_BUFS);
-                const int slot = (int)(tb % SB);
                 bool got = true;
                 if (j == 0)
                     got = ptx::mbar_wait(tfull(gi), ((tb / KBP) / NG) & 1u, abort_flag, err, kErrTimeout, p.limit_ns);
-                if (PER_ROW_B)
-                    got = got && ptx::mbar_wait(sfull(slot), (tb / SB) & 1u, abort_flag, err, kErrTimeout, p.limit_ns);
                 if (!__all_sync(0xFFFFFFFFu, got)) // keep the warp converged for tcgen05.ld
                     return false;
                 ptx::tc_fence_after();
-                const float *sbs = sb_ring + (size_t)slot * BN + col0;
-                // 16-column chunks, the next one in flight while the current one is folded (decode
-                // slices: a warp whose 32 rows are all past the tile's rows has nothing to keep)
-                if (use && (BN > 64 || ti.a_row0 + quarter * 32 < ti.m_end)) {
+                // 16-column chunks, the next one in flight while the current one is folded (a
+                // warp whose 32 rows are all past the tile's rows has nothing to keep)
+                if (use && ti.a_row0 + quarter * 32 < ti.m_end) {
                     constexpr int NCH = C::kCols / 16;
                     uint32_t PP[2][16];
                     const uint32_t tbase = tmem_base + lane_addr + (uint32_t)(b * BN + col0);
@@ -355,147 +589,53 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                         if (ch + 1 < NCH)
                             ptx::tmem_ld_32x32b_x16(tbase + (uint32_t)((ch + 1) * 16), PP[(ch + 1) & 1]);
                         const uint32_t (&P)[16] = PP[ch & 1];
-                        if constexpr (PER_ROW_B) {
+                        const float2 s2 = make_float2(s, s);
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const float4 sb4 = *reinterpret_cast<const float4 *>(sbs + ch * 16 + 4 * q);
-                                const float2 s01 = __fmul2_rn(make_float2(sa, sa), make_float2(sb4.x, sb4.y));
-                                const float2 s23 = __fmul2_rn(make_float2(sa, sa), make_float2(sb4.z, sb4.w));
-                                float2 &a0 = acc[ch * 8 + 2 * q];
-                                float2 &a1 = acc[ch * 8 + 2 * q + 1];
-                                a0 = __ffma2_rn(make_float2(__uint_as_float(P[4 * q]), __uint_as_float(P[4 * q + 1])), s01, a0);
-                                a1 = __ffma2_rn(make_float2(__uint_as_float(P[4 * q + 2]), __uint_as_float(P[4 * q + 3])), s23, a1);
-                            }
-                        } else {
-                            const float2 s2 = make_float2(s, s);
-#pragma unroll
-                            for (int h = 0; h < 8; ++h)
-                                acc[ch * 8 + h] = __ffma2_rn(
-                                    make_float2(__uint_as_float(P[2 * h]), __uint_as_float(P[2 * h + 1])), s2, acc[ch * 8 + h]);
-                        }
+                        for (int h = 0; h < 8; ++h)
+                            acc[ch * 8 + h] = __ffma2_rn(
+                                make_float2(__uint_as_float(P[2 * h]), __uint_as_float(P[2 * h + 1])), s2, acc[ch * 8 + h]);
                         if (ch + 1 < NCH)
                             ptx::tmem_ld_wait_regs(PP[(ch + 1) & 1]);
                     }
                 }
                 ptx::tc_fence_before();
-                // the column-scale slot was read through the generic proxy and the next
-                // bulk copy into it writes through the async proxy: every reader orders
-                // its reads before that write with a proxy fence ahead of the release
-                if (PER_ROW_B)
-                    ptx::fence_proxy_async_smem();
                 if (j == KBP - 1)
                     ptx::mbar_arrive(tempty(gi));
-                if (PER_ROW_B)
-                    ptx::mbar_arrive(sempty(slot));
                 ++tb;
                 return true;
             };
-            if constexpr (PF == 1) {
-                for (int kb = 0; kb < ti.num_kb; ++kb) {
-                    const float sa = sa_n;
-                    const float s = PER_ROW_B ? 0.0f : __fmul_rn(sa, sb_n);
-                    if (kb + 1 < ti.num_kb) {
-                        const int kn = ti.kb0 + kb + 1;
-                        sa_n = load_ok ? __ldg(sa_ptr + (int64_t)kn * p.sa_ld) : 0.0f;
-                        if (!PER_ROW_B)
-                            sb_n = col_ok ? __ldg(sb_ptr + kn) : 0.0f;
-                    } else if (t + (int)gridDim.x < num_tiles) {
-                        load_first(get_tile(sc, gt, t + gridDim.x));
-                    }
-                    if (!fold(sa, s, true)) {
-                        ok = false;
-                        break;
-                    }
-                }
-            } else {
-                // the scales of PF K-blocks in flight: a decode slice spends too little
-                // time per K-block to hide one global load behind the next
-                float qa[PF], qb[PF];
+            // the scales of PF K-blocks in flight: a decode slice spends too little
+            // time per K-block to hide one global load behind the next
+            float qa[PF], qb[PF];
+#pragma unroll
+            for (int u = 0; u < PF; ++u) {
+                const bool in = u < ti.num_kb;
+                qa[u] = in && load_ok ? __ldg(sa_ptr + (int64_t)(ti.kb0 + u) * p.sa_ld) : 0.0f;
+                qb[u] = in && col_ok ? __ldg(sb_ptr + ti.kb0 + u) : 0.0f;
+            }
+            for (int kb0 = 0; kb0 < ti.num_kb && ok; kb0 += PF) {
 #pragma unroll
                 for (int u = 0; u < PF; ++u) {
-                    const bool in = u < ti.num_kb;
-                    qa[u] = in && load_ok ? __ldg(sa_ptr + (int64_t)(ti.kb0 + u) * p.sa_ld) : 0.0f;
-                    qb[u] = !PER_ROW_B && in && col_ok ? __ldg(sb_ptr + ti.kb0 + u) : 0.0f;
-                }
-                for (int kb0 = 0; kb0 < ti.num_kb && ok; kb0 += PF) {
-#pragma unroll
-                    for (int u = 0; u < PF; ++u) {
-                        const int kb = kb0 + u;
-                        if (kb < ti.num_kb && ok) {
-                            const float sa = qa[u];
-                            const float s = PER_ROW_B ? 0.0f : __fmul_rn(sa, qb[u]);
-                            const int kn = kb + PF;
-                            if (kn < ti.num_kb) {
-                                qa[u] = load_ok ? __ldg(sa_ptr + (int64_t)(ti.kb0 + kn) * p.sa_ld) : 0.0f;
-                                if (!PER_ROW_B)
-                                    qb[u] = col_ok ? __ldg(sb_ptr + ti.kb0 + kn) : 0.0f;
-                            }
-                            ok = fold(sa, s, true);
+                    const int kb = kb0 + u;
+                    if (kb < ti.num_kb && ok) {
+                        const float s = __fmul_rn(qa[u], qb[u]);
+                        const int kn = kb + PF;
+                        if (kn < ti.num_kb) {
+                            qa[u] = load_ok ? __ldg(sa_ptr + (int64_t)(ti.kb0 + kn) * p.sa_ld) : 0.0f;
+                            qb[u] = col_ok ? __ldg(sb_ptr + ti.kb0 + kn) : 0.0f;
                         }
+                        ok = fold(s, true);
                     }
                 }
             }
             if constexpr (KBP > 1) {
                 const int padded = (ti.num_kb + KBP - 1) / KBP * KBP;
                 for (int kb = ti.num_kb; kb < padded && ok; ++kb)
-                    ok = fold(0.0f, 0.0f, false);
+                    ok = fold(0.0f, false);
             }
             if (!ok)
                 break;
-            if (BN >= 128 && (p.out_bf16 || !p.accumulate)) {
-                // through the warp's staging area: each thread writes 64 bytes of its row, then the
-                // warp stores 8 rows x 64 contiguous bytes per instruction (16-byte chunks swizzled
-                // by row so both the writes and the reads are free of bank conflicts)
-                uint8_t *stg = stage_out + (size_t)ew * 2048;
-                const int64_t mw = (int64_t)ti.a_row0 + quarter * 32; // the warp's first row
-                // one pass: the thread's 16 bytes of chunk c of its row, then the warp's 32 rows out
-                auto pass = [&](auto chunk, auto store) {
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        *reinterpret_cast<uint4 *>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = chunk(c);
-                    __syncwarp();
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        const int pc = lane + 32 * i, r = pc >> 2, c = pc & 3;
-                        const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
-                        if (col_ok && mw + r < ti.m_end)
-                            store(mw + r, c, v);
-                    }
-                    __syncwarp();
-                };
-                if (p.out_bf16) {
-#pragma unroll
-                    for (int ps = 0; ps < C::kCols / 32; ++ps) // 32 BF16 columns a pass
-                        pass(
-                            [&](int c) {
-                                uint32_t w[4];
-#pragma unroll
-                                for (int h = 0; h < 4; ++h) {
-                                    const float2 a = acc[ps * 16 + 4 * c + h];
-                                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(a.x, a.y);
-                                    w[h] = *reinterpret_cast<const uint32_t *>(&b2);
-                                }
-                                return make_uint4(w[0], w[1], w[2], w[3]);
-                            },
-                            [&](int64_t row, int c, const uint4 &v) {
-                                *reinterpret_cast<uint4 *>(reinterpret_cast<__nv_bfloat16 *>(p.out) + row * p.ldo + n0 +
-                                                           ps * 32 + c * 8) = v;
-                            });
-                } else {
-#pragma unroll
-                    for (int ps = 0; ps < C::kCols / 16; ++ps) // 16 FP32 columns a pass
-                        pass(
-                            [&](int c) {
-                                const float2 a = acc[ps * 8 + 2 * c], b2 = acc[ps * 8 + 2 * c + 1];
-                                return make_uint4(__float_as_uint(a.x), __float_as_uint(a.y), __float_as_uint(b2.x),
-                                                  __float_as_uint(b2.y));
-                            },
-                            [&](int64_t row, int c, const uint4 &v) {
-                                *reinterpret_cast<uint4 *>(reinterpret_cast<float *>(p.out) + ti.e * p.out_e_stride +
-                                                           row * p.ldo + n0 + ps * 16 + c * 4) = v;
-                            });
-                }
-            } else if (row_ok && col_ok) {
+            if (row_ok && col_ok) {
                 if (p.out_bf16) {
                     __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(p.out) + m * p.ldo + n0;
 #pragma unroll
@@ -510,7 +650,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                         *reinterpret_cast<uint4 *>(o + 8 * j8) = v;
                     }
                 } else {
-                    float *o = reinterpret_cast<float *>(p.out) + ti.e * p.out_e_stride + m * p.ldo + n0;
+                    float *o = reinterpret_cast<float *>(p.out) + m * p.ldo + n0;
 #pragma unroll
                     for (int j4 = 0; j4 < C::kCols / 4; ++j4) {
                         float4 v = make_float4(acc[2 * j4].x, acc[2 * j4].y, acc[2 * j4 + 1].x, acc[2 * j4 + 1].y);
@@ -593,6 +733,25 @@ cudaError_t make_bf16_tile_map(CUtensorMap *map, const void *base, int64_t cols,
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Output map for the training tiles' TMA stores: [rows x cols] of BF16 or
+// FP32, boxes of 64 bytes x 32 rows, 64-byte swizzle.
+cudaError_t make_store_map(CUtensorMap *map, const void *base, int64_t cols, int64_t rows, int64_t ld, bool bf16)
+{
+    EncodeTiledFn fn = encode_fn();
+    if (!fn)
+        return cudaErrorNotSupported;
+    const int esize = bf16 ? 2 : 4;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)ld * esize};
+    const cuuint32_t box[2] = {(cuuint32_t)(64 / esize), 32u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    const CUresult r =
+        fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void *>(base),
+           dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+           CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t make_kmajor_map(CUtensorMap *map, const void *base, int64_t k_extent, int64_t rows, int64_t ld,
                             int box_rows, int kb_per_box)
 {
@@ -628,11 +787,11 @@ cudaError_t make_kmajor_map(CUtensorMap *map, const void *base, int64_t k_extent
 namespace {
 
 template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, bool PER_ROW_B, int A_STRIDE_MAX = 16384, int KBP = 1,
-          int PF = 1>
+          int PF = 1, class E = EpiNarrow>
 cudaError_t run(const GemmProblem &g, cudaStream_t st)
 {
-    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS, A_STRIDE_MAX, KBP>;
-    auto kern = k_gemm_b128<BN, EPI_WARPS, STAGES, TMEM_BUFS, PER_ROW_B, A_STRIDE_MAX, KBP, PF>;
+    using C = Cfg<BN, EPI_WARPS, STAGES, TMEM_BUFS, A_STRIDE_MAX, KBP, PER_ROW_B, E>;
+    auto kern = k_gemm_b128<BN, EPI_WARPS, STAGES, TMEM_BUFS, PER_ROW_B, A_STRIDE_MAX, KBP, PF, E>;
     if (KBP > 1 && g.group != GroupKind::None)
         return cudaErrorInvalidValue; // multi-K-block boxes serve dense problems only
     static int configured_device = -1;
@@ -644,6 +803,16 @@ cudaError_t run(const GemmProblem &g, cudaStream_t st)
         if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)C::kSmem)) !=
             cudaSuccess)
             return e;
+        if constexpr (E::REG_WG0 > 0) {
+            // setmaxnreg.inc waits until the CTA's register pool can serve it: the
+            // launch must provide every warpgroup's share, or the kernel would stall
+            cudaFuncAttributes fa;
+            if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess)
+                return e;
+            if (fa.numRegs < E::REG_WG0 || fa.numRegs > E::REG_EPI ||
+                fa.numRegs * C::kThreads < E::REG_WG0 * 128 + E::REG_EPI * 32 * EPI_WARPS)
+                return cudaErrorInvalidConfiguration;
+        }
         configured_device = dev;
     }
     // an epilogue thread stores kCols consecutive columns once the first is in
@@ -693,6 +862,18 @@ cudaError_t run(const GemmProblem &g, cudaStream_t st)
     kp.out_bf16 = g.out_dtype == JETQ_OUT_BF16;
     kp.accumulate = g.accumulate;
     kp.limit_ns = kWaitLimitNs;
+    // output tiles leave by TMA when the output rows are 16-byte aligned (a
+    // grouped WGrad's experts are stacked: one map over their E x M rows)
+    CUtensorMap to;
+    memset(&to, 0, sizeof to);
+    kp.tma_out = 0;
+    if (E::TMA_OUT && !g.accumulate && (g.ldo * (kp.out_bf16 ? 2 : 4)) % 16 == 0 &&
+        (reinterpret_cast<uintptr_t>(g.out) & 15u) == 0) {
+        const int64_t rows = g.group == GroupKind::K ? g.M * g.num_experts : g.M;
+        if ((e = make_store_map(&to, g.out, g.N, rows, g.ldo, kp.out_bf16)) != cudaSuccess)
+            return e;
+        kp.tma_out = 1;
+    }
     int grid = sm_count();
     if (g.group == GroupKind::None) {
         const int tiles = s.mt * s.nt;
@@ -701,8 +882,23 @@ cudaError_t run(const GemmProblem &g, cudaStream_t st)
         const int tiles = s.mt * s.nt * g.num_experts;
         grid = tiles < grid ? tiles : grid;
     }
-    kern<<<grid, C::kThreads, C::kSmem, st>>>(ta, tbm, kp);
+    kern<<<grid, C::kThreads, C::kSmem, st>>>(ta, tbm, to, kp);
     return cudaGetLastError();
+}
+
+// FProp / DGrad training tiles: 128 x 256, 8 epilogue warps (one row x 128
+// columns a thread, 216 registers after the split), TMEM read in 32-column
+// groups (two 16-column loads per wait).
+cudaError_t run_train(const GemmProblem &g, cudaStream_t st)
+{
+    return run<256, 8, 4, 2, false, 16384, 1, 1, EpiWide<16, 2, 72, 216>>(g, st);
+}
+
+// WGrad (per-column B scales): 128 x 192 tiles folded by three epilogue
+// warpgroups (64 columns a thread, one 16-column TMEM load per wait).
+cudaError_t run_wgrad(const GemmProblem &g, cudaStream_t st)
+{
+    return run<192, 12, 4, 2, true, 16384, 1, 1, EpiWide<16, 1, 0, 0>>(g, st);
 }
 
 } // namespace
@@ -715,15 +911,15 @@ cudaError_t launch_gemm_block128(const GemmProblem &g, GemmShape shape, cudaStre
     // 192-column tiles folded by three epilogue warpgroups (64 columns a
     // thread, no register spills) and row scales two K-blocks ahead
     if (g.bscale == BScale::PerRow)
-        return run<192, 12, 4, 2, true, 16384, 1, 2>(g, st);
+        return run_wgrad(g, st);
     if (shape == GemmShape::Train)
-        return run<256, 8, 4, 2, false>(g, st);
+        return run_train(g, st);
     if (gemm_decode_swapped_applies(g))
         return launch_gemm_decode_swapped(g, st);
     // past the swapped kernel's 64 tokens the training tiles stream the weight
     // faster once they cover 32 CTAs (same per-element arithmetic either way)
     if (g.group == GroupKind::None && ((g.M + 127) / 128) * ((g.N + 255) / 256) >= 32)
-        return run<256, 8, 4, 2, false>(g, st);
+        return run_train(g, st);
     // decode: 32 weight rows per tile, four K-blocks per copy, scales eight
     // K-blocks ahead; a batch of up to 32 (64) tokens packs its A K-blocks
     // 4 KB (8 KB) apart

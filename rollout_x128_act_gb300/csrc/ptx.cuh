@@ -156,6 +156,75 @@ __device__ __forceinline__ void cluster_sync()
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Per-thread asynchronous copies global -> shared of 4 or 16 bytes; src_size
+// bytes are read (0 reads nothing) and the rest of the destination is zeroed.
+__device__ __forceinline__ void cp_async_4(uint32_t dst, const void *src, uint32_t src_size)
+{
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(src_size) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_16(uint32_t dst, const void *src, uint32_t src_size)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_size) : "memory");
+}
+
+// One arrival on the mbarrier once every cp.async this thread issued so far
+// has completed (the arrival is counted in the barrier's expected count).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared.b64 [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all()
+{
+    asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+// Tiled 2-D store shared -> global (bulk-group completion).  Elements outside
+// the tensor's bounds are not written; coordinates must be non-negative.
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, uint32_t src, int x, int y)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(src), "r"(x), "r"(y)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group()
+{
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Waits until every bulk group this thread committed has finished reading its
+// shared-memory source (the buffer may be overwritten).
+__device__ __forceinline__ void bulk_wait_group_read0()
+{
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Waits until every bulk group this thread committed has completed.
+__device__ __forceinline__ void bulk_wait_group0()
+{
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+
+// Register split between warpgroups: every warp of a warpgroup executes the
+// same instruction.  dec returns registers to the CTA's pool; inc waits until
+// the pool holds enough (the launch must have provided them).
+template <int N>
+__device__ __forceinline__ void setmaxnreg_dec()
+{
+    static_assert(N >= 24 && N <= 256 && N % 8 == 0, "setmaxnreg count");
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+template <int N>
+__device__ __forceinline__ void setmaxnreg_inc()
+{
+    static_assert(N >= 24 && N <= 256 && N % 8 == 0, "setmaxnreg count");
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
 __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap *map)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
@@ -294,6 +363,50 @@ __device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[16])
                  :
                  : "memory");
 }
+
+__device__ __forceinline__ void tmem_ld_wait_regs(uint32_t (&r)[32])
+{
+    asm volatile("tcgen05.wait::ld.sync.aligned;"
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// Ties 32 registers to the preceding instruction (no code): later uses of r
+// cannot move above it.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32])
+{
+    asm volatile(""
+                 : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                   "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                   "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                   "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                   "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+                 :
+                 : "memory");
+}
+
+// tcgen05.wait::ld tied to N (a multiple of 32, or 16) loaded registers.
+template <int N>
+__device__ __forceinline__ void tmem_ld_wait_tie(uint32_t (&r)[N])
+{
+    if constexpr (N == 16) {
+        tmem_ld_wait_regs(r);
+    } else {
+        static_assert(N % 32 == 0, "tie width");
+        tmem_ld_wait_regs(*reinterpret_cast<uint32_t(*)[32]>(&r[0]));
+#pragma unroll
+        for (int i = 32; i < N; i += 32)
+            reg_fence(*reinterpret_cast<uint32_t(*)[32]>(&r[i]));
+    }
+}
+
+__device__ __forceinline__ void tmem_ld_x(uint32_t taddr, uint32_t (&r)[16]) { tmem_ld_32x32b_x16(taddr, r); }
+__device__ __forceinline__ void tmem_ld_x(uint32_t taddr, uint32_t (&r)[32]) { tmem_ld_32x32b_x32(taddr, r); }
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
 // with 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart,
