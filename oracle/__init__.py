@@ -85,6 +85,8 @@ def _load():
         lib.jo_quant_nvfp4.restype = None
         lib.jo_dequant_nvfp4_bf16.argtypes = [P, P, P, I, I, ctypes.c_int, P]
         lib.jo_dequant_nvfp4_bf16.restype = None
+        lib.jo_dequant_nvfp4.argtypes = [P, P, P, I, I, ctypes.c_int, P]
+        lib.jo_dequant_nvfp4.restype = None
         for f in ("jo_fprop", "jo_dgrad", "jo_wgrad"):
             getattr(lib, f).argtypes = [P, P, I, I, I, P, I, P, P]
         for f in ("jo_quant_rowgroups", "jo_quant_colgroups", "jo_quant_blocks", "jo_quant_mx_rows",
@@ -437,11 +439,11 @@ def dequant_nvfp4_bf16(q, sb, sg):
 
 
 def dequant_nvfp4(q, sb, sg) -> np.ndarray:
-    """Exact binary64 values e2m1 * decode(e_b) * S_g."""
-    q = np.asarray(q, np.uint8)
-    codes = np.empty((q.shape[0], q.shape[1] * 2), np.uint8)
-    codes[:, 0::2] = q & 15
-    codes[:, 1::2] = q >> 4
-    s = np.asarray(sg, np.float64)
-    s = s[:, None] if s.size == q.shape[0] and s.size > 1 else s.reshape(1, 1)
-    return e2m1_decode(codes) * np.repeat(e4m3_decode(sb), 16, axis=1) * s
+    """Exact binary64 values e2m1 * decode(e_b) * S_g (per-row scales when sg has one entry per row)."""
+    q = _c(q, np.uint8)
+    sb = _c(sb, np.uint8)
+    sg = _c(sg, np.float32)
+    R, C = q.shape[0], q.shape[1] * 2
+    out = np.empty((R, C), np.float64)
+    _load().jo_dequant_nvfp4(_p(q), _p(sb), _p(sg), R, C, int(sg.size > 1), _p(out))
+    return out

@@ -829,6 +829,24 @@ void jo_quant_nvfp4(const uint16_t *x, int64_t rows, int64_t cols, int64_t ldx, 
     }
 }
 
+/* out = e2m1 * decode(e_b) * S_g in binary64 (exact: a 2-bit times a 4-bit
+ * times a 24-bit significand), the operand value the NVFP4 GEMM multiplies
+ * (Miles "Blackwell-native RL recipes", NVFP4 section: E2M1 values, one E4M3
+ * scale per 16 values, one FP32 scale for a larger scope).  Codes packed two
+ * per byte, element 2j in the low nibble; sg per row (per_row) or one. */
+void jo_dequant_nvfp4(const uint8_t *q, const uint8_t *sb, const float *sg, int64_t rows, int64_t cols,
+                      int per_row, double *out)
+{
+    int64_t r, c;
+    for (r = 0; r < rows; ++r)
+        for (c = 0; c < cols; ++c) {
+            uint8_t byte = q[r * (cols / 2) + c / 2];
+            uint8_t code = (c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15);
+            out[r * cols + c] =
+                jo_e2m1_decode(code) * jo_e4m3_decode(sb[r * (cols / 16) + c / 16]) * (double)sg[per_row ? r : 0];
+        }
+}
+
 /* out = BF16(e2m1 * decode(e_b) * S_g), rounded once: the product of a 2-bit,
  * a 4-bit and a 24-bit significand is exact in binary64. */
 void jo_dequant_nvfp4_bf16(const uint8_t *q, const uint8_t *sb, const float *sg, int64_t rows, int64_t cols,

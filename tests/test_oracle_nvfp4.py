@@ -122,3 +122,27 @@ def test_dequant_bf16_rounds_the_exact_product_once():
     down = np.nextafter(s, np.float32(0.0))
     assert np.all(oracle.dequant_nvfp4_bf16(q, sb, np.array([up], np.float32)) == 0x3FC2)
     assert np.all(oracle.dequant_nvfp4_bf16(q, sb, np.array([down], np.float32)) == 0x3FC1)
+
+
+def test_dequant_fp64_hand_values_and_bf16_relation():
+    """Hand values of the binary64 dequantizer (code x E4M3 scale x scope scale), the
+    nibble order (element 2j in the low nibble) and the per-row / per-tensor scope; its
+    BF16 rounding is the BF16 dequantizer's output."""
+    # byte 0x5A: element 0 = code 0xA (-1.0), element 1 = code 0x5 (3.0)
+    q = np.array([[0x5A] + [0x00] * 7, [0x71] + [0xFF] * 7], np.uint8)
+    sb = np.array([[0x40], [0x30]], np.uint8)   # E4M3 0x40 = 2.0, 0x30 = 0.5
+    sg = np.array([0.25, 3.0], np.float32)
+    d = oracle.dequant_nvfp4(q, sb, sg)
+    assert d[0, 0] == -1.0 * 2.0 * 0.25 and d[0, 1] == 3.0 * 2.0 * 0.25 and not d[0, 2:].any()
+    assert d[1, 0] == 0.5 * 0.5 * 3.0 and d[1, 1] == 6.0 * 0.5 * 3.0 and np.all(d[1, 2:] == -6.0 * 0.5 * 3.0)
+    dt = oracle.dequant_nvfp4(q, sb, np.array([0.25], np.float32))  # one tensor scope for every row
+    assert dt[1, 1] == 6.0 * 0.5 * 0.25
+    x = synth.activation(16, 128, seed=23, stream="test")
+    q, sb, sg = oracle.quant_nvfp4(x)
+    # binary64 -> BF16 rounded once (nearest, ties to even on the 7 kept fraction bits);
+    # the values are normal binary32 numbers, so the rounded double converts exactly
+    u = oracle.dequant_nvfp4(q, sb, sg).view(np.uint64)
+    lsb = (u >> np.uint64(45)) & np.uint64(1)
+    r = ((u + np.uint64((1 << 44) - 1) + lsb) >> np.uint64(45)) << np.uint64(45)
+    assert np.array_equal(synth.bf16_bits(r.view(np.float64).astype(np.float32)),
+                          oracle.dequant_nvfp4_bf16(q, sb, sg))
