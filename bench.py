@@ -515,8 +515,27 @@ def measure_nvfp4(dev):
     ms_q = _time(lambda: jq.jetq_quant_nvfp4(x, o["q"], o["sb"], o["sg"]), 20)
     ms_d = _time(lambda: jq.jetq_dequant_nvfp4_bf16(o["q"], o["sb"], o["sg"], True, out), 20)
     n = R * Cn
-    return {"quant_gbs": round((n * (2 + 0.5 + 1 / 16) + 4 * R) / (ms_q * 1e-3) / 1e9, 1), "quant_us": round(ms_q * 1e3, 1),
-            "dequant_gbs": round(n * (0.5 + 1 / 16 + 2) / (ms_d * 1e-3) / 1e9, 1), "dequant_us": round(ms_d * 1e3, 1)}
+    res = {"quant_gbs": round((n * (2 + 0.5 + 1 / 16) + 4 * R) / (ms_q * 1e-3) / 1e9, 1),
+           "quant_us": round(ms_q * 1e3, 1),
+           "dequant_gbs": round(n * (0.5 + 1 / 16 + 2) / (ms_d * 1e-3) / 1e9, 1), "dequant_us": round(ms_d * 1e3, 1)}
+    del out
+    # NVFP4 FProp (block-scaled FP4 MMA, per-token x tensor scope scales in the epilogue):
+    # the dense-8B gate projection, 8192 tokens x 4096 -> 12288, BF16 out
+    xa = act(N_TOK, C)
+    wq = act(D, C)
+    ga = jq.quant_nvfp4(xa)
+    ga["atoms"] = jq.nvfp4_atoms(ga["sb"], C)
+    gw = jq.quant_nvfp4(wq, scope_amax=jq.amax_bf16(wq))
+    gw["atoms"] = jq.nvfp4_atoms(gw["sb"], C)
+    y = torch.empty((N_TOK, D), dtype=torch.bfloat16, device=dev)
+    ms_g = _time(lambda: jq.jetq_gemm_nvfp4(ga["q"], ga["atoms"], ga["sg"], True, gw["q"], gw["atoms"], gw["sg"],
+                                            N_TOK, D, C, y), 20)
+    if jq.jetq_check_device_error() != 0:
+        raise RuntimeError("device error word set by the NVFP4 GEMM")
+    res["gemm"] = {"shape": f"{N_TOK}x{D}x{C}", "ms": round(ms_g, 4),
+                   "tflops": round(GEMM_FLOP / (ms_g * 1e-3) / 1e12, 1),
+                   "note": "FP4 dense nominal 13.5 PFLOP/s (3 x FP8); scope scales applied in the epilogue"}
+    return res
 
 
 def measure_rollout_step(dev, peaks):
@@ -922,6 +941,7 @@ PROFILE_CASES = {
     "quant_rmsnorm": "RMSNorm statistics + fused RMSNorm quantizer, X 32768 x 4096 BF16 (row + column copies)",
     "quant_swiglu": "fused SwiGLU quantizer, gate and up 8192 x 12288 BF16 (row + column copies)",
     "quant_nvfp4": "NVFP4 quantizer, per-token scope, 131072 routed rows x 2048 BF16",
+    "gemm_nvfp4": "NVFP4 FProp 4096 x 12288 x 4096 (per-token x tensor scope, BF16 out)",
 }
 
 
@@ -997,6 +1017,14 @@ def run_case(name: str, launches: int = 5):
     elif name == "quant_nvfp4":
         x = bf16(synth.activation(131072, 2048, seed=0, stream="x"))
         fn = lambda: jq.quant_nvfp4(x)  # noqa: E731
+    elif name == "gemm_nvfp4":
+        n, c, d = 4096, 4096, 12288
+        ga = jq.quant_nvfp4(bf16(synth.activation(n, c, seed=0, stream="x")))
+        ga["atoms"] = jq.nvfp4_atoms(ga["sb"], c)
+        wd = bf16(synth.weight(d, c, seed=0, stream="w_up"))
+        gw = jq.quant_nvfp4(wd, scope_amax=jq.amax_bf16(wd))
+        gw["atoms"] = jq.nvfp4_atoms(gw["sb"], c)
+        fn = lambda: jq.nvfp4_fprop(ga, gw, c, out_dtype=torch.bfloat16)  # noqa: E731
     elif name == "quant_mx":
         x = bf16(synth.activation(8192, 12288, seed=0, stream="h"))
         fn = lambda: jq.quant_mx(x)  # noqa: E731

@@ -454,6 +454,50 @@ JETQ_API jetq_status jetq_gemm_grouped(jetq_gemm_kind kind, jetq_recipe recipe,
                                        void *out, jetq_out_dtype out_dtype, int64_t ldo, int accumulate,
                                        void *stream);
 
+/* ======================================================================== */
+/* NVFP4 GEMM                                                               */
+/* ======================================================================== */
+/*
+ * Scale atoms of an NVFP4 payload with R rows and K columns (K a multiple of
+ * 256): the E4M3 block scales (one per row and 16 columns) regrouped into the
+ * 512-byte unit the tensor core's block-scaled FP4 MMA reads, one atom per
+ * 256-column K-block kb, 128-row band rb and 64-column step s:
+ *   RB = ceil(R / 128);  atom (kb, rb, s) at ((kb * RB + rb) * 4 + s) * 512
+ *   byte of (r, k) inside it: (r % 32) * 16 + ((r % 128) / 32) * 4 + (k % 64) / 16
+ * Rows past R in the last band are zero.
+ */
+JETQ_API int64_t jetq_nvfp4_atom_bytes(int64_t rows, int64_t k);
+
+/*
+ * Row-major block scales sb [rows x k/16] (as jetq_quant_nvfp4 writes them) ->
+ * scale atoms (layout above, jetq_nvfp4_atom_bytes(rows, k) bytes).  A pure
+ * byte permutation.  k % 256 == 0; sb and atoms 16-byte aligned.
+ */
+JETQ_API jetq_status jetq_nvfp4_scale_atoms(const uint8_t *sb, int64_t rows, int64_t k, uint8_t *atoms,
+                                            void *stream);
+
+/*
+ * NVFP4 FProp with the scope scales in the epilogue (Miles "Blackwell-native
+ * RL recipes" post, NVFP4 section: per-token FP32 scaling of the activations,
+ * which the post's training path applied as a separate operation instead of
+ * in a native per-token NVFP4 GEMM):
+ *   acc[i, j] = sum_k (e2m1(qa[i, k]) * e4m3(sba[i, k/16])) * (e2m1(qb[j, k]) * e4m3(sbb[j, k/16]))
+ *               (tensor core: block-scaled FP4 MMA, FP32 accumulation over all of K)
+ *   out[i, j] = fl32(fl32(sga[per_row_a ? i : 0] * sgb[0]) * acc[i, j]), F32 or BF16 (RNE of that)
+ *   qa    packed E2M1 codes of A [m x k/2] (activations: jetq_quant_nvfp4, element 2j
+ *         in the low nibble of byte j); sfa = its scale atoms (m, k); sga [m] (per-token
+ *         scope, per_row_a = 1) or [1]
+ *   qb    packed codes of B [n x k/2] (the weight, Y = X W^T); sfb = its atoms (n, k);
+ *         sgb [1] (tensor scope)
+ *   out   [m x n], row stride ldo
+ * Limits: m >= 0; n a multiple of 128; k a multiple of 256; qa, qb, sfa, sfb,
+ * out 16-byte aligned; sga, sgb 4-byte aligned.
+ */
+JETQ_API jetq_status jetq_gemm_nvfp4(const uint8_t *qa, const uint8_t *sfa, const float *sga, int per_row_a,
+                                     const uint8_t *qb, const uint8_t *sfb, const float *sgb,
+                                     int64_t m, int64_t n, int64_t k,
+                                     void *out, jetq_out_dtype out_dtype, int64_t ldo, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

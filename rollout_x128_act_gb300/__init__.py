@@ -71,6 +71,9 @@ def lib() -> ctypes.CDLL:
             "jetq_gemm_dgrad": (I32, [I32, P, P, P, P, I64, I64, I64, P, I32, I64, P]),
             "jetq_gemm_wgrad": (I32, [I32, P, P, P, P, I64, I64, I64, I64, P, I64, I32, P]),
             "jetq_gemm_grouped": (I32, [I32, I32, P, P, P, P, I64, I64, I64, I64, P, I32, P, I32, I64, I32, P]),
+            "jetq_nvfp4_atom_bytes": (I64, [I64, I64]),
+            "jetq_nvfp4_scale_atoms": (I32, [P, I64, I64, P, P]),
+            "jetq_gemm_nvfp4": (I32, [P, P, P, I32, P, P, P, I64, I64, I64, P, I32, I64, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -161,6 +164,19 @@ def jetq_dequant_nvfp4_bf16(q, sb, sg, per_row, out, stream=None):
     r, c = out.shape
     _check(lib().jetq_dequant_nvfp4_bf16(_p(q), _p(sb), _p(sg), int(per_row), r, c, _p(out), out.stride(0),
                                          _s(stream)), "jetq_dequant_nvfp4_bf16")
+
+
+def jetq_nvfp4_atom_bytes(rows: int, k: int) -> int:
+    return int(lib().jetq_nvfp4_atom_bytes(rows, k))
+
+
+def jetq_nvfp4_scale_atoms(sb, rows, k, atoms, stream=None):
+    _check(lib().jetq_nvfp4_scale_atoms(_p(sb), rows, k, _p(atoms), _s(stream)), "jetq_nvfp4_scale_atoms")
+
+
+def jetq_gemm_nvfp4(qa, sfa, sga, per_row_a, qb, sfb, sgb, m, n, k, out, stream=None):
+    _check(lib().jetq_gemm_nvfp4(_p(qa), _p(sfa), _p(sga), int(per_row_a), _p(qb), _p(sfb), _p(sgb), m, n, k,
+                                 _p(out), _out_dtype(out), out.stride(0), _s(stream)), "jetq_gemm_nvfp4")
 
 
 def jetq_quant_w_128x128(w, q, s, qT=None, sT=None, stream=None):
@@ -322,6 +338,23 @@ def dequant_nvfp4_bf16(q, sb, sg, stream=None):
     out = torch.empty((r, q.shape[1] * 2), dtype=torch.bfloat16, device=q.device)
     jetq_dequant_nvfp4_bf16(q, sb, sg, sg.numel() > 1, out, stream)
     return out
+
+
+def nvfp4_atoms(sb, k, stream=None):
+    """Scale atoms (the block-scaled FP4 MMA's layout) of row-major NVFP4 block scales sb [rows x k/16]."""
+    rows = sb.shape[0]
+    atoms = torch.empty(jetq_nvfp4_atom_bytes(rows, k), dtype=torch.uint8, device=sb.device)
+    jetq_nvfp4_scale_atoms(sb, rows, k, atoms, stream)
+    return atoms
+
+
+def nvfp4_fprop(a, b, k, out_dtype=torch.float32, stream=None):
+    """NVFP4 FProp of two quant_nvfp4 dicts (A: activations, B: weight), each with 'atoms' added."""
+    m, n = a["q"].shape[0], b["q"].shape[0]
+    y = torch.empty((m, n), dtype=out_dtype, device=a["q"].device)
+    jetq_gemm_nvfp4(a["q"], a["atoms"], a["sg"], a["sg"].numel() > 1, b["q"], b["atoms"], b["sg"], m, n, k, y,
+                    stream)
+    return y
 
 
 def quant_weight(w, transposed=True, stream=None):

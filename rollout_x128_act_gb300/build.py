@@ -16,7 +16,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libjetq.so")
-SOURCES = ["api.cu", "quant.cu", "gemm.cu", "gemm_mx.cu", "gemm_decode.cu"]
+SOURCES = ["api.cu", "quant.cu", "gemm.cu", "gemm_mx.cu", "gemm_decode.cu", "gemm_nvfp4.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
          "--diag-suppress", "177"]

@@ -113,12 +113,57 @@ int64_t jetq_mx_scale_bytes(int64_t rows, int64_t k)
     return (rows + 127) / 128 * ((k + 127) / 128) * 512;
 }
 
+int64_t jetq_nvfp4_atom_bytes(int64_t rows, int64_t k)
+{
+    if (rows <= 0 || k <= 0)
+        return 0;
+    return (rows + 127) / 128 * ((k + 255) / 256) * 4 * 512;
+}
+
+jetq_status jetq_nvfp4_scale_atoms(const uint8_t *sb, int64_t rows, int64_t k, uint8_t *atoms, void *stream)
+{
+    JQ_REQUIRE(rows >= 0 && k > 0, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(k % 256 == 0, JETQ_ERR_UNSUPPORTED_SHAPE);
+    if (rows == 0)
+        return JETQ_OK;
+    JQ_REQUIRE(sb != nullptr && atoms != nullptr, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(aligned16(sb) && aligned16(atoms), JETQ_ERR_MISALIGNED);
+    const jetq_status a = check_arch();
+    if (a != JETQ_OK)
+        return a;
+    return from_cuda(launch_nvfp4_atoms(sb, rows, k, atoms, static_cast<cudaStream_t>(stream)));
+}
+
+jetq_status jetq_gemm_nvfp4(const uint8_t *qa, const uint8_t *sfa, const float *sga, int per_row_a,
+                            const uint8_t *qb, const uint8_t *sfb, const float *sgb, int64_t m, int64_t n, int64_t k,
+                            void *out, jetq_out_dtype out_dtype, int64_t ldo, void *stream)
+{
+    JQ_REQUIRE(m >= 0 && n > 0 && k > 0 && (per_row_a == 0 || per_row_a == 1), JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(out_dtype == JETQ_OUT_F32 || out_dtype == JETQ_OUT_BF16, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(n % 128 == 0 && k % 256 == 0 && ldo >= n, JETQ_ERR_UNSUPPORTED_SHAPE);
+    if (m == 0)
+        return JETQ_OK;
+    JQ_REQUIRE(qa != nullptr && sfa != nullptr && sga != nullptr && qb != nullptr && sfb != nullptr &&
+                   sgb != nullptr && out != nullptr,
+               JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(aligned16(qa) && aligned16(qb) && aligned16(sfa) && aligned16(sfb) &&
+                   (reinterpret_cast<uintptr_t>(sga) & 3u) == 0 && (reinterpret_cast<uintptr_t>(sgb) & 3u) == 0 &&
+                   aligned16(out) && ldo % (out_dtype == JETQ_OUT_F32 ? 4 : 8) == 0,
+               JETQ_ERR_MISALIGNED);
+    const jetq_status a = check_arch();
+    if (a != JETQ_OK)
+        return a;
+    Nvfp4GemmProblem g{qa, sfa, sga, per_row_a, qb, sfb, sgb, m, n, k, out, ldo, out_dtype};
+    return from_cuda(launch_gemm_nvfp4(g, static_cast<cudaStream_t>(stream)));
+}
+
 jetq_status jetq_check_device_error(void *stream)
 {
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     unsigned word = 0;
     if (gemm_read_and_clear_error(st, &word) != cudaSuccess || gemm_mx_read_and_clear_error(st, &word) != cudaSuccess ||
-        gemm_decode_read_and_clear_error(st, &word) != cudaSuccess || quant_read_and_clear_error(st, &word) != cudaSuccess)
+        gemm_decode_read_and_clear_error(st, &word) != cudaSuccess || quant_read_and_clear_error(st, &word) != cudaSuccess ||
+        gemm_nvfp4_read_and_clear_error(st, &word) != cudaSuccess)
         return JETQ_ERR_CUDA;
     return word ? JETQ_ERR_TIMEOUT : JETQ_OK;
 }

@@ -177,6 +177,25 @@ cudaError_t launch_quant_nvfp4(const uint16_t *x, int64_t rows, int64_t cols, in
 cudaError_t launch_dequant_nvfp4(const uint8_t *q, const uint8_t *sb, const float *sg, int per_row, int64_t rows,
                                  int64_t cols, uint16_t *out, int64_t ldo, cudaStream_t st);
 
+// NVFP4 FProp: packed E2M1 operands [M x K/2], [N x K/2] bytes, scale atoms
+// (include/jetq.h layout), FP32 scope scales applied in the epilogue.
+struct Nvfp4GemmProblem {
+    const uint8_t *a;
+    const uint8_t *sfa;
+    const float *sga;
+    int per_row_a;
+    const uint8_t *b;
+    const uint8_t *sfb;
+    const float *sgb;
+    int64_t M, N, K;
+    void *out;
+    int64_t ldo;
+    jetq_out_dtype out_dtype;
+};
+cudaError_t launch_gemm_nvfp4(const Nvfp4GemmProblem &p, cudaStream_t st);
+cudaError_t launch_nvfp4_atoms(const uint8_t *sb, int64_t rows, int64_t k, uint8_t *atoms, cudaStream_t st);
+cudaError_t gemm_nvfp4_read_and_clear_error(cudaStream_t st, unsigned *out);
+
 // TMA descriptor for a BF16 matrix [rows x cols], row stride ld elements:
 // 128 x 128 boxes (32 KB, rows of 256 bytes, no swizzle), zero fill out of bounds.
 cudaError_t make_bf16_tile_map(CUtensorMap *map, const void *base, int64_t cols, int64_t rows, int64_t ld);
