@@ -923,17 +923,14 @@ __device__ __forceinline__ void transpose8x8(const uint2 (&in)[8], uint2 (&out)[
 }
 
 // Weight quantizer: one scale per 128x128 block, codes + transposed codes.
-__global__ void __launch_bounds__(kThreads, 2) k_quant_weight(WeightQuantArgs a)
+// One 128 x 128 weight block (rows d0.., columns c0..), the thread's 8 x 8
+// block in v; red (8 floats) and tileT (16 KB) are the CTA's shared scratch.
+// Leaves with every thread past the block's last shared-memory access.
+__device__ __forceinline__ void quant_weight_tile(const WeightQuantArgs &a, float *red, uint8_t *tileT,
+                                                  const float (&v)[8][8], int64_t d0, int64_t c0)
 {
-    __shared__ float red[8];
-    __shared__ __align__(16) uint8_t tileT[128 * 128];
-
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int rg = t >> 4, cc = t & 15;
-    const int64_t d0 = (int64_t)blockIdx.x * 128, c0 = (int64_t)blockIdx.y * 128;
-
-    float v[8][8];
-    load_block(a.w, a.ldw, d0, c0, 128, rg, cc, v);
 
     float m = 0.0f;
 #pragma unroll
@@ -988,6 +985,82 @@ __global__ void __launch_bounds__(kThreads, 2) k_quant_weight(WeightQuantArgs a)
             tileT_put(tileT, cc * 8 + j, rg, cols[j]);
         __syncthreads();
         store_tileT(tileT, a.qT, a.d, c0, d0);
+    }
+}
+
+// Weight quantizer, persistent: two CTAs of 256 threads per SM walk the
+// 128 x 128 blocks, warp 0 keeping the next block's BF16 input in flight by
+// TMA (a two-stage ring).
+struct WPipeSmem {
+    uint16_t stage[2][128 * 128];
+    uint8_t tileT[128 * 128];
+    float red[8];
+    unsigned long long full[2];
+    int issued[2];
+    int abort;
+};
+constexpr size_t kWPipeSmemBytes = sizeof(WPipeSmem) + 1024;
+
+__global__ void __launch_bounds__(kThreads, 2)
+    k_quant_weight_tma(const __grid_constant__ WeightQuantArgs a, const __grid_constant__ CUtensorMap tmw)
+{
+    extern __shared__ uint8_t smem_raw[];
+    WPipeSmem &sm = *reinterpret_cast<WPipeSmem *>(ptx::align_smem<1024>(smem_raw));
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int rg = t >> 4, cc = t & 15;
+    const int ncb = (int)(a.c / 128);
+    const int64_t total = (a.d / 128) * ncb;
+    unsigned *err = &g_quant_error;
+
+    auto issue = [&](int64_t k) { // warp 0, lane 0
+        const int64_t T = blockIdx.x + k * (int64_t)gridDim.x;
+        if (T >= total || sm.abort)
+            return;
+        const int s = (int)(k & 1);
+        const uint32_t bar = ptx::smem_addr(&sm.full[s]);
+        sm.issued[s] += 1;
+        ptx::mbar_arrive_expect_tx(bar, kPipeTileBytes);
+        ptx::tma_load_2d(ptx::smem_addr(sm.stage[s]), &tmw, bar, (int)((T % ncb) * 128), (int)((T / ncb) * 128));
+    };
+
+    if (t == 0) {
+        for (int s = 0; s < 2; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&sm.full[s]), 1);
+            sm.issued[s] = 0;
+        }
+        sm.abort = 0;
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    if (t == 0) {
+        ptx::prefetch_tensormap(&tmw);
+        issue(0);
+        issue(1);
+    }
+    for (int64_t k = 0;; ++k) {
+        const int64_t T = blockIdx.x + k * (int64_t)gridDim.x;
+        if (T >= total)
+            break;
+        const int s = (int)(k & 1);
+        ptx::mbar_wait(ptx::smem_addr(&sm.full[s]), (uint32_t)((k >> 1) & 1), &sm.abort, err, kQuantErrTimeout,
+                       kQuantWaitLimitNs);
+        float v[8][8];
+        const uint16_t *st = sm.stage[s];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            unpack8(*reinterpret_cast<const uint4 *>(st + (rg * 8 + i) * 128 + cc * 8), v[i]);
+        // every thread has its block (and finished the previous block's shared-memory work)
+        ptx::fence_proxy_async_smem();
+        __syncthreads();
+        if (t == 0)
+            issue(k + 2);
+        quant_weight_tile(a, sm.red, sm.tileT, v, (T / ncb) * 128, (T % ncb) * 128);
+    }
+    if (t == 0 && sm.abort) {
+        for (int s = 0; s < 2; ++s)
+            if (sm.issued[s] > 0)
+                ptx::mbar_wait(ptx::smem_addr(&sm.full[s]), (uint32_t)((sm.issued[s] - 1) & 1), &sm.abort, err,
+                               kQuantErrTimeout, kQuantWaitLimitNs, false);
     }
 }
 
@@ -1049,27 +1122,26 @@ __global__ void __launch_bounds__(kThreads, 2) k_quant_weight_pow2(WeightPow2Arg
 // MX-style quantizer with E8M0 scales: 1xG row blocks and Gx1 column blocks,
 // G = 32 (MXFP8) or 128 (the 128-block recipe with power-of-two scales; each
 // 32-element sub-block byte of the scale atoms then carries its group's exponent).
-template <bool ROW, bool COL, int G>
-__global__ void __launch_bounds__(kThreads, 2) k_quant_mx(MxQuantArgs a)
-{
-    __shared__ __align__(16) float red[8][128];
-    __shared__ __align__(16) uint8_t tileT[128 * 128];
-    __shared__ __align__(16) uint32_t e8T[128];
-    __shared__ Group grp;
+// Shared memory of one MX tile: column partial maxima, the transposed column
+// codes and the column scale bytes.
+struct MxTileSmem {
+    float red[8][128];
+    uint8_t tileT[128 * 128];
+    uint32_t e8T[128];
+};
 
+// One 128 x 128 tile (rows t0 .. t0 + cnt of a segment, columns c0 .. c0 + 127):
+// the thread holds its 8 x 8 block v (rows rg * 8 + i, columns cc * 8 + j).
+// Leaves with every thread past the tile's last shared-memory access.
+template <bool ROW, bool COL, int G>
+__device__ __forceinline__ void quant_mx_tile(const MxQuantArgs &a, MxTileSmem &ts, const float (&v)[8][8],
+                                              int64_t t0, int cnt, int64_t p0, int64_t c0)
+{
+    float (&red)[8][128] = ts.red;
+    uint8_t *tileT = ts.tileT;
+    uint32_t *e8T = ts.e8T;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int rg = t >> 4, cc = t & 15;
-    const int64_t c0 = (int64_t)blockIdx.y * 128;
-
-    map_group(blockIdx.x, a.rows, a.seg, a.nseg, &grp);
-    __syncthreads();
-    const int cnt = grp.cnt;
-    if (cnt == 0)
-        return;
-    const int64_t t0 = grp.t0, p0 = grp.p0;
-
-    float v[8][8];
-    load_block(a.x, a.ldx, t0, c0, cnt, rg, cc, v);
 
     if (ROW) {
         const int64_t ka = (a.rows + 127) / 128; // row bands of the row copy
@@ -1147,6 +1219,110 @@ __global__ void __launch_bounds__(kThreads, 2) k_quant_mx(MxQuantArgs a)
             const int64_t ka = (a.cols + 127) / 128; // row bands of the column copy (rows = channels)
             *reinterpret_cast<uint32_t *>(a.e8_col + mx_atom_offset(c0 + t, p0 >> 5, ka)) = e8T[t];
         }
+    }
+}
+
+// MX quantizer, persistent: two CTAs of 256 threads per SM walk the 128 x 128
+// tiles; warp 0 keeps the next tile's BF16 input in flight by TMA (a two-stage
+// ring, as in the FP8 activation quantizer), so HBM sees requests while a tile
+// is reduced, quantized and stored.
+constexpr int kMxStages = 2;
+struct MxPipeSmem {
+    uint16_t stage[kMxStages][128 * 128];
+    MxTileSmem ts;
+    Group grp[kMxStages];
+    unsigned long long full[kMxStages];
+    int issued[kMxStages];
+    int abort;
+};
+constexpr size_t kMxPipeSmemBytes = sizeof(MxPipeSmem) + 1024;
+
+template <bool ROW, bool COL, int G>
+__global__ void __launch_bounds__(kThreads, 2)
+    k_quant_mx_tma(const __grid_constant__ MxQuantArgs a, const __grid_constant__ CUtensorMap tmx, int64_t ngroups,
+                   int ncb)
+{
+    extern __shared__ uint8_t smem_raw[];
+    MxPipeSmem &sm = *reinterpret_cast<MxPipeSmem *>(ptx::align_smem<1024>(smem_raw));
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    const int rg = t >> 4, cc = t & 15;
+    const int64_t total = ngroups * ncb;
+    unsigned *err = &g_quant_error;
+
+    // warp 0: map the CTA's k-th tile to its rows and start its load into stage k % kMxStages
+    auto issue = [&](int64_t k) {
+        const int64_t T = blockIdx.x + k * (int64_t)gridDim.x;
+        if (T >= total || sm.abort)
+            return;
+        const int s = (int)(k % kMxStages);
+        map_group(T / ncb, a.rows, a.seg, a.nseg, &sm.grp[s]);
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t bar = ptx::smem_addr(&sm.full[s]);
+            sm.issued[s] += 1;
+            if (sm.grp[s].cnt > 0) {
+                ptx::mbar_arrive_expect_tx(bar, kPipeTileBytes);
+                ptx::tma_load_2d(ptx::smem_addr(sm.stage[s]), &tmx, bar, (int)((T % ncb) * 128), (int)sm.grp[s].t0);
+            } else {
+                ptx::mbar_arrive(bar);
+            }
+        }
+        __syncwarp();
+    };
+
+    if (t == 0) {
+        for (int s = 0; s < kMxStages; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&sm.full[s]), 1);
+            sm.issued[s] = 0;
+        }
+        sm.abort = 0;
+        ptx::fence_barrier_init();
+    }
+    __syncthreads();
+    if (warp == 0) {
+        if (lane == 0)
+            ptx::prefetch_tensormap(&tmx);
+        for (int s = 0; s < kMxStages; ++s)
+            issue(s);
+    }
+
+    for (int64_t k = 0;; ++k) {
+        const int64_t T = blockIdx.x + k * (int64_t)gridDim.x;
+        if (T >= total)
+            break;
+        const int s = (int)(k % kMxStages);
+        ptx::mbar_wait(ptx::smem_addr(&sm.full[s]), (uint32_t)((k / kMxStages) & 1), &sm.abort, err,
+                       kQuantErrTimeout, kQuantWaitLimitNs);
+        const int cnt = sm.grp[s].cnt;
+        const int64_t t0 = sm.grp[s].t0, p0 = sm.grp[s].p0;
+        const int64_t c0 = (T % ncb) * 128;
+        float v[8][8];
+        if (cnt > 0) {
+            const uint16_t *st = sm.stage[s];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = rg * 8 + i;
+                const uint4 raw = r < cnt ? *reinterpret_cast<const uint4 *>(st + r * 128 + cc * 8) : make_uint4(0, 0, 0, 0);
+                unpack8(raw, v[i]);
+            }
+        }
+        // every thread has its block (and finished the previous tile's shared-memory
+        // work): the stage can be refilled
+        ptx::fence_proxy_async_smem();
+        __syncthreads();
+        if (warp == 0)
+            issue(k + kMxStages);
+        if (cnt > 0)
+            quant_mx_tile<ROW, COL, G>(a, sm.ts, v, t0, cnt, p0, c0);
+    }
+
+    // after a timed-out wait no new loads were started; wait (bounded) for the
+    // ones still in flight before the CTA's shared memory is released
+    if (t == 0 && sm.abort) {
+        for (int s = 0; s < kMxStages; ++s)
+            if (sm.issued[s] > 0)
+                ptx::mbar_wait(ptx::smem_addr(&sm.full[s]), (uint32_t)((sm.issued[s] - 1) & 1), &sm.abort, err,
+                               kQuantErrTimeout, kQuantWaitLimitNs, false);
     }
 }
 
@@ -1528,6 +1704,28 @@ cudaError_t launch_quant_act_tma(const ActQuantArgs &a, const CUtensorMap &map, 
     return cudaGetLastError();
 }
 
+template <bool ROW, bool COL, int G>
+cudaError_t launch_quant_mx_tma(const MxQuantArgs &a, const CUtensorMap &map, int64_t ngroups, int ncb,
+                                cudaStream_t st)
+{
+    auto kern = k_quant_mx_tma<ROW, COL, G>;
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (configured_device != dev) {
+        if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMxPipeSmemBytes)) !=
+            cudaSuccess)
+            return e;
+        configured_device = dev;
+    }
+    const int64_t tiles = ngroups * ncb;
+    const int64_t cap = 2 * (int64_t)sm_count();
+    kern<<<(unsigned)(tiles < cap ? tiles : cap), kThreads, kMxPipeSmemBytes, st>>>(a, map, ngroups, ncb);
+    return cudaGetLastError();
+}
+
 template <int P>
 cudaError_t launch_quant_act_tma_p(const ActQuantArgs &a, cudaStream_t st)
 {
@@ -1641,8 +1839,25 @@ cudaError_t quant_read_and_clear_error(cudaStream_t st, unsigned *out)
 
 cudaError_t launch_quant_weight(const WeightQuantArgs &a, cudaStream_t st)
 {
-    dim3 grid((unsigned)(a.d / 128), (unsigned)(a.c / 128));
-    k_quant_weight<<<grid, kThreads, 0, st>>>(a);
+    if (a.d > 2147483647 || a.c > 2147483647)
+        return cudaErrorInvalidValue; // TMA coordinates are 32-bit
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (configured_device != dev) {
+        if ((e = cudaFuncSetAttribute(k_quant_weight_tma, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      (int)kWPipeSmemBytes)) != cudaSuccess)
+            return e;
+        configured_device = dev;
+    }
+    CUtensorMap map;
+    if ((e = make_bf16_tile_map(&map, a.w, a.c, a.d, a.ldw)) != cudaSuccess)
+        return e;
+    const int64_t tiles = (a.d / 128) * (a.c / 128);
+    const int64_t cap = 2 * (int64_t)sm_count();
+    k_quant_weight_tma<<<(unsigned)(tiles < cap ? tiles : cap), kThreads, kWPipeSmemBytes, st>>>(a, map);
     return cudaGetLastError();
 }
 
@@ -1652,23 +1867,26 @@ cudaError_t launch_quant_mx(const MxQuantArgs &a, int group, cudaStream_t st)
         return cudaSuccess;
     if (group != 32 && group != 128)
         return cudaErrorInvalidValue;
-    dim3 grid((unsigned)groups_upper_bound(a.rows, a.seg, a.nseg), (unsigned)(a.cols / 128));
+    if (a.rows > 2147483647 - 128 || a.cols > 2147483647)
+        return cudaErrorInvalidValue; // TMA coordinates are 32-bit
+    CUtensorMap map;
+    cudaError_t e = make_bf16_tile_map(&map, a.x, a.cols, a.rows, a.ldx);
+    if (e != cudaSuccess)
+        return e;
+    const int64_t ngroups = groups_upper_bound(a.rows, a.seg, a.nseg);
+    const int ncb = (int)(a.cols / 128);
     if (group == 32) {
         if (a.q_row && a.q_col)
-            k_quant_mx<true, true, 32><<<grid, kThreads, 0, st>>>(a);
-        else if (a.q_row)
-            k_quant_mx<true, false, 32><<<grid, kThreads, 0, st>>>(a);
-        else
-            k_quant_mx<false, true, 32><<<grid, kThreads, 0, st>>>(a);
-    } else {
-        if (a.q_row && a.q_col)
-            k_quant_mx<true, true, 128><<<grid, kThreads, 0, st>>>(a);
-        else if (a.q_row)
-            k_quant_mx<true, false, 128><<<grid, kThreads, 0, st>>>(a);
-        else
-            k_quant_mx<false, true, 128><<<grid, kThreads, 0, st>>>(a);
+            return launch_quant_mx_tma<true, true, 32>(a, map, ngroups, ncb, st);
+        if (a.q_row)
+            return launch_quant_mx_tma<true, false, 32>(a, map, ngroups, ncb, st);
+        return launch_quant_mx_tma<false, true, 32>(a, map, ngroups, ncb, st);
     }
-    return cudaGetLastError();
+    if (a.q_row && a.q_col)
+        return launch_quant_mx_tma<true, true, 128>(a, map, ngroups, ncb, st);
+    if (a.q_row)
+        return launch_quant_mx_tma<true, false, 128>(a, map, ngroups, ncb, st);
+    return launch_quant_mx_tma<false, true, 128>(a, map, ngroups, ncb, st);
 }
 
 cudaError_t launch_requant_col(const RequantArgs &a, cudaStream_t st)
