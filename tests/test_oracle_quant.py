@@ -153,6 +153,14 @@ def test_colgroups_segments_and_partial_groups():
     deq = oracle.dequant_colgroups(qc, sc, 300, offsets=off)
     xf = bf16_f32(x).astype(np.float64)
     assert np.all(np.abs(deq - xf) <= 2.0 ** -4 * np.abs(xf) + 1e-3 * np.abs(xf).max())
+    # exactly decode(code) * S of the token's own group: row i of segment e is position
+    # starts[e] + i of the copy, scaled by that 128-position group's scale of its column
+    dec = oracle.e4m3_decode(np.arange(256))
+    for e in range(4):
+        for i in range(off[e + 1] - off[e]):
+            pos = starts[e] + i
+            want = dec[qc[:, pos]] * sc[pos // 128].astype(np.float64)
+            assert np.array_equal(deq[off[e] + i], want), (e, i)
 
 
 def test_blocks_brute_and_transpose():
