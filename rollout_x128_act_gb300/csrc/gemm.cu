@@ -79,6 +79,7 @@ __host__ __device__ constexpr int lcm_int(int a, int b) { return a / gcd_int(a, 
 // flight while the current one is folded; 2 KB per-warp store staging.
 struct EpiNarrow {
     static constexpr bool kWide = false;
+    static constexpr int STG_BUFS = 1;
     static constexpr int LDX = 16, REG_WG0 = 0, REG_EPI = 0, DEPTH = 1;
     static constexpr int TMA_OUT = 0;
 };
@@ -89,11 +90,14 @@ struct EpiNarrow {
 // in a shared-memory ring filled ahead by warp 2 (per-thread asynchronous
 // copies), so no global load sits on the fold's path; tiles leave through
 // TMA stores of 32-row x 64-byte boxes from a per-warp staging area.
-template <int LDX_, int DEPTH_, int REG_WG0_, int REG_EPI_>
+template <int LDX_, int DEPTH_, int REG_WG0_, int REG_EPI_, int STG_BUFS_ = 1>
 struct EpiWide {
     static constexpr bool kWide = true;
     static constexpr int LDX = LDX_, DEPTH = DEPTH_, REG_WG0 = REG_WG0_, REG_EPI = REG_EPI_;
     static constexpr int TMA_OUT = 1;
+    // 2 KB staging buffers per epilogue warp: with two, a pass is written while
+    // the previous pass's TMA store still reads the other one
+    static constexpr int STG_BUFS = STG_BUFS_;
 };
 
 template <int BN, int EPI_WARPS, int STAGES, int TMEM_BUFS, int A_STRIDE_MAX = 16384, int KBP = 1,
@@ -123,7 +127,7 @@ struct Cfg {
     static constexpr size_t kSbBytes =
         (E::kWide || PER_ROW_B) ? ((size_t)kSbSlots * kSlotFloats * 4 + 1023) / 1024 * 1024 : 0;
     // output staging per epilogue warp: 32 rows x 64 bytes (the stores' unit)
-    static constexpr size_t kStgWarp = 2048;
+    static constexpr size_t kStgWarp = 2048 * (size_t)E::STG_BUFS;
     static constexpr size_t kStageOutBytes = (size_t)EPI_WARPS * kStgWarp;
     // layout: barriers (512 B) and group tables first, then 1024-aligned tiles,
     // the column-scale ring and the output staging.  With TMA stores the size
@@ -377,7 +381,7 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
 
         uint32_t tb = 0; // K-blocks folded so far (TMEM buffer tb % TMEM_BUFS, scale slot tb % SB)
         bool ok = true;
-        bool stored = false; // a TMA store of this warp may still be reading the staging area
+        uint32_t npass = 0; // store passes of this warp so far (staging buffer npass % STG_BUFS)
         for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
             const TileInfo ti = get_tile(sc, gt, t);
             const int64_t mw = (int64_t)ti.a_row0 + quarter * 32; // the warp's first row
@@ -453,30 +457,28 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
                              (mw + 32 <= ti.m_end || (ti.m_end == sc.M && sc.mode != kGroupedK));
             const int64_t out_row0 = (sc.mode == kGroupedK ? (int64_t)ti.e * sc.M : 0) + mw;
             auto pass = [&](int px, auto chunk, auto store) {
-                if (stored) {
-                    // the previous box must have been read before the area is rewritten
-                    if (lane == 0)
-                        ptx::bulk_wait_group_read0();
-                    __syncwarp();
-                    stored = false;
-                }
+                uint8_t *buf = stg + (size_t)(npass % E::STG_BUFS) * 2048;
+                ++npass;
+                // the store that last used this buffer must have finished reading it
+                if (lane == 0)
+                    ptx::bulk_wait_group_read<E::STG_BUFS - 1>();
+                __syncwarp();
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    *reinterpret_cast<uint4 *>(stg + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = chunk(c);
+                    *reinterpret_cast<uint4 *>(buf + lane * 64 + ((c ^ ((lane >> 1) & 3)) << 4)) = chunk(c);
                 if (tma) {
                     ptx::fence_proxy_async_smem();
                     __syncwarp();
                     if (lane == 0) {
-                        ptx::tma_store_2d(&tmO, ptx::smem_addr(stg), px, (int)out_row0);
+                        ptx::tma_store_2d(&tmO, ptx::smem_addr(buf), px, (int)out_row0);
                         ptx::bulk_commit_group();
                     }
-                    stored = true;
                 } else {
                     __syncwarp();
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         const int pc = lane + 32 * i, r = pc >> 2, c = pc & 3;
-                        const uint4 v = *reinterpret_cast<const uint4 *>(stg + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
+                        const uint4 v = *reinterpret_cast<const uint4 *>(buf + r * 64 + ((c ^ ((r >> 1) & 3)) << 4));
                         if (col_ok && mw + r < ti.m_end)
                             store(mw + r, c, v);
                     }
@@ -895,10 +897,12 @@ cudaError_t run_train(const GemmProblem &g, cudaStream_t st)
 }
 
 // WGrad (per-column B scales): 128 x 192 tiles folded by three epilogue
-// warpgroups (64 columns a thread, one 16-column TMEM load per wait).
+// warpgroups (64 columns a thread, one 16-column TMEM load per wait), two
+// staging buffers a warp (FP32 tiles are twice the bytes; a MoE expert's WGrad
+// tiles can be a few K-blocks long, so the store is a large share).
 cudaError_t run_wgrad(const GemmProblem &g, cudaStream_t st)
 {
-    return run<192, 12, 4, 2, true, 16384, 1, 1, EpiWide<16, 1, 0, 0>>(g, st);
+    return run<192, 12, 4, 2, true, 16384, 1, 1, EpiWide<16, 1, 0, 0, 2>>(g, st);
 }
 
 } // namespace

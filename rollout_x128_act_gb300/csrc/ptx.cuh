@@ -195,11 +195,12 @@ __device__ __forceinline__ void bulk_commit_group()
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
-// Waits until every bulk group this thread committed has finished reading its
-// shared-memory source (the buffer may be overwritten).
-__device__ __forceinline__ void bulk_wait_group_read0()
+// Waits until at most N of the bulk groups this thread committed are still
+// reading their shared-memory sources (the others' buffers may be overwritten).
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read()
 {
-    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
 }
 
 // Waits until every bulk group this thread committed has completed.
