@@ -961,6 +961,14 @@ PROFILE_CASES = {
     "quant_swiglu": "fused SwiGLU quantizer, gate and up 8192 x 12288 BF16 (row + column copies)",
     "quant_nvfp4": "NVFP4 quantizer, per-token scope, 131072 routed rows x 2048 BF16",
     "gemm_nvfp4": "NVFP4 FProp 4096 x 12288 x 4096 (per-token x tensor scope, BF16 out)",
+    "decode_narrow": "FProp 128 tokens x W_down 4096 x 12288 (narrow 32-row weight tiles, BF16 out)",
+    "gemm_mx_dgrad": "MXFP8 DGrad 4096 x 4096 x 12288 (BF16 out)",
+    "gemm_mx_wgrad": "MXFP8 WGrad 12288 x 4096 x K=4096 (FP32 out)",
+    "grouped_wgrad": "grouped WGrad, 32 experts x 1536 x 2048, 16384 routed rows (Zipf 1.2), FP32 out",
+    "quant_act_pow2": "power-of-two 1x128 row + 128x1 column copies, X 8192 x 12288 BF16",
+    "quant_w_pow2": "power-of-two 128x128 weight blocks + transposed copy, W 12288 x 12288 BF16",
+    "amax_bf16": "max |x| over 131072 x 2048 BF16 (NVFP4 tensor scope)",
+    "dequant_nvfp4": "BF16 dequantization of the NVFP4 copy of 131072 x 2048 (per-token scope)",
 }
 
 
@@ -1036,6 +1044,49 @@ def run_case(name: str, launches: int = 5):
     elif name == "quant_nvfp4":
         x = bf16(synth.activation(131072, 2048, seed=0, stream="x"))
         fn = lambda: jq.quant_nvfp4(x)  # noqa: E731
+    elif name == "decode_narrow":
+        n, c, d = 128, 12288, 4096
+        ax = jq.quant_act(bf16(synth.activation(n, c, seed=0, stream="h")), col=False)
+        qw, sw, _, _ = jq.quant_weight(bf16(synth.weight(d, c, seed=0, stream="w_down")), transposed=False)
+        out = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
+        fn = lambda: jq.jetq_gemm_fprop(jq.RECIPE_BLOCK128, ax["q_row"], ax["s_row"], qw, sw, n, d, c, out,  # noqa
+                                        jq.PATH_DECODE)
+    elif name in ("gemm_mx_dgrad", "gemm_mx_wgrad"):
+        n, c, d = 4096, 4096, 12288
+        gdy = jq.quant_mx(bf16(synth.gradient(n, d, seed=0, stream="dy_up")))
+        if name == "gemm_mx_dgrad":
+            gw = jq.quant_mx(bf16(synth.weight(d, c, seed=0, stream="w_up")))
+            out = torch.empty((n, c), dtype=torch.bfloat16, device=dev)
+            fn = lambda: jq.jetq_gemm_dgrad(jq.RECIPE_MXFP8, gdy["q_row"], gdy["e8_row"], gw["q_col"],  # noqa
+                                            gw["e8_col"], n, d, c, out)
+        else:
+            gx = jq.quant_mx(bf16(synth.activation(n, c, seed=0, stream="x")))
+            out = torch.empty((d, c), dtype=torch.float32, device=dev)
+            fn = lambda: jq.jetq_gemm_wgrad(jq.RECIPE_MXFP8, gdy["q_col"], gdy["e8_col"], gx["q_col"],  # noqa
+                                            gx["e8_col"], n, gx["ldq_col"], d, c, out)
+    elif name == "grouped_wgrad":
+        E, c, d = 32, 2048, 1536
+        off, _ = synth.zipf_topk_routing(2048, E, 8, 1.2, seed=0)
+        R = int(off[-1])
+        seg = torch.tensor(off, dtype=torch.int64, device=dev)
+        ax = jq.quant_act(bf16(synth.activation(R, c, seed=0, stream="x")), row=False, seg_offsets=seg)
+        ady = jq.quant_act(bf16(synth.gradient(R, d, seed=0, stream="dy_gate")), row=False, seg_offsets=seg)
+        P = int(sum((int(off[e + 1] - off[e]) + 127) // 128 * 128 for e in range(E)))
+        out = torch.empty((E, d, c), dtype=torch.float32, device=dev)
+        fn = lambda: jq.grouped(jq.GEMM_WGRAD, ady["q_col"], ady["s_col"], ax["q_col"], ax["s_col"], seg, n=c,  # noqa
+                                k=P, out=out)
+    elif name == "quant_act_pow2":
+        x = bf16(synth.activation(8192, 12288, seed=0, stream="h"))
+        fn = lambda: jq.quant_act_pow2(x)  # noqa: E731
+    elif name == "quant_w_pow2":
+        w = bf16(synth.weight(12288, 12288, seed=0, stream="w"))
+        fn = lambda: jq.quant_weight_pow2(w)  # noqa: E731
+    elif name == "amax_bf16":
+        x = bf16(synth.activation(131072, 2048, seed=0, stream="x"))
+        fn = lambda: jq.amax_bf16(x)  # noqa: E731
+    elif name == "dequant_nvfp4":
+        o = jq.quant_nvfp4(bf16(synth.activation(131072, 2048, seed=0, stream="x")))
+        fn = lambda: jq.dequant_nvfp4_bf16(o["q"], o["sb"], o["sg"])  # noqa: E731
     elif name == "gemm_nvfp4":
         n, c, d = 4096, 4096, 12288
         ga = jq.quant_nvfp4(bf16(synth.activation(n, c, seed=0, stream="x")))

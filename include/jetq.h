@@ -96,6 +96,8 @@ JETQ_API int jetq_version(void);
  * Synchronize `stream`, then read and clear the device error word of every
  * kernel family.  Returns JETQ_ERR_TIMEOUT if any kernel gave up a bounded
  * wait since the last call, JETQ_ERR_CUDA if the synchronization failed.
+ * The read and the clear are separate copies: call it when no jetq kernel is
+ * running on another stream, or a word set in between would be lost.
  */
 JETQ_API jetq_status jetq_check_device_error(void *stream);
 
@@ -327,8 +329,8 @@ JETQ_API jetq_status jetq_quant_w_128x128_pow2(const uint16_t *w, int64_t d, int
 /*
  * Column copy re-quantized from the FP8 row copy (JetRL's
  * requantize_for_dgrad: the 1x128 copy goes back through dequantization and
- * is quantized again along the token dimension; the Miles post calls this the
- * DeepSeek-V3 style, as opposed to taking both copies from BF16).  Each value
+ * is quantized again along the token dimension; the Miles post traces this
+ * to DeepSeek-V3 and contrasts it with taking both copies from BF16).  Each value
  * is rebuilt in binary32, v = fl32(decode(q_row[r,k]) * s_row[k/128, r]),
  * then quantized as the column copy of jetq_quant_act_1x128 quantizes BF16:
  * S = fl32(amax/448) per 128x1 group inside each segment, q = E4M3(fl32(v/S)).
@@ -478,9 +480,8 @@ JETQ_API jetq_status jetq_nvfp4_scale_atoms(const uint8_t *sb, int64_t rows, int
 
 /*
  * NVFP4 FProp with the scope scales in the epilogue (Miles "Blackwell-native
- * RL recipes" post, NVFP4 section: per-token FP32 scaling of the activations,
- * which the post's training path applied as a separate operation instead of
- * in a native per-token NVFP4 GEMM):
+ * RL recipes" post, NVFP4 section: activations carry a per-token FP32 scale,
+ * which that post's path applied in a step of its own, outside the GEMM):
  *   acc[i, j] = sum_k (e2m1(qa[i, k]) * e4m3(sba[i, k/16])) * (e2m1(qb[j, k]) * e4m3(sbb[j, k/16]))
  *               (tensor core: block-scaled FP4 MMA, FP32 accumulation over all of K)
  *   out[i, j] = fl32(fl32(sga[per_row_a ? i : 0] * sgb[0]) * acc[i, j]), F32 or BF16 (RNE of that)

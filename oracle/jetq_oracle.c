@@ -17,9 +17,9 @@
  *         DGrad) and section 4.2 (1x128 activations, 128x128 weights, the
  *         WGrad operands grouped along the token axis).
  *   [MB]  the Miles "Blackwell-native RL recipes" post, MXFP8 section
- *         (32 consecutive E4M3 values share one E8M0 scale, rounded up so the
- *         block maximum is not clipped; row-wise and column-wise copies are
- *         each quantized from full precision).
+ *         (one E8M0 scale per 32 consecutive E4M3 values, a power of two
+ *         rounded upward so that the largest value of a block still fits;
+ *         the row-wise and column-wise copies each come from full precision).
  *
  * Readings where the pages are silent or garbled (each is listed in the
  * design notes):
@@ -408,7 +408,7 @@ void jo_rmsnorm_bf16(const uint16_t *x, const uint16_t *w, int64_t rows, int64_t
  *   w  : bf16 [rows x cols], row stride ldw
  *   q  : codes [rows x cols] (dense), s : [rows/bs x cols/bs] row-major
  *   qT : optional transposed codes [cols x rows], sT : [cols/bs x rows/bs]
- *        ([JR]: for DGrad "only a transpose" of the quantized weight).
+ *        ([JR]: DGrad takes the quantized weight merely transposed).
  */
 void jo_quant_blocks(const uint16_t *w, int64_t rows, int64_t cols, int64_t ldw, int64_t bs,
                      uint8_t *q, float *s, uint8_t *qT, float *sT)
@@ -441,7 +441,7 @@ void jo_quant_blocks(const uint16_t *w, int64_t rows, int64_t cols, int64_t ldw,
 
 /* ------------------------------------------------------------------------ */
 /* MXFP8 ([MB], MXFP8 section): blocks of 32 consecutive values share one   */
-/* E8M0 scale 2^e, "rounded up" so the block maximum is not clipped:        */
+/* E8M0 scale 2^e, rounded upward so the block maximum stays in range:     */
 /* e is the smallest integer with amax <= 448 * 2^e, clamped to [-127,127]; */
 /* the scale byte is e + 127 and q = E4M3(x * 2^-e) (the product is exact   */
 /* in binary64, so there is exactly one rounding).  All-zero block: byte    */

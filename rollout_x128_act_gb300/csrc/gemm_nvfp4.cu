@@ -6,9 +6,9 @@
 // The Miles post on Blackwell-native RL recipes (NVFP4 section) quantizes MoE
 // expert operands to E2M1 with one E4M3 scale per 16 values and one FP32
 // scale for a larger scope (per token for activations, per tensor for
-// weights), and names the missing piece of its training path: a native
-// per-token NVFP4 GEMM with the per-token scaling fused into the epilogue.
-// This is that GEMM: the block scales ride the tensor core's block-scaled MMA
+// weights), and traces part of its training gap to applying the per-token
+// scale as a separate step outside the GEMM.  Here it is inside: the block
+// scales ride the tensor core's block-scaled MMA
 // (scale_vec::4X: four E4M3 scales per 64-element K step), the whole K loop
 // accumulates in TMEM, and the epilogue applies the two FP32 scope scales once.
 //
