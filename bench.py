@@ -323,12 +323,15 @@ def measure_decode(dev, peaks):
         for n in (1, 8, 64, 256):
             a = jq.quant_act(x[:n], col=False)
             y = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
+            # the split-K decode's partial sums (allocated once, as a rollout engine would)
+            work = torch.empty(max(jq.jetq_decode_workspace_bytes(n, d, c), 16), dtype=torch.uint8, device=dev)
             i = [0]
 
             def call():
                 q, s, _, _ = ws[i[0] % 8]
                 i[0] += 1
-                jq.jetq_gemm_fprop(jq.RECIPE_BLOCK128, a["q_row"], a["s_row"], q, s, n, d, c, y, jq.PATH_DECODE)
+                jq.jetq_gemm_fprop_ws(jq.RECIPE_BLOCK128, a["q_row"], a["s_row"], q, s, n, d, c, y, work,
+                                      jq.PATH_DECODE)
 
             ms = _time(call, 40)
             # CUDA-graph replay of 8 calls (one per weight copy), as a decode step replays

@@ -395,6 +395,34 @@ JETQ_API jetq_status jetq_gemm_fprop(jetq_recipe recipe,
                             jetq_path path, void *stream);
 
 /*
+ * FProp with a caller-owned workspace, for rollout-sized batches.  The SkyRL
+ * post ("On-Policy FP8 weight sync") has the rollout engine run the trainer's
+ * FP8 weights, and the Jet-RL explainer's rollout keeps 128 sequences in
+ * flight: each decode step multiplies a few tokens by whole weights.  When the
+ * decode path applies (BLOCK128, 1 <= n <= 64, a weight of at least 32 and at
+ * most 152 128-row bands), a cluster of SMs shares each band's K range and
+ * the partial sums pass through `workspace`; the fold order is unchanged, so
+ * the result equals jetq_gemm_fprop's bit for bit.  Otherwise (another recipe
+ * or path, other sizes, a null or too small workspace) it runs exactly what
+ * jetq_gemm_fprop runs.
+ *
+ * workspace: device memory, 16-byte aligned, at least
+ * jetq_decode_workspace_bytes(n, d, c) bytes (0 when the shape does not use
+ * one; currently d * c/128 * n * 4 bytes).  No initial contents are needed;
+ * the call overwrites it.  Calls that share a workspace must not overlap on
+ * the GPU.  Errors as jetq_gemm_fprop, plus JETQ_ERR_MISALIGNED for the
+ * workspace.
+ */
+JETQ_API size_t jetq_decode_workspace_bytes(int64_t n, int64_t d, int64_t c);
+JETQ_API jetq_status jetq_gemm_fprop_ws(jetq_recipe recipe,
+                            const uint8_t *qx, const void *sx,
+                            const uint8_t *qw, const void *sw,
+                            int64_t n, int64_t d, int64_t c,
+                            void *y, jetq_out_dtype y_dtype, int64_t ldy,
+                            void *workspace, size_t workspace_bytes,
+                            jetq_path path, void *stream);
+
+/*
  * DGrad.  BLOCK128: qdy = row copy of dY [n x d], sdy [d/128 x n]; qwt = the
  * transposed weight copy [c x d], swt [c/128 x d/128].  MXFP8: qdy row MX
  * copy of dY (n, d); qwt = column MX copy of W ([c x d], blocks of 32 along d).

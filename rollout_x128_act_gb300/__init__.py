@@ -68,6 +68,8 @@ def lib() -> ctypes.CDLL:
             "jetq_requant_col_from_row": (I32, [P, P, I64, I64, P, P, I64, P, I32, P]),
             "jetq_dequant_bf16": (I32, [P, P, I64, I64, I32, P, I64, P]),
             "jetq_gemm_fprop": (I32, [I32, P, P, P, P, I64, I64, I64, P, I32, I64, I32, P]),
+            "jetq_decode_workspace_bytes": (ctypes.c_size_t, [I64, I64, I64]),
+            "jetq_gemm_fprop_ws": (I32, [I32, P, P, P, P, I64, I64, I64, P, I32, I64, P, ctypes.c_size_t, I32, P]),
             "jetq_gemm_dgrad": (I32, [I32, P, P, P, P, I64, I64, I64, P, I32, I64, P]),
             "jetq_gemm_wgrad": (I32, [I32, P, P, P, P, I64, I64, I64, I64, P, I64, I32, P]),
             "jetq_gemm_grouped": (I32, [I32, I32, P, P, P, P, I64, I64, I64, I64, P, I32, P, I32, I64, I32, P]),
@@ -244,6 +246,17 @@ def jetq_gemm_fprop(recipe, qx, sx, qw, sw, n, d, c, y, path=PATH_AUTO, stream=N
                                  y.stride(0), path, _s(stream)), "jetq_gemm_fprop")
 
 
+def jetq_decode_workspace_bytes(n, d, c):
+    return int(lib().jetq_decode_workspace_bytes(n, d, c))
+
+
+def jetq_gemm_fprop_ws(recipe, qx, sx, qw, sw, n, d, c, y, ws, path=PATH_AUTO, stream=None):
+    _check(lib().jetq_gemm_fprop_ws(recipe, _p(qx), _p(sx), _p(qw), _p(sw), n, d, c, _p(y), _out_dtype(y),
+                                    y.stride(0), None if ws is None else _p(ws),
+                                    0 if ws is None else ws.numel() * ws.element_size(), path, _s(stream)),
+           "jetq_gemm_fprop_ws")
+
+
 def jetq_gemm_dgrad(recipe, qdy, sdy, qwt, swt, n, d, c, dx, stream=None):
     _check(lib().jetq_gemm_dgrad(recipe, _p(qdy), _p(sdy), _p(qwt), _p(swt), n, d, c, _p(dx), _out_dtype(dx),
                                  dx.stride(0), _s(stream)), "jetq_gemm_dgrad")
@@ -416,11 +429,20 @@ def quant_weight_pow2(w, transposed=True, stream=None):
     return q, e8, qT, e8T
 
 
-def fprop(qx, sx, qw, sw, out_dtype=torch.float32, path=PATH_AUTO, recipe=RECIPE_BLOCK128, stream=None):
+def fprop(qx, sx, qw, sw, out_dtype=torch.float32, path=PATH_AUTO, recipe=RECIPE_BLOCK128, stream=None,
+          workspace=None):
+    """Y = X W^T.  Rollout-sized calls that can spread a weight band over several
+    SMs get a workspace (the caller's, if large enough, else a fresh one)."""
     n, c = qx.shape
     d = qw.shape[0]
     y = torch.empty((n, d), dtype=out_dtype, device=qx.device)
-    jetq_gemm_fprop(recipe, qx, sx, qw, sw, n, d, c, y, path, stream)
+    wsb = jetq_decode_workspace_bytes(n, d, c) if recipe == RECIPE_BLOCK128 and path != PATH_TRAIN else 0
+    if wsb:
+        if workspace is None or workspace.numel() * workspace.element_size() < wsb:
+            workspace = torch.empty(wsb, dtype=torch.uint8, device=qx.device)
+        jetq_gemm_fprop_ws(recipe, qx, sx, qw, sw, n, d, c, y, workspace, path, stream)
+    else:
+        jetq_gemm_fprop(recipe, qx, sx, qw, sw, n, d, c, y, path, stream)
     return y
 
 

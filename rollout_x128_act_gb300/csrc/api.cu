@@ -446,9 +446,9 @@ jetq_status jetq_dequant_bf16(const uint8_t *q, const float *s, int64_t rows, in
     return from_cuda(launch_dequant_bf16(args, static_cast<cudaStream_t>(stream)));
 }
 
-jetq_status jetq_gemm_fprop(jetq_recipe recipe, const uint8_t *qx, const void *sx, const uint8_t *qw, const void *sw,
-                            int64_t n, int64_t d, int64_t c, void *y, jetq_out_dtype y_dtype, int64_t ldy,
-                            jetq_path path, void *stream)
+static jetq_status fprop_impl(jetq_recipe recipe, const uint8_t *qx, const void *sx, const uint8_t *qw,
+                              const void *sw, int64_t n, int64_t d, int64_t c, void *y, jetq_out_dtype y_dtype,
+                              int64_t ldy, void *workspace, size_t workspace_bytes, jetq_path path, void *stream)
 {
     JQ_REQUIRE(recipe == JETQ_RECIPE_BLOCK128 || recipe == JETQ_RECIPE_MXFP8 ||
                    recipe == JETQ_RECIPE_BLOCK128_POW2,
@@ -473,8 +473,34 @@ jetq_status jetq_gemm_fprop(jetq_recipe recipe, const uint8_t *qx, const void *s
     GemmProblem g{qx, static_cast<const float *>(sx), qw, static_cast<const float *>(sw), n, d, c, c, c,
                   BScale::Block128, y, ldy, y_dtype, 0};
     const bool decode = path == JETQ_PATH_DECODE || (path == JETQ_PATH_AUTO && n <= 256);
+    if (decode && workspace) {
+        g.ws = workspace;
+        g.ws_bytes = workspace_bytes;
+    }
     return from_cuda(launch_gemm_block128(g, decode ? GemmShape::Decode : GemmShape::Train,
                                           static_cast<cudaStream_t>(stream)));
+}
+
+jetq_status jetq_gemm_fprop(jetq_recipe recipe, const uint8_t *qx, const void *sx, const uint8_t *qw, const void *sw,
+                            int64_t n, int64_t d, int64_t c, void *y, jetq_out_dtype y_dtype, int64_t ldy,
+                            jetq_path path, void *stream)
+{
+    return fprop_impl(recipe, qx, sx, qw, sw, n, d, c, y, y_dtype, ldy, nullptr, 0, path, stream);
+}
+
+size_t jetq_decode_workspace_bytes(int64_t n, int64_t d, int64_t c)
+{
+    if (n < 1 || d <= 0 || c <= 0 || d % 128 != 0 || c % 128 != 0 || check_arch() != JETQ_OK)
+        return 0;
+    return decode_split_workspace_bytes(n, d, c);
+}
+
+jetq_status jetq_gemm_fprop_ws(jetq_recipe recipe, const uint8_t *qx, const void *sx, const uint8_t *qw,
+                               const void *sw, int64_t n, int64_t d, int64_t c, void *y, jetq_out_dtype y_dtype,
+                               int64_t ldy, void *workspace, size_t workspace_bytes, jetq_path path, void *stream)
+{
+    JQ_REQUIRE(workspace == nullptr || aligned16(workspace), JETQ_ERR_MISALIGNED);
+    return fprop_impl(recipe, qx, sx, qw, sw, n, d, c, y, y_dtype, ldy, workspace, workspace_bytes, path, stream);
 }
 
 jetq_status jetq_gemm_dgrad(jetq_recipe recipe, const uint8_t *qdy, const void *sdy, const uint8_t *qwt,

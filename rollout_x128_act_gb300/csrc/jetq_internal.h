@@ -127,6 +127,8 @@ struct GemmProblem {
     GroupKind group = GroupKind::None;
     const int64_t *seg = nullptr; // device [num_experts + 1]
     int num_experts = 1;
+    void *ws = nullptr;           // device workspace of the split-K decode (optional)
+    size_t ws_bytes = 0;
 };
 
 enum class GemmShape : int { Train = 0, Decode = 1 };
@@ -164,6 +166,10 @@ cudaError_t launch_selftest_wait(unsigned long long limit_ns, long long *elapsed
 // weight tiles, K a multiple of 128.  Bitwise equal to launch_gemm_block128.
 constexpr int64_t kDecodeSwappedMinTiles = 32;
 bool gemm_decode_swapped_applies(const GemmProblem &g);
+// Split-K decode (a cluster of CTAs per 128-row band; partial sums through a
+// workspace): cluster size for a shape (1 = not used) and workspace bytes.
+int decode_split_factor(int64_t M, int64_t N, int64_t K);
+size_t decode_split_workspace_bytes(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_gemm_decode_swapped(const GemmProblem &g, cudaStream_t st);
 cudaError_t gemm_decode_read_and_clear_error(cudaStream_t st, unsigned *out);
 

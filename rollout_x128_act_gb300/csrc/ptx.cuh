@@ -74,19 +74,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
     return ok != 0;
 }
 
+// The same with acquire at cluster scope: for phases completed by arrivals of
+// other CTAs of the cluster (their writes to this CTA's shared memory before
+// the arrive are visible after the wait).
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Waits for the phase with the given parity.  Gives up after limit_ns of
 // wall time, or (when honor_abort) as soon as another thread of the CTA has
 // given up (abort flag in shared memory); on timing out it raises the abort
 // flag, records `code` in the device error word and returns false.
+template <bool kClusterAcquire = false>
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort_flag,
                                           unsigned *err_word, unsigned code, uint64_t limit_ns,
                                           bool honor_abort = true)
 {
-    if (mbar_try_wait(bar, parity))
+    auto poll = [&]() { return kClusterAcquire ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+    if (poll())
         return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity))
+        if (poll())
             return true;
         if ((i & 31u) == 0u) {
             if (honor_abort && *abort_flag)
@@ -148,6 +166,41 @@ __device__ __forceinline__ uint32_t map_to_cta(uint32_t saddr, uint32_t rank)
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t cluster_addr)
 {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Bulk copy from this CTA's shared memory into the shared memory of a CTA of
+// the cluster; completion (bytes) is signalled on an mbarrier of the
+// destination CTA.  dst and bar come from map_to_cta; addresses 16-byte
+// aligned, size a multiple of 16.
+__device__ __forceinline__ void bulk_copy_to_cta(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                 uint32_t bar_cluster)
+{
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst_cluster),
+                 "r"(src), "r"(bytes), "r"(bar_cluster)
+                 : "memory");
+}
+
+// 16-byte store to this CTA's shared memory (shared-window address).
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster with the default
+// (CTA-scope release) semantics: the consumer release of a pipeline slot that
+// the peer next overwrites with a bulk copy; the releasing threads have
+// consumed the slot's values before they arrive.
+__device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t cluster_addr)
+{
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
+}
+
+// Named barrier `id` (1..15) over `count` threads (whole warps) of the CTA;
+// the threads of a warp may arrive apart (non-aligned form).
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
+{
+    asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
 // Hardware cluster barrier (every thread of every CTA of the cluster).

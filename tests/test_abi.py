@@ -55,7 +55,8 @@ def _ctype_of(param):
     base = param.rsplit(" ", 1)[0].replace("const ", "").strip()
     if base in re.findall(r"}\s*(jetq_\w+)\s*;", open(HEADER).read()):  # the header's enums
         return ctypes.c_int
-    return {"int64_t": ctypes.c_int64, "int": ctypes.c_int, "float": ctypes.c_float, "uint64_t": ctypes.c_uint64}[base]
+    return {"int64_t": ctypes.c_int64, "int": ctypes.c_int, "float": ctypes.c_float, "uint64_t": ctypes.c_uint64,
+            "size_t": ctypes.c_size_t}[base]
 
 
 def test_binding_matches_every_declaration(L):

@@ -79,3 +79,57 @@ def test_decode_repeated_launches_identical(fprop_case):
     for y in ys[1:]:
         assert torch.equal(y.view(torch.int32), ys[0].view(torch.int32))
     assert np.isfinite(ys[0].cpu().numpy()).all()
+
+
+# With a workspace, batches of up to 32 tokens against weights of 32-76 row
+# blocks take the split-K kernel: a cluster of 4 CTAs per row block (at most 38
+# blocks, at least 16 K-blocks) or of 2 (at least 8 K-blocks); the partial
+# sums pass through the workspace and the cluster's CTAs fold them in
+# ascending K.  K-block counts leave a partial last chunk and cluster members
+# with fewer chunks than others; the token counts cover both token-column
+# widths (16, 32) and the fold's 1, 2, 4 and 8 elements a thread; 33 and 64
+# tokens and a 96-block weight check that the others keep the one-CTA kernel.
+SPLIT_CASES = [
+    (4096, 2048, 1), (4096, 2176, 16), (4096, 2432, 8), (4096, 2176, 17), (4864, 2688, 32),
+    (4096, 3200, 33), (4864, 2176, 64), (4096, 12288, 5),
+    (8192, 1024, 1), (8192, 2048, 8), (9728, 1152, 13), (6144, 1408, 24), (12288, 4096, 8),
+]
+
+
+@pytest.mark.parametrize("D,C,n", SPLIT_CASES)
+def test_decode_split_k_against_oracle_and_training(D, C, n):
+    x = synth.activation(n, C, seed=D + C + n, stream="x")
+    w = synth.weight(D, C, seed=D + C, stream="w")
+    qw, sw, _, _ = jq.quant_weight(to_dev_bf16(w), transposed=False)
+    a = jq.quant_act(to_dev_bf16(x), col=False)
+    # batches of up to 32 tokens against at most 76 row blocks split K; the
+    # others keep one CTA per row band
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    split = n <= 32 and D // 128 <= sms // 2
+    assert jq.jetq_decode_workspace_bytes(n, D, C) == (D * (C // 128) * n * 4 if split else 0)
+    y_dec = jq.fprop(a["q_row"], a["s_row"], qw, sw, path=jq.PATH_DECODE)  # with a workspace
+    y_dec16 = jq.fprop(a["q_row"], a["s_row"], qw, sw, out_dtype=torch.bfloat16, path=jq.PATH_DECODE)
+    y_one = torch.empty_like(y_dec)  # no workspace: one CTA per row band
+    jq.jetq_gemm_fprop(jq.RECIPE_BLOCK128, a["q_row"], a["s_row"], qw, sw, n, D, C, y_one, jq.PATH_DECODE)
+    y_train = jq.fprop(a["q_row"], a["s_row"], qw, sw, path=jq.PATH_TRAIN)
+    torch.cuda.synchronize()
+    assert jq.jetq_check_device_error() == jq.OK
+    assert torch.equal(y_dec.view(torch.int32), y_train.view(torch.int32))
+    assert torch.equal(y_one.view(torch.int32), y_train.view(torch.int32))
+    assert torch.equal(y_dec16, y_dec.to(torch.bfloat16))
+    X = oracle.dequant_rowgroups(*oracle.quant_rowgroups(x))
+    W = oracle.dequant_blocks(*oracle.quant_blocks(w)[:2])
+    assert_gemm_close(y_dec, *oracle.fprop(X, W))
+
+
+def test_decode_split_k_repeated_launches_identical():
+    D, C, n = 4096, 2304, 40
+    x = synth.activation(n, C, seed=11, stream="x")
+    w = synth.weight(D, C, seed=11, stream="w")
+    qw, sw, _, _ = jq.quant_weight(to_dev_bf16(w), transposed=False)
+    a = jq.quant_act(to_dev_bf16(x), col=False)
+    ys = [jq.fprop(a["q_row"], a["s_row"], qw, sw, path=jq.PATH_DECODE) for _ in range(4)]
+    torch.cuda.synchronize()
+    assert jq.jetq_check_device_error() == jq.OK
+    for y in ys[1:]:
+        assert torch.equal(y.view(torch.int32), ys[0].view(torch.int32))
