@@ -423,6 +423,37 @@ JETQ_API jetq_status jetq_gemm_fprop_ws(jetq_recipe recipe,
                             jetq_path path, void *stream);
 
 /*
+ * Rollout FProp that allocates nothing (BLOCK128, the decode path).  No
+ * counterpart in the pages: this is a library convenience.  Some callers
+ * cannot hand out device memory for a workspace: a framework whose caching
+ * allocator must own every device allocation, a serving loop that cannot
+ * afford the device-wide synchronization of cudaMalloc/cudaFree, or a host
+ * that gives a plugin only a stream and its input/output buffers.  This call
+ * computes exactly what jetq_gemm_fprop(JETQ_RECIPE_BLOCK128, ...,
+ * JETQ_PATH_DECODE, ...) and jetq_gemm_fprop_ws compute, bit for bit, with
+ * the split-K decode's partial sums kept in a scratch array built into the
+ * library (JETQ_NOALLOC_SCRATCH_BYTES of device memory, held by every GPU
+ * that loads the library until the process exits).  It calls no allocator.
+ *
+ * Arguments as jetq_gemm_fprop (qx [n x c], sx [c/128 x n], qw [d x c],
+ * sw [d/128 x c/128], y [n x ldy]).  Returns JETQ_ERR_UNSUPPORTED_SHAPE when
+ * the split-K partials of this shape, jetq_decode_workspace_bytes(n, d, c),
+ * exceed JETQ_NOALLOC_SCRATCH_BYTES (e.g. more than 10 tokens against a
+ * 4096 x 12288 weight); shapes that need no partials run without the array.
+ * The first call on a device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream
+ * capture.  Every call shares the one array: calls that overlap on the GPU
+ * (other streams, or several host threads) race on it.  Nothing in it needs
+ * an initial value: each call writes every partial before reading it.
+ */
+#define JETQ_NOALLOC_SCRATCH_BYTES (16u << 20)
+JETQ_API jetq_status jetq_gemm_fprop_noalloc(const uint8_t *qx, const float *sx,
+                            const uint8_t *qw, const float *sw,
+                            int64_t n, int64_t d, int64_t c,
+                            void *y, jetq_out_dtype y_dtype, int64_t ldy,
+                            void *stream);
+
+/*
  * DGrad.  BLOCK128: qdy = row copy of dY [n x d], sdy [d/128 x n]; qwt = the
  * transposed weight copy [c x d], swt [c/128 x d/128].  MXFP8: qdy row MX
  * copy of dY (n, d); qwt = column MX copy of W ([c x d], blocks of 32 along d).

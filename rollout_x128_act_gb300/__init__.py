@@ -70,6 +70,7 @@ def lib() -> ctypes.CDLL:
             "jetq_gemm_fprop": (I32, [I32, P, P, P, P, I64, I64, I64, P, I32, I64, I32, P]),
             "jetq_decode_workspace_bytes": (ctypes.c_size_t, [I64, I64, I64]),
             "jetq_gemm_fprop_ws": (I32, [I32, P, P, P, P, I64, I64, I64, P, I32, I64, P, ctypes.c_size_t, I32, P]),
+            "jetq_gemm_fprop_noalloc": (I32, [P, P, P, P, I64, I64, I64, P, I32, I64, P]),
             "jetq_gemm_dgrad": (I32, [I32, P, P, P, P, I64, I64, I64, P, I32, I64, P]),
             "jetq_gemm_wgrad": (I32, [I32, P, P, P, P, I64, I64, I64, I64, P, I64, I32, P]),
             "jetq_gemm_grouped": (I32, [I32, I32, P, P, P, P, I64, I64, I64, I64, P, I32, P, I32, I64, I32, P]),
@@ -255,6 +256,16 @@ def jetq_gemm_fprop_ws(recipe, qx, sx, qw, sw, n, d, c, y, ws, path=PATH_AUTO, s
                                     y.stride(0), None if ws is None else _p(ws),
                                     0 if ws is None else ws.numel() * ws.element_size(), path, _s(stream)),
            "jetq_gemm_fprop_ws")
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20  # JETQ_NOALLOC_SCRATCH_BYTES
+
+
+def jetq_gemm_fprop_noalloc(qx, sx, qw, sw, n, d, c, y, stream=None):
+    """Rollout FProp (128-block recipe, decode path) that allocates nothing: the
+    split-K partial sums use a device array built into the library."""
+    _check(lib().jetq_gemm_fprop_noalloc(_p(qx), _p(sx), _p(qw), _p(sw), n, d, c, _p(y), _out_dtype(y),
+                                         y.stride(0), _s(stream)), "jetq_gemm_fprop_noalloc")
 
 
 def jetq_gemm_dgrad(recipe, qdy, sdy, qwt, swt, n, d, c, dx, stream=None):

@@ -503,6 +503,26 @@ jetq_status jetq_gemm_fprop_ws(jetq_recipe recipe, const uint8_t *qx, const void
     return fprop_impl(recipe, qx, sx, qw, sw, n, d, c, y, y_dtype, ldy, workspace, workspace_bytes, path, stream);
 }
 
+jetq_status jetq_gemm_fprop_noalloc(const uint8_t *qx, const float *sx, const uint8_t *qw, const float *sw, int64_t n,
+                                    int64_t d, int64_t c, void *y, jetq_out_dtype y_dtype, int64_t ldy, void *stream)
+{
+    JQ_REQUIRE(n >= 0 && d > 0 && c > 0, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(d % 128 == 0 && c % 128 == 0, JETQ_ERR_UNSUPPORTED_SHAPE);
+    jetq_status st = check_out(y, y_dtype, ldy, d);
+    if (st != JETQ_OK)
+        return st;
+    if (n == 0)
+        return JETQ_OK;
+    JQ_REQUIRE(qx && sx && qw && sw, JETQ_ERR_INVALID_ARG);
+    JQ_REQUIRE(aligned16(qx) && aligned16(qw) && aligned16(sx) && aligned16(sw), JETQ_ERR_MISALIGNED);
+    if ((st = check_arch()) != JETQ_OK)
+        return st;
+    // the built-in array must hold this shape's partial sums
+    JQ_REQUIRE(decode_split_workspace_bytes(n, d, c) <= decode_static_scratch_bytes(), JETQ_ERR_UNSUPPORTED_SHAPE);
+    GemmProblem g{qx, sx, qw, sw, n, d, c, c, c, BScale::Block128, y, ldy, y_dtype, 0};
+    return from_cuda(launch_gemm_decode_static(g, static_cast<cudaStream_t>(stream)));
+}
+
 jetq_status jetq_gemm_dgrad(jetq_recipe recipe, const uint8_t *qdy, const void *sdy, const uint8_t *qwt,
                             const void *swt, int64_t n, int64_t d, int64_t c, void *dx, jetq_out_dtype dx_dtype,
                             int64_t lddx, void *stream)

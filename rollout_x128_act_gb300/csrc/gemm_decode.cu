@@ -32,6 +32,8 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <mutex>
+
 #include "jetq_internal.h"
 #include "ptx.cuh"
 
@@ -818,6 +820,57 @@ cudaError_t launch_gemm_decode_swapped(const GemmProblem &g, cudaStream_t st)
     if (g.M <= 32)
         return run_decode<32, 3, 3, 9>(g, st);
     return run_decode<64, 3, 3, 6>(g, st);
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free split-K decode (jetq_gemm_fprop_noalloc): the partial sums
+// live in this file-scope device array instead of a caller's workspace.
+// Every GPU that loads the library holds it until the process exits; every
+// call shares it (overlapping calls race), and no element needs an initial
+// value (each call writes every partial it reads).
+namespace {
+constexpr size_t kStaticScratchBytes = JETQ_NOALLOC_SCRATCH_BYTES;
+constexpr int kStaticScratchDevices = 64;
+static __device__ __align__(256) float g_decode_static_scratch[kStaticScratchBytes / sizeof(float)];
+
+// The array's device address on the current device.  In host code the
+// array's name is only a host-side handle, so the address comes from
+// cudaGetSymbolAddress, once per device with that device current, cached.
+cudaError_t static_scratch_address(float **out)
+{
+    static std::mutex mu;
+    static float *addr[kStaticScratchDevices] = {};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess)
+        return e;
+    if (dev < 0 || dev >= kStaticScratchDevices)
+        return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        if ((e = cudaGetSymbolAddress(&p, g_decode_static_scratch)) != cudaSuccess)
+            return e;
+        addr[dev] = static_cast<float *>(p);
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+} // namespace
+
+size_t decode_static_scratch_bytes() { return kStaticScratchBytes; }
+
+cudaError_t launch_gemm_decode_static(GemmProblem g, cudaStream_t st)
+{
+    if (decode_split_workspace_bytes(g.M, g.N, g.K) > kStaticScratchBytes)
+        return cudaErrorInvalidValue;
+    float *scratch = nullptr;
+    cudaError_t e = static_scratch_address(&scratch);
+    if (e != cudaSuccess)
+        return e;
+    g.ws = scratch;
+    g.ws_bytes = kStaticScratchBytes;
+    return launch_gemm_block128(g, GemmShape::Decode, st);
 }
 
 cudaError_t gemm_decode_read_and_clear_error(cudaStream_t st, unsigned *out)

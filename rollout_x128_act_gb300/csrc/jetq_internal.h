@@ -170,6 +170,11 @@ bool gemm_decode_swapped_applies(const GemmProblem &g);
 // workspace): cluster size for a shape (1 = not used) and workspace bytes.
 int decode_split_factor(int64_t M, int64_t N, int64_t K);
 size_t decode_split_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// The same FProp with the partial sums in a device array built into the
+// library (no allocation; see jetq_gemm_fprop_noalloc): its size, and the
+// launch (cudaErrorInvalidValue when the shape needs more than the array).
+size_t decode_static_scratch_bytes();
+cudaError_t launch_gemm_decode_static(GemmProblem g, cudaStream_t st);
 cudaError_t launch_gemm_decode_swapped(const GemmProblem &g, cudaStream_t st);
 cudaError_t gemm_decode_read_and_clear_error(cudaStream_t st, unsigned *out);
 
