@@ -972,6 +972,7 @@ PROFILE_CASES = {
     "quant_w_pow2": "power-of-two 128x128 weight blocks + transposed copy, W 12288 x 12288 BF16",
     "amax_bf16": "max |x| over 131072 x 2048 BF16 (NVFP4 tensor scope)",
     "dequant_nvfp4": "BF16 dequantization of the NVFP4 copy of 131072 x 2048 (per-token scope)",
+    "decode_split": "split-K FProp 8 tokens x W_down 4096 x 12288 with a workspace (4 weight copies rotate: 201 MB)",
 }
 
 
@@ -1009,6 +1010,19 @@ def run_case(name: str, launches: int = 5):
             out = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
             fn = lambda: jq.jetq_gemm_fprop(jq.RECIPE_BLOCK128, ax["q_row"], ax["s_row"], qw, sw, n, d, c,  # noqa
                                             out, path)
+    elif name == "decode_split":
+        n, c, d = 8, 12288, 4096
+        ax = jq.quant_act(bf16(synth.activation(n, c, seed=0, stream="h")), col=False)
+        wq = [jq.quant_weight(bf16(synth.weight(d, c, seed=i, stream="w_down")), transposed=False) for i in range(4)]
+        out = torch.empty((n, d), dtype=torch.bfloat16, device=dev)
+        work = torch.empty(jq.jetq_decode_workspace_bytes(n, d, c), dtype=torch.uint8, device=dev)
+        turn = [0]
+
+        def fn():
+            qw, sw, _, _ = wq[turn[0] % 4]
+            turn[0] += 1
+            jq.jetq_gemm_fprop_ws(jq.RECIPE_BLOCK128, ax["q_row"], ax["s_row"], qw, sw, n, d, c, out, work,
+                                  jq.PATH_DECODE)
     elif name == "gemm_mx_fprop":
         n, c, d = 4096, 4096, 12288
         gx = jq.quant_mx(bf16(synth.activation(n, c, seed=0, stream="x")), col=False)
