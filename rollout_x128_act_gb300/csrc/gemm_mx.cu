@@ -207,34 +207,78 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
             ptx::mbar_wait(done, 0u, abort_flag, err, kErrTimeout, p.limit_ns, false);
         } else if (warp == 2 && gather_a) {
             // -------------------------------------------------- A scale gather (grouped rows)
-            // row a_row0 + i (i = lane + 32 j) of the tile -> byte lane * 16 + j * 4 of the atom
-            uint32_t it = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; t < num_tiles && ok; t += gridDim.x) {
-                const TileInfo ti = get_tile(sc, gt, t);
-                for (int kb = 0; kb < ti.num_kb; ++kb, ++it) {
-                    const int s = (int)(it % STAGES);
-                    const uint32_t ph = (it / STAGES) & 1u;
-                    const bool got = ptx::mbar_wait(empty(s), ph ^ 1u, abort_flag, err, kErrTimeout, p.limit_ns);
-                    if (!__all_sync(0xFFFFFFFFu, got)) {
-                        ok = false;
-                        break;
-                    }
-                    const int64_t kg = ti.kb0 + kb;
-                    uint32_t w[4];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int64_t r = (int64_t)ti.a_row0 + lane + 32 * j;
-                        w[j] = r < sc.M ? __ldg(reinterpret_cast<const uint32_t *>(
-                                              p.sfa + (kg * p.rba + (r >> 7)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4))
-                                        : 0u;
-                    }
-                    *reinterpret_cast<uint4 *>(sf + (size_t)s * C::kSfStage + lane * 16) = make_uint4(w[0], w[1], w[2], w[3]);
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); // visible to tcgen05.cp
-                    __syncwarp();
-                    if (lane == 0)
-                        ptx::mbar_arrive(full(s));
+            // row a_row0 + i (i = lane + 32 j) of the tile -> byte lane * 16 + j * 4 of the atom.
+            // The words of the next kGather K-blocks of the CTA's (tile, K-block)
+            // sequence are loaded while a group is stored, so the global-load
+            // latency is paid once per group.
+            constexpr int kGather = 4;
+            int ft = blockIdx.x, fkb = 0; // fetch cursor
+            TileInfo fti{};
+            bool fvalid = ft < num_tiles;
+            if (fvalid)
+                fti = get_tile(sc, gt, ft);
+            auto settle = [&]() { // skip to the next (tile, K-block) that exists
+                while (fvalid && fkb >= fti.num_kb) {
+                    ft += gridDim.x;
+                    fkb = 0;
+                    fvalid = ft < num_tiles;
+                    if (fvalid)
+                        fti = get_tile(sc, gt, ft);
                 }
+            };
+            auto fetch = [&](uint32_t (&w)[4]) {
+                settle();
+                if (!fvalid) {
+                    w[0] = w[1] = w[2] = w[3] = 0u;
+                    return;
+                }
+                const int64_t kg = fti.kb0 + fkb;
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int64_t r = (int64_t)fti.a_row0 + lane + 32 * j;
+                    w[j] = r < sc.M ? __ldg(reinterpret_cast<const uint32_t *>(
+                                          p.sfa + (kg * p.rba + (r >> 7)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4))
+                                    : 0u;
+                }
+                ++fkb;
+            };
+            uint32_t total = 0; // the CTA's K-blocks
+            for (int t = blockIdx.x; t < num_tiles; t += gridDim.x)
+                total += (uint32_t)get_tile(sc, gt, t).num_kb;
+            uint32_t cur[kGather][4];
+#pragma unroll
+            for (int u = 0; u < kGather; ++u)
+                fetch(cur[u]);
+            bool ok = true;
+            for (uint32_t it0 = 0; it0 < total && ok; it0 += kGather) {
+                uint32_t nxt[kGather][4];
+#pragma unroll
+                for (int u = 0; u < kGather; ++u)
+                    fetch(nxt[u]);
+#pragma unroll
+                for (int u = 0; u < kGather; ++u) {
+                    const uint32_t it = it0 + (uint32_t)u;
+                    if (it < total && ok) {
+                        const int s = (int)(it % STAGES);
+                        const uint32_t ph = (it / STAGES) & 1u;
+                        const bool got = ptx::mbar_wait(empty(s), ph ^ 1u, abort_flag, err, kErrTimeout, p.limit_ns);
+                        if (!__all_sync(0xFFFFFFFFu, got)) {
+                            ok = false;
+                        } else {
+                            *reinterpret_cast<uint4 *>(sf + (size_t)s * C::kSfStage + lane * 16) =
+                                make_uint4(cur[u][0], cur[u][1], cur[u][2], cur[u][3]);
+                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); // visible to tcgen05.cp
+                            __syncwarp();
+                            if (lane == 0)
+                                ptx::mbar_arrive(full(s));
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kGather; ++u)
+#pragma unroll
+                    for (int j = 0; j < 4; ++j)
+                        cur[u][j] = nxt[u][j];
             }
         }
         __syncwarp();
