@@ -185,6 +185,10 @@ __global__ void __launch_bounds__(256, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the prologue above overlaps the stream's previous kernel; global memory
+    // only after it has completed
+    ptx::grid_dep_launch();
+    ptx::grid_dep_wait();
 
     const int nkb = p.num_kb;
     const int spt = (nkb + KBP - 1) / KBP; // stages per tile
@@ -410,7 +414,18 @@ cudaError_t run_decode(const GemmProblem &g, cudaStream_t st)
     p.out_bf16 = g.out_dtype == JETQ_OUT_BF16;
     p.limit_ns = kWaitLimitNs;
     const int grid = p.tiles < sm_count() ? p.tiles : sm_count();
-    kern<<<grid, C::kThreads, C::kSmem, st>>>(tw, tx, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(C::kThreads);
+    cfg.dynamicSmemBytes = C::kSmem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization; // prologue overlaps the previous kernel
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if ((e = cudaLaunchKernelEx(&cfg, kern, tw, tx, p)) != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 
@@ -577,6 +592,10 @@ __global__ void __launch_bounds__(256, (SCfg<NB, S, STAGES, KBP, TMEM_BUFS>::kMi
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // the prologue above overlaps the stream's previous kernel; global memory
+    // (the workspace included) only after it has completed
+    ptx::grid_dep_launch();
+    ptx::grid_dep_wait();
 
     const int nch = (nkb + KBP - 1) / KBP; // chunks of the band
     const int last_nk = nkb - (nch - 1) * KBP;
@@ -755,13 +774,15 @@ cudaError_t run_decode_split(const GemmProblem &g, cudaStream_t st)
     cfg.blockDim = dim3(C::kThreads);
     cfg.dynamicSmemBytes = C::kSmem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = S;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization; // prologue overlaps the previous kernel
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     if ((e = cudaLaunchKernelEx(&cfg, kern, tw, tx, p, static_cast<float *>(g.ws))) != cudaSuccess)
         return e;
     return cudaGetLastError();

@@ -196,6 +196,21 @@ __device__ __forceinline__ void mbar_arrive_remote_cta(uint32_t cluster_addr)
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
 
+// Programmatic dependent launch.  grid_dep_wait: the executing thread waits
+// until the kernels this one may overlap (the stream's preceding kernel, when
+// the launch allowed it) have completed and their memory is visible; a no-op
+// otherwise.  grid_dep_launch: this CTA allows the stream's next kernel to
+// start (its own prologue; it waits in grid_dep_wait before touching memory).
+__device__ __forceinline__ void grid_dep_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dep_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // Named barrier `id` (1..15) over `count` threads (whole warps) of the CTA;
 // the threads of a warp may arrive apart (non-aligned form).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count)
