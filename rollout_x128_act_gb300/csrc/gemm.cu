@@ -215,6 +215,10 @@ __global__ void __launch_bounds__(128 + 32 * EPI_WARPS, 1)
         ptx::tmem_alloc(ptx::smem_addr(tmem_slot), C::kTmemCols);
         ptx::tmem_relinquish();
     }
+    // the prologue above overlaps the stream's previous kernel; global memory
+    // (the segment offsets included) only after it has completed
+    ptx::grid_dep_launch();
+    ptx::grid_dep_wait();
     if (warp == 3 && sc.mode != kDense)
         build_group_tables(sc, gt);
     ptx::tc_fence_before();
@@ -884,7 +888,8 @@ cudaError_t run(const GemmProblem &g, cudaStream_t st)
         const int tiles = s.mt * s.nt * g.num_experts;
         grid = tiles < grid ? tiles : grid;
     }
-    kern<<<grid, C::kThreads, C::kSmem, st>>>(ta, tbm, to, kp);
+    if ((e = launch_pdl(kern, dim3(grid), dim3(C::kThreads), C::kSmem, st, ta, tbm, to, kp)) != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 

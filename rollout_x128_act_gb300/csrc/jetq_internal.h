@@ -133,6 +133,27 @@ struct GemmProblem {
 
 enum class GemmShape : int { Train = 0, Decode = 1 };
 
+// Launch with programmatic stream serialization: the kernel's prologue may
+// overlap the stream's previous kernel (the kernel calls griddepcontrol.wait
+// before it touches global memory, and launch_dependents once its own
+// prologue is done).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                              Args &&...args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args &&>(args)...);
+}
+
 cudaError_t launch_gemm_block128(const GemmProblem &p, GemmShape shape, cudaStream_t st);
 
 // MXFP8 GEMM: both operands K-major E4M3 with E8M0 scale atoms (include/jetq.h

@@ -763,6 +763,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         ptx::fence_barrier_init();
     }
     __syncthreads();
+    // global memory only after the stream's previous kernel has completed (no
+    // early launch_dependents: the next kernel starts as these CTAs exit, which
+    // measured faster in a decode step than letting it in at once)
+    ptx::grid_dep_wait();
     if (warp == 0) {
         if (lane == 0)
             ptx::prefetch_tensormap(&tmx);
@@ -1032,6 +1036,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         ptx::fence_barrier_init();
     }
     __syncthreads();
+    // global memory only after the stream's previous kernel has completed (no
+    // early launch_dependents: the next kernel starts as these CTAs exit, which
+    // measured faster in a decode step than letting it in at once)
+    ptx::grid_dep_wait();
     if (t == 0) {
         ptx::prefetch_tensormap(&tmw);
         issue(0);
@@ -1700,7 +1708,9 @@ cudaError_t launch_quant_act_tma(const ActQuantArgs &a, const CUtensorMap &map, 
     }
     const int64_t tiles = ngroups * ncb;
     const int64_t cap = 2 * (int64_t)sm_count();
-    kern<<<(unsigned)(tiles < cap ? tiles : cap), kThreads, kPipeSmemBytes, st>>>(a, map, ngroups, ncb);
+    if ((e = launch_pdl(kern, dim3((unsigned)(tiles < cap ? tiles : cap)), dim3(kThreads), kPipeSmemBytes, st, a, map,
+                        ngroups, ncb)) != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 
@@ -1857,7 +1867,9 @@ cudaError_t launch_quant_weight(const WeightQuantArgs &a, cudaStream_t st)
         return e;
     const int64_t tiles = (a.d / 128) * (a.c / 128);
     const int64_t cap = 2 * (int64_t)sm_count();
-    k_quant_weight_tma<<<(unsigned)(tiles < cap ? tiles : cap), kThreads, kWPipeSmemBytes, st>>>(a, map);
+    if ((e = launch_pdl(k_quant_weight_tma, dim3((unsigned)(tiles < cap ? tiles : cap)), dim3(kThreads),
+                        kWPipeSmemBytes, st, a, map)) != cudaSuccess)
+        return e;
     return cudaGetLastError();
 }
 
