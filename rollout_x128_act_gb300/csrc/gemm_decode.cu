@@ -18,16 +18,21 @@
 //   warp 1      MMA issuer: per K-block 4 x tcgen05.mma (K = 32) into its own
 //               TMEM buffer; one commit per stage releases the smem stage
 //               and hands the stage's buffer group to the epilogue
-//   warp 2      scale producer: per K-block the NB products fl32(Sx * Sw)
-//               into a shared-memory ring
+//   warp 2      scale producer: the NB products fl32(Sx * Sw) of each
+//               K-block into a shared-memory ring, eight K-blocks a slot
 //   warps 4-7   epilogue: per K-block tcgen05.ld the partial (TMEM lanes =
 //               weight rows, columns = tokens), acc = fma(P, s, acc); after
 //               the last K-block, store y[t, o] for t < n (coalesced along o)
 //
-// One CTA per SM, persistent over 128-row weight tiles.  Every mbarrier wait
-// is bounded; a CTA that gives up raises its abort flag, records the error
-// in the device error word, drains its TMA copies and MMAs (bounded) and
-// frees its TMEM.
+// One CTA per SM, persistent over 128-row weight tiles.  Weights with few
+// row bands (the down projection has 32) leave most SMs idle that way; with
+// a caller's workspace they take the split-K kernel further down (a cluster
+// of CTAs per band, partial sums through the workspace, the same fold).
+// Both kernels are launched so that their prologue overlaps the stream's
+// previous kernel (programmatic dependent launch) and wait for it before
+// touching global memory.  Every mbarrier wait is bounded; a CTA that gives
+// up raises its abort flag, records the error in the device error word,
+// drains its TMA copies and MMAs (bounded) and frees its TMEM.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
