@@ -973,6 +973,7 @@ PROFILE_CASES = {
     "amax_bf16": "max |x| over 131072 x 2048 BF16 (NVFP4 tensor scope)",
     "dequant_nvfp4": "BF16 dequantization of the NVFP4 copy of 131072 x 2048 (per-token scope)",
     "decode_split": "split-K FProp 8 tokens x W_down 4096 x 12288 with a workspace (4 weight copies rotate: 201 MB)",
+    "grouped_mx_fprop": "MXFP8 grouped FProp, 32 experts x 1536 x 2048, 16384 routed rows (Zipf 1.2), BF16 out",
 }
 
 
@@ -1041,6 +1042,18 @@ def run_case(name: str, launches: int = 5):
         qw, sw = torch.stack([q[0] for q in qs]), torch.stack([q[1] for q in qs])
         out = torch.empty((R, d), dtype=torch.bfloat16, device=dev)
         fn = lambda: jq.grouped(jq.GEMM_FPROP, ax["q_row"], ax["s_row"], qw, sw, seg, n=d, k=c, out=out)  # noqa
+    elif name == "grouped_mx_fprop":
+        E, c, d = 32, 2048, 1536
+        off, _ = synth.zipf_topk_routing(2048, E, 8, 1.2, seed=0)
+        R = int(off[-1])
+        seg = torch.tensor(off, dtype=torch.int64, device=dev)
+        gx = jq.quant_mx(bf16(synth.activation(R, c, seed=0, stream="x")), col=False, seg_offsets=seg)
+        ws = bf16(synth.weight(E * d, c, seed=0, stream="w_gate"))
+        gws = [jq.quant_mx(ws[e * d:(e + 1) * d], col=False) for e in range(E)]
+        qw, ew = torch.stack([g["q_row"] for g in gws]), torch.cat([g["e8_row"] for g in gws])
+        out = torch.empty((R, d), dtype=torch.bfloat16, device=dev)
+        fn = lambda: jq.grouped(jq.GEMM_FPROP, gx["q_row"], gx["e8_row"], qw, ew, seg, n=d, k=c, out=out,  # noqa
+                                recipe=jq.RECIPE_MXFP8)
     elif name in ("requant_col", "dequant_bf16"):
         a = jq.quant_act(bf16(synth.activation(8192, 12288, seed=0, stream="h")), col=False)
         if name == "requant_col":
