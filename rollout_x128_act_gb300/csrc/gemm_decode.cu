@@ -836,7 +836,7 @@ cudaError_t launch_gemm_decode_swapped(const GemmProblem &g, cudaStream_t st)
     if (g.ws && g.ws_bytes >= decode_split_workspace_bytes(g.M, g.N, g.K)) {
         const int S = decode_split_factor(g.M, g.N, g.K);
         if (S == 4)
-            return g.M <= 16 ? run_decode_split<16, 4, 4, 2, 16>(g, st) : run_decode_split<32, 4, 3, 2, 16>(g, st);
+            return g.M <= 16 ? run_decode_split<16, 4, 4, 2, 16>(g, st) : run_decode_split<32, 4, 4, 2, 16>(g, st);
         if (S == 2) // two CTAs fit on an SM (shared memory, TMEM and registers)
             return g.M <= 16 ? run_decode_split<16, 2, 3, 2, 16>(g, st) : run_decode_split<32, 2, 2, 2, 8>(g, st);
     }
