@@ -152,3 +152,20 @@ def test_validation_happens_before_cuda(L):
     assert L.jetq_amax_bf16(fake, 4, 12, 12, fake, None) == 2
     # MX: columns not a multiple of 128
     assert L.jetq_quant_mx32(fake, 4, 96, 96, fake, fake, None, None, 0, None, 0, None) == 2
+    # FProp with a workspace: misaligned workspace; D not a multiple of 128
+    assert L.jetq_gemm_fprop_ws(0, fake, fake, fake, fake, 8, 128, 128, fake, 0, 128, P(4100), 1024, 2, None) == 3
+    assert L.jetq_gemm_fprop_ws(0, fake, fake, fake, fake, 8, 100, 128, fake, 0, 128, fake, 1024, 2, None) == 2
+    # allocation-free FProp: D not a multiple of 128; negative batch
+    assert L.jetq_gemm_fprop_noalloc(fake, fake, fake, fake, 8, 100, 128, fake, 0, 128, None) == 2
+    assert L.jetq_gemm_fprop_noalloc(fake, fake, fake, fake, -1, 128, 128, fake, 0, 128, None) == 1
+
+
+def test_decode_workspace_size_is_zero_without_the_device(L):
+    """The size query needs the GB300 (its SM count picks the split): on any other
+    device, or none, it reports that no workspace is used."""
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    assert L.jetq_decode_workspace_bytes(1, 4096, 12288) == 0
+    assert L.jetq_decode_workspace_bytes(0, 4096, 12288) == 0
