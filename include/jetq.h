@@ -423,8 +423,8 @@ JETQ_API jetq_status jetq_gemm_fprop_ws(jetq_recipe recipe,
                             jetq_path path, void *stream);
 
 /*
- * Rollout FProp that allocates nothing (BLOCK128, the decode path).  No
- * counterpart in the pages: this is a library convenience.  Some callers
+ * Rollout FProp that allocates nothing (BLOCK128, the decode path).  The
+ * paper has no counterpart to it: it is a library convenience.  Some callers
  * cannot hand out device memory for a workspace: a framework whose caching
  * allocator must own every device allocation, a serving loop that cannot
  * afford the device-wide synchronization of cudaMalloc/cudaFree, or a host
